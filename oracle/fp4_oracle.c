@@ -1,0 +1,513 @@
+/*
+ * fp4_oracle.c -- the CPU oracle for the block-scaled FP4 quantizer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, scalar, obviously-correct
+ * statement of what the quantizer computes.  Only the test-suite, the smoke
+ * check and the CPU-baseline leg of the benchmark load it.  It shares no
+ * code, header, table or constant generator with the CUDA library.
+ *
+ * Build: plain C99, IEEE binary32 arithmetic, no FMA contraction
+ * (-ffp-contract=off), no fast-math, subnormals preserved.  Every
+ * arithmetic step of the method written below as a `float` expression is one
+ * binary32 round-to-nearest-even operation; `double` is used only where the
+ * step is exact (comparisons, grid distances, power-of-two scalings).
+ *
+ * Sources (pages of the block-scaled FP4 quantizer study):
+ *   [ALTO]   "NVFP4 / AMD-FP4 outer-block (two-level) scaling for FP4 training",
+ *            sections "Background", "Technical design" (scale levels 1-3 and
+ *            key properties), "Implementation" (quantization core).
+ *   [FP4T]   "fp4-train" README, sections "Method", "API", "Correctness",
+ *            "Requirements and limits".
+ *   [TEQAT]  "MXFP4 weight QAT recipes on MXFP8 and FP8 block-scaling hosts",
+ *            sections "Overview", "Design", "Implementations", "Correctness",
+ *            "Known limitations".
+ *   [BLOG]   "Block-Scaled FP8 and FP4 Weight Quantization", sections 3-8.
+ *
+ * Parity status of each entry point is stated beside it; where a step is a
+ * reading of silent or garbled text, the comment says which reading.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BF16 1
+#define ORC_FP32 2
+
+#define ORC_MODE_NONE 0
+#define ORC_MODE_TENSORWISE 1
+#define ORC_MODE_OUTER 2
+
+#define ORC_FMT_E4M3 0
+#define ORC_FMT_UE5M3 1
+
+#define ORC_RNE 0
+#define ORC_SR 1
+
+#define ORC_ROW 1
+#define ORC_COL 2
+
+/* Configuration of one oracle call (independent of the library's own struct). */
+typedef struct {
+  int64_t G, M, K, ld;       /* logical [G,M,K]; input row stride ld >= K   */
+  int32_t in_dtype;          /* ORC_BF16 | ORC_FP32                         */
+  int32_t out_dtype;         /* dequant / qdq output dtype                   */
+  int32_t mode;              /* ORC_MODE_*                                   */
+  int32_t ob;                /* outer block size (outer mode only)           */
+  int32_t outer_2d;          /* 0: 1 x ob, 1: ob x ob                         */
+  int32_t inner_2d;          /* 0: 1 x 16, 1: 16 x 16                         */
+  int32_t fmt;               /* ORC_FMT_*                                    */
+  int32_t rounding;          /* ORC_RNE | ORC_SR                              */
+  uint64_t seed;
+  uint32_t step;
+  uint32_t out_mask;         /* ORC_ROW | ORC_COL                              */
+  int32_t use_precomputed;   /* read outer scales instead of computing them  */
+} orc_cfg;
+
+/* ------------------------------------------------------------------------ */
+/* bf16 <-> binary32                                                          */
+/* ------------------------------------------------------------------------ */
+
+static float bits_to_f32(uint32_t b) { float f; memcpy(&f, &b, 4); return f; }
+static uint32_t f32_to_bits(float f) { uint32_t b; memcpy(&b, &f, 4); return b; }
+
+float orc_bf16_to_f32(uint16_t h) { return bits_to_f32((uint32_t)h << 16); }
+
+/* Round a binary32 value to the nearest bfloat16, ties to even (NaN -> the
+ * canonical quiet NaN 0x7FC0). */
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t b = f32_to_bits(f);
+  if (isnan(f)) return 0x7FC0;
+  uint32_t lsb = (b >> 16) & 1u;
+  return (uint16_t)((b + 0x7FFFu + lsb) >> 16);
+}
+
+static float load_in(const void *x, int32_t dtype, int64_t idx) {
+  if (dtype == ORC_BF16) return orc_bf16_to_f32(((const uint16_t *)x)[idx]);
+  return ((const float *)x)[idx];
+}
+
+static void store_out(void *y, int32_t dtype, int64_t idx, float v) {
+  if (dtype == ORC_BF16) ((uint16_t *)y)[idx] = orc_f32_to_bf16(v);
+  else ((float *)y)[idx] = v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* E2M1 values: the grid {0, .5, 1, 1.5, 2, 3, 4, 6} with a sign bit           */
+/* ([FP4T] "Method"; the 3-bit magnitude index is the code's low bits).        */
+/* ------------------------------------------------------------------------ */
+
+static const double E2M1_GRID[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1_decode(uint8_t code) {
+  double m = E2M1_GRID[code & 7];
+  return (code & 8) ? -m : m;
+}
+
+/* Nearest grid point, ties to the even code, |t| beyond 6 saturates to 6,
+ * sign bit kept (so -0.1 gives code 0x8).  Brute force over the 8 points. */
+uint8_t orc_e2m1_rne(double t) {
+  uint8_t sign = signbit(t) ? 8 : 0;
+  double a = fabs(t);
+  if (a >= 6.0) return (uint8_t)(sign | 7); /* satfinite */
+  int best = 0;
+  double bestd = a;
+  for (int k = 1; k < 8; k++) {
+    double d = fabs(a - E2M1_GRID[k]);
+    if (d < bestd || (d == bestd && (k % 2) == 0)) { best = k; bestd = d; }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* Stochastic rounding ([FP4T] "Method": the higher neighbour is chosen with
+ * probability equal to the fractional distance).  The uniform draw is the top
+ * 24 bits of the 32-bit random word w; round up iff draw < f * 2^24. */
+uint8_t orc_e2m1_sr(double t, uint32_t w) {
+  uint8_t sign = signbit(t) ? 8 : 0;
+  double a = fabs(t);
+  int k;
+  if (a >= 6.0) {
+    k = 7;
+  } else {
+    int lo = 0;
+    while (lo < 7 && E2M1_GRID[lo + 1] <= a) lo++;
+    double f = (a - E2M1_GRID[lo]) / (E2M1_GRID[lo + 1] - E2M1_GRID[lo]);
+    k = ((double)(w >> 8) < f * 16777216.0) ? lo + 1 : lo;
+  }
+  return (uint8_t)(sign | k);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Inner-scale formats.  E4M3 (NVFP4, max 448) and UE5M3 (AMD-FP4, max       */
+/* 114688) from [ALTO] "Technical design" item 1.  Byte c = eeee(e)mmm:      */
+/*   e == 0: m * 2^(1-bias-3)   (subnormal)                                   */
+/*   e  > 0: (8+m) * 2^(e-bias-3)                                              */
+/* E4M3: bias 7, codes 0x00..0x7E (0x7F is NaN).  UE5M3: the unsigned 5-bit-  */
+/* exponent/3-bit-mantissa format whose largest finite value is 114688:       */
+/* bias 15, codes 0x00..0xFE (0xFF is NaN).                                   */
+/* ------------------------------------------------------------------------ */
+
+static int fmt_bias(int fmt) { return fmt == ORC_FMT_E4M3 ? 7 : 15; }
+static int fmt_maxcode(int fmt) { return fmt == ORC_FMT_E4M3 ? 0x7E : 0xFE; }
+
+double orc_scale_decode(int fmt, uint8_t c) {
+  int bias = fmt_bias(fmt);
+  int e = c >> 3, m = c & 7;
+  if (e == 0) return ldexp((double)m, 1 - bias - 3);
+  return ldexp((double)(8 + m), e - bias - 3);
+}
+
+/* Nearest representable scale, ties to the even code, values above the
+ * largest finite one saturate to it (satfinite).  v >= 0 and finite. */
+uint8_t orc_scale_encode(int fmt, float v) {
+  int maxc = fmt_maxcode(fmt);
+  double dv = (double)v;
+  if (dv >= orc_scale_decode(fmt, (uint8_t)maxc)) return (uint8_t)maxc;
+  /* binary search: largest code lo with value <= dv (code 0 is 0.0) */
+  int lo = 0, hi = maxc;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (orc_scale_decode(fmt, (uint8_t)mid) <= dv) lo = mid; else hi = mid;
+  }
+  /* now value(lo) <= dv < value(lo+1) */
+  double dlo = dv - orc_scale_decode(fmt, (uint8_t)lo);
+  double dhi = orc_scale_decode(fmt, (uint8_t)(lo + 1)) - dv;
+  if (dlo < dhi) return (uint8_t)lo;
+  if (dhi < dlo) return (uint8_t)(lo + 1);
+  return (uint8_t)((lo % 2 == 0) ? lo : lo + 1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as  */
+/* easy as 1, 2, 3", SC'11): ten rounds of the 4x32 multiply-xor bijection, */
+/* the key advanced by the Weyl constants between rounds.                    */
+/* ------------------------------------------------------------------------ */
+
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+  uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; round++) {
+    if (round > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+    uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+    uint32_t n1 = (uint32_t)p1;
+    uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+    uint32_t n3 = (uint32_t)p0;
+    c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+  }
+  memcpy(out, c, sizeof c);
+}
+
+/* The 32-bit random word of element n (flat index in its orientation's
+ * logical tensor) for stochastic rounding: the (seed, step, global-index)
+ * counter RNG of [FP4T] "Method".  One Philox call yields the words of four
+ * consecutive elements; `orient` separates the rowwise and columnwise
+ * streams. */
+uint32_t orc_sr_word(uint64_t seed, uint32_t step, uint32_t orient, uint64_t n) {
+  uint64_t blk = n >> 2;
+  uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), step, orient};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return out[n & 3];
+}
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 / AMD-FP4 quantization                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Reading of "NaN-input sanitization" ([ALTO] "Op-level test coverage"):
+ * NaN -> +0 and +-inf -> +- the largest finite value of the input dtype. */
+static float sanitize(float u, int32_t in_dtype) {
+  if (isnan(u)) return 0.0f;
+  if (isinf(u)) {
+    float mx = (in_dtype == ORC_BF16) ? bits_to_f32(0x7F7F0000u) : bits_to_f32(0x7F7FFFFFu);
+    return u > 0 ? mx : -mx;
+  }
+  return u;
+}
+
+/* amax / (scale_max * 6) with scale_max = 448 (E4M3) or 114688 (UE5M3):
+ * [ALTO] "Technical design" item 1.  The denominator is exact in binary32;
+ * the quotient is one binary32 division ("held in FP32, no grid rounding"). */
+static float outer_scale(float amax, int fmt) {
+  float denom = (fmt == ORC_FMT_E4M3) ? 2688.0f : 688128.0f;
+  return amax / denom;
+}
+
+/* Element of the orientation's logical tensor: o = row -> u[g][r][c];
+ * o = col -> u[g][c][r] (the columnwise tensor is x transposed). */
+static int64_t u_index(const orc_cfg *cf, int o, int64_t g, int64_t r, int64_t c) {
+  return (o == ORC_ROW) ? (g * cf->M + r) * cf->K + c : (g * cf->M + c) * cf->K + r;
+}
+
+/* Outer scale applying to element (g, r, c) of orientation o. */
+static float outer_of(const orc_cfg *cf, int o, int64_t g, int64_t r, int64_t c,
+                      const float *S_row, const float *S_col, const float *S_tile) {
+  if (cf->mode == ORC_MODE_NONE) return 1.0f;
+  if (cf->mode == ORC_MODE_TENSORWISE) return S_tile[0];
+  int64_t ob = cf->ob;
+  if (cf->outer_2d) {
+    /* one scale per ob x ob tile of x, shared by both orientations */
+    int64_t i = (o == ORC_ROW) ? r : c, j = (o == ORC_ROW) ? c : r;
+    return S_tile[(g * (cf->M / ob) + i / ob) * (cf->K / ob) + j / ob];
+  }
+  if (o == ORC_ROW) return S_row[(g * cf->M + r) * (cf->K / ob) + c / ob];
+  return S_col[(g * cf->K + r) * (cf->M / ob) + c / ob];
+}
+
+/* Compute the outer scales from u (sanitized, error-feedback-corrected input,
+ * stored [G,M,K] contiguous). */
+static void compute_outer(const orc_cfg *cf, const float *u, float *S_row, float *S_col, float *S_tile) {
+  int64_t G = cf->G, M = cf->M, K = cf->K, ob = cf->ob;
+  if (cf->mode == ORC_MODE_TENSORWISE) {
+    float A = 0.0f;
+    for (int64_t n = 0; n < G * M * K; n++) A = fmaxf(A, fabsf(u[n]));
+    S_tile[0] = outer_scale(A, cf->fmt);
+    return;
+  }
+  if (cf->mode != ORC_MODE_OUTER) return;
+  if (cf->outer_2d) {
+    for (int64_t g = 0; g < G; g++)
+      for (int64_t bi = 0; bi < M / ob; bi++)
+        for (int64_t bj = 0; bj < K / ob; bj++) {
+          float A = 0.0f;
+          for (int64_t i = bi * ob; i < (bi + 1) * ob; i++)
+            for (int64_t j = bj * ob; j < (bj + 1) * ob; j++)
+              A = fmaxf(A, fabsf(u[(g * M + i) * K + j]));
+          S_tile[(g * (M / ob) + bi) * (K / ob) + bj] = outer_scale(A, cf->fmt);
+        }
+    return;
+  }
+  if ((cf->out_mask & ORC_ROW) && S_row)
+    for (int64_t g = 0; g < G; g++)
+      for (int64_t i = 0; i < M; i++)
+        for (int64_t bj = 0; bj < K / ob; bj++) {
+          float A = 0.0f;
+          for (int64_t j = bj * ob; j < (bj + 1) * ob; j++) A = fmaxf(A, fabsf(u[(g * M + i) * K + j]));
+          S_row[(g * M + i) * (K / ob) + bj] = outer_scale(A, cf->fmt);
+        }
+  if ((cf->out_mask & ORC_COL) && S_col)
+    for (int64_t g = 0; g < G; g++)
+      for (int64_t j = 0; j < K; j++)
+        for (int64_t bi = 0; bi < M / ob; bi++) {
+          float A = 0.0f;
+          for (int64_t i = bi * ob; i < (bi + 1) * ob; i++) A = fmaxf(A, fabsf(u[(g * M + i) * K + j]));
+          S_col[(g * K + j) * (M / ob) + bi] = outer_scale(A, cf->fmt);
+        }
+}
+
+/* Quantize one orientation o of u.  R x C is the orientation's logical shape
+ * ([M,K] rowwise, [K,M] columnwise).  Steps, per [ALTO] "Implementation" and
+ * [FP4T] "Method":
+ *   x' = u / S                      (normalize by the outer scale; S == 0 -> +-0)
+ *   a  = max |x'| over the inner block (1x16, or 16x16 with inner_2d)
+ *   sc = ENC(a / 6), s = DEC(sc)    (inner scale on the E4M3 / UE5M3 grid)
+ *   t  = x' / s                     (s == 0 -> +-0)
+ *   q  = RNE or SR of t onto E2M1
+ * codes pack two per byte, the even column in the low nibble. deq (for error
+ * feedback and QDQ) is ((e2m1(q) * s) * S) in binary32.
+ * The 16x16 inner scale is stored once per 1x16 microblock (replicated). */
+static void quantize_orientation(const orc_cfg *cf, int o, const float *u,
+                                 const float *S_row, const float *S_col, const float *S_tile,
+                                 uint8_t *codes, uint8_t *scales, float *deq_out /* [R,C] or NULL */) {
+  int64_t G = cf->G;
+  int64_t R = (o == ORC_ROW) ? cf->M : cf->K;
+  int64_t C = (o == ORC_ROW) ? cf->K : cf->M;
+  int64_t bh = cf->inner_2d ? 16 : 1; /* inner block height in this orientation */
+  float *xp = (float *)malloc(sizeof(float) * (size_t)(bh * 16));
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t r0 = 0; r0 < R; r0 += bh)
+      for (int64_t c0 = 0; c0 < C; c0 += 16) {
+        /* normalize the block and take its amax */
+        float a = 0.0f;
+        for (int64_t dr = 0; dr < bh; dr++)
+          for (int64_t dc = 0; dc < 16; dc++) {
+            int64_t r = r0 + dr, c = c0 + dc;
+            float uv = u[u_index(cf, o, g, r, c)];
+            float S = outer_of(cf, o, g, r, c, S_row, S_col, S_tile);
+            float v = (S > 0.0f) ? uv / S : copysignf(0.0f, uv);
+            xp[dr * 16 + dc] = v;
+            a = fmaxf(a, fabsf(v));
+          }
+        float vsc = a / 6.0f;
+        uint8_t sc = orc_scale_encode(cf->fmt, vsc);
+        float s = (float)orc_scale_decode(cf->fmt, sc);
+        for (int64_t dr = 0; dr < bh; dr++) {
+          int64_t r = r0 + dr;
+          scales[(g * R + r) * (C / 16) + c0 / 16] = sc;
+          for (int64_t dc = 0; dc < 16; dc++) {
+            int64_t c = c0 + dc;
+            float v = xp[dr * 16 + dc];
+            float t = (s > 0.0f) ? v / s : copysignf(0.0f, v);
+            uint8_t q;
+            if (cf->rounding == ORC_SR) {
+              uint64_t n = (uint64_t)((g * R + r) * C + c);
+              q = orc_e2m1_sr((double)t, orc_sr_word(cf->seed, cf->step, o == ORC_ROW ? 0u : 1u, n));
+            } else {
+              q = orc_e2m1_rne((double)t);
+            }
+            int64_t byte = (g * R + r) * (C / 2) + c / 2;
+            if ((c & 1) == 0) codes[byte] = (uint8_t)(q & 0xF);
+            else codes[byte] = (uint8_t)(codes[byte] | (q << 4));
+            if (deq_out) {
+              float S = outer_of(cf, o, g, r, c, S_row, S_col, S_tile);
+              float qs = (float)orc_e2m1_decode(q) * s;
+              deq_out[(g * R + r) * C + c] = qs * S;
+            }
+          }
+        }
+      }
+  free(xp);
+}
+
+/* u = sanitize(x (+ r)) as a contiguous [G,M,K] binary32 array. The error
+ * feedback input is "added into the next quantization" ([FP4T] "Method"). */
+static float *build_u(const orc_cfg *cf, const void *x, const float *residual) {
+  int64_t G = cf->G, M = cf->M, K = cf->K;
+  float *u = (float *)malloc(sizeof(float) * (size_t)(G * M * K));
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t i = 0; i < M; i++)
+      for (int64_t j = 0; j < K; j++) {
+        float xv = load_in(x, cf->in_dtype, (g * M + i) * cf->ld + j);
+        int64_t n = (g * M + i) * K + j;
+        float v = residual ? xv + residual[n] : xv;
+        u[n] = sanitize(v, cf->in_dtype);
+      }
+  return u;
+}
+
+/* Quantize x into the requested orientations.  Outer-scale buffers:
+ * S_row [G,M,K/ob] (1-D rowwise), S_col [G,K,M/ob] (1-D columnwise),
+ * S_tile [G,M/ob,K/ob] (2-D, shared) or [1] (tensorwise).  With
+ * use_precomputed the scales are read from those buffers instead.  The
+ * residual (rowwise only) is replaced by u - deq.  Returns 0. */
+int orc_quantize(const orc_cfg *cf, const void *x, float *residual,
+                 uint8_t *row_codes, uint8_t *row_scales, float *S_row,
+                 uint8_t *col_codes, uint8_t *col_scales, float *S_col, float *S_tile) {
+  int64_t n_el = cf->G * cf->M * cf->K;
+  float *u = build_u(cf, x, residual);
+  if (!cf->use_precomputed) compute_outer(cf, u, S_row, S_col, S_tile);
+  if (cf->out_mask & ORC_ROW) {
+    float *deq = residual ? (float *)malloc(sizeof(float) * (size_t)n_el) : NULL;
+    quantize_orientation(cf, ORC_ROW, u, S_row, S_col, S_tile, row_codes, row_scales, deq);
+    if (residual) {
+      /* r <- u - dequant(quantize(u))  ([FP4T] "Method", error feedback) */
+      for (int64_t n = 0; n < n_el; n++) residual[n] = u[n] - deq[n];
+      free(deq);
+    }
+  }
+  if (cf->out_mask & ORC_COL)
+    quantize_orientation(cf, ORC_COL, u, S_row, S_col, S_tile, col_codes, col_scales, NULL);
+  free(u);
+  return 0;
+}
+
+/* Dequantize one orientation's buffers ([FP4T] "API": dequantize(packed,
+ * scale, M, K)): y = OUT((e2m1(q) * s) * S), binary32 products, then
+ * round-to-nearest-even to the output dtype.  orient selects the outer-scale
+ * indexing; y is [G,R,C] contiguous. */
+int orc_dequantize(const orc_cfg *cf, int orient, const uint8_t *codes, const uint8_t *scales,
+                   const float *S_row, const float *S_col, const float *S_tile, void *y) {
+  int64_t G = cf->G;
+  int64_t R = (orient == ORC_ROW) ? cf->M : cf->K;
+  int64_t C = (orient == ORC_ROW) ? cf->K : cf->M;
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t r = 0; r < R; r++)
+      for (int64_t c = 0; c < C; c++) {
+        uint8_t byte = codes[(g * R + r) * (C / 2) + c / 2];
+        uint8_t q = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+        float s = (float)orc_scale_decode(cf->fmt, scales[(g * R + r) * (C / 16) + c / 16]);
+        float S = outer_of(cf, orient, g, r, c, S_row, S_col, S_tile);
+        float qs = (float)orc_e2m1_decode(q) * s;
+        store_out(y, cf->out_dtype, (g * R + r) * C + c, qs * S);
+      }
+  return 0;
+}
+
+/* QDQ ([FP4T] "API": quantize then dequantize; [ALTO] "Implementation": the
+ * _qdq axis).  orient = ORC_ROW quantizes along K (axis -1), ORC_COL along M
+ * (axis 0); y is always in x's [G,M,K] layout (contiguous).  The outer
+ * scales are written to (or, with use_precomputed, read from) the buffers. */
+int orc_qdq(const orc_cfg *cf, int orient, const void *x, void *y, float *residual,
+            float *S_row, float *S_col, float *S_tile) {
+  int64_t G = cf->G, M = cf->M, K = cf->K;
+  int64_t n_el = G * M * K;
+  orc_cfg c2 = *cf;
+  c2.out_mask = (uint32_t)orient;
+  float *u = build_u(&c2, x, residual);
+  if (!c2.use_precomputed) compute_outer(&c2, u, S_row, S_col, S_tile);
+  int64_t R = (orient == ORC_ROW) ? M : K, C = (orient == ORC_ROW) ? K : M;
+  uint8_t *codes = (uint8_t *)calloc((size_t)(G * R * C / 2), 1);
+  uint8_t *scales = (uint8_t *)calloc((size_t)(G * R * C / 16), 1);
+  float *deq = (float *)malloc(sizeof(float) * (size_t)n_el);
+  quantize_orientation(&c2, orient, u, S_row, S_col, S_tile, codes, scales, deq);
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t i = 0; i < M; i++)
+      for (int64_t j = 0; j < K; j++) {
+        int64_t n = (g * M + i) * K + j;
+        float d = (orient == ORC_ROW) ? deq[n] : deq[(g * K + j) * M + i];
+        store_out(y, cf->out_dtype, n, d);
+        if (residual) residual[n] = u[n] - d;
+      }
+  free(codes); free(scales); free(deq); free(u);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* MXFP4 fake-quantize ([TEQAT] "Overview", "Design", "Correctness",        */
+/* "Known limitations"): per 1x32 block along K                              */
+/*   A  = max |x|; any inf/NaN in the block -> every output is NaN           */
+/*   Ac = max(A, 6 * 2^-126)                 (deployment clamp)              */
+/*   E  = smallest integer with 6 * 2^E >= Ac, clamped to [-126, 125]        */
+/*   y  = e2m1_rne(x * 2^-E) * 2^E           (exact in bf16 and binary32)    */
+/* The scale is the power of two 2^E (a UE8M0 code E + 127).                 */
+/* ------------------------------------------------------------------------ */
+
+/* The power-of-two exponent E of a block with absolute maximum A (finite). */
+int orc_mxfp4_exponent(double A) {
+  double Ac = A > ldexp(6.0, -126) ? A : ldexp(6.0, -126);
+  int e = -130;
+  while (ldexp(6.0, e) < Ac) e++;   /* exact comparisons in double */
+  if (e < -126) e = -126;
+  if (e > 125) e = 125;
+  return e;
+}
+
+int orc_mxfp4_fake_quantize(const orc_cfg *cf, const void *x, void *y) {
+  int64_t G = cf->G, M = cf->M, K = cf->K;
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t i = 0; i < M; i++)
+      for (int64_t j0 = 0; j0 < K; j0 += 32) {
+        double A = 0.0;
+        int poisoned = 0;
+        for (int64_t j = j0; j < j0 + 32; j++) {
+          double v = (double)load_in(x, cf->in_dtype, (g * M + i) * cf->ld + j);
+          if (!isfinite(v)) poisoned = 1;
+          else if (fabs(v) > A) A = fabs(v);
+        }
+        int E = orc_mxfp4_exponent(A);
+        for (int64_t j = j0; j < j0 + 32; j++) {
+          int64_t n = (g * M + i) * K + j;
+          if (poisoned) {
+            if (cf->out_dtype == ORC_BF16) ((uint16_t *)y)[n] = 0x7FC0;
+            else ((uint32_t *)y)[n] = 0x7FC00000u;
+            continue;
+          }
+          double v = (double)load_in(x, cf->in_dtype, (g * M + i) * cf->ld + j);
+          uint8_t q = orc_e2m1_rne(ldexp(v, -E));
+          double out = ldexp(orc_e2m1_decode(q), E);
+          store_out(y, cf->out_dtype, n, (float)out);
+        }
+      }
+  return 0;
+}
+
+/* Startup check used by the tests: subnormals survive a multiply (no
+ * flush-to-zero in this process). */
+int orc_subnormals_ok(void) {
+  volatile float a = ldexpf(1.0f, -126), b = 0.5f;
+  float c = a * b;
+  return c == ldexpf(1.0f, -127);
+}
