@@ -63,6 +63,7 @@ class Cfg(ctypes.Structure):
         ("ob", ctypes.c_int32), ("outer_2d", ctypes.c_int32), ("inner_2d", ctypes.c_int32),
         ("fmt", ctypes.c_int32), ("rounding", ctypes.c_int32), ("seed", ctypes.c_uint64),
         ("step", ctypes.c_uint32), ("out_mask", ctypes.c_uint32), ("use_precomputed", ctypes.c_int32),
+        ("sr_index_base", ctypes.c_int64),
     ]
 
 
@@ -133,7 +134,8 @@ def _as3d(x):
 
 
 def make_cfg(x, K=None, *, mode="none", ob=0, outer_2d=False, inner_2d=False, fmt="e4m3",
-             rounding="rne", seed=0, step=0, out_mask=ROW, use_precomputed=False, out_dtype=None):
+             rounding="rne", seed=0, step=0, out_mask=ROW, use_precomputed=False, out_dtype=None,
+             sr_index_base=0):
     G, M, ld = x.shape
     K = ld if K is None else K
     in_code = _dtype_code(x)
@@ -141,7 +143,7 @@ def make_cfg(x, K=None, *, mode="none", ob=0, outer_2d=False, inner_2d=False, fm
     return Cfg(G, M, K, ld, in_code, out_code, _MODES[mode] if isinstance(mode, str) else mode, ob,
                int(outer_2d), int(inner_2d), _FMTS[fmt] if isinstance(fmt, str) else fmt,
                {"rne": RNE, "sr": SR}[rounding] if isinstance(rounding, str) else rounding,
-               seed, step, out_mask, int(use_precomputed))
+               seed, step, out_mask, int(use_precomputed), int(sr_index_base))
 
 
 def outer_shapes(cfg):

@@ -62,6 +62,10 @@ typedef struct {
   uint32_t step;
   uint32_t out_mask;         /* ORC_ROW | ORC_COL                              */
   int32_t use_precomputed;   /* read outer scales instead of computing them  */
+  int64_t sr_index_base;     /* added to every element's flat index in the
+                                stochastic-rounding counter, so a slice of
+                                rows can be checked with the indices it has
+                                in the whole tensor (0 for whole tensors)   */
 } orc_cfg;
 
 /* ------------------------------------------------------------------------ */
@@ -343,7 +347,7 @@ static void quantize_orientation(const orc_cfg *cf, int o, const float *u,
             float t = (s > 0.0f) ? v / s : copysignf(0.0f, v);
             uint8_t q;
             if (cf->rounding == ORC_SR) {
-              uint64_t n = (uint64_t)((g * R + r) * C + c);
+              uint64_t n = (uint64_t)(cf->sr_index_base + (g * R + r) * C + c);
               q = orc_e2m1_sr((double)t, orc_sr_word(cf->seed, cf->step, o == ORC_ROW ? 0u : 1u, n));
             } else {
               q = orc_e2m1_rne((double)t);
