@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the block-scaled FP4 quantizer on GB300.
+
+One step = one pass of the quantizer over one batch of synthetic input.  The
+headline workload is MXFP4 fake-quantization of a bf16 [8192, 8192] weight
+~ N(0, 0.02) with 0.1 % edge blocks (the workload the pages quote their
+B200 timing on); the metric is GB/s of algorithmic bytes (bf16 in + bf16 out)
+and its fraction of the measured HBM copy bandwidth.  The other workloads
+(NVFP4 rowwise+columnwise activations, MoE expert weights with 2-D outer
+scales, the SR + error-feedback weight update, dequantize) are timed in the
+same run and reported under "kernels".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (weak scaling, no data-path collective); timing is bracketed by barriers
+and the maximum over ranks is reported by rank 0.  ``--impl reference`` times
+the CPU oracle (the plain restatement of the method) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MXFP4_BYTES = 2 * 2 * 8192 * 8192           # bf16 in + bf16 out
+B200_CUTE_DSL_GBS = MXFP4_BYTES / 59e-6 / 1e9  # the pages' best figure for this workload (B200)
+L2_BYTES = 126 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-kernel table of other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (barriers and a max over ranks only)
+# ---------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        import torch
+
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = list(csv.reader(io.StringIO(out)))
+        sm, mx, reasons, n_all = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 10:
+                continue
+            n_all += 1
+            try:
+                ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except ValueError:
+                continue
+            if ts < int(t0) or ts > t1 + 1:
+                continue
+            try:
+                sm.append(float(r[2]))
+                mx.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# measured peak and ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source has not changed since the counters were taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    ent = table.get(kernel_key)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    for src in ent["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return ent["dram_bytes_per_launch"] if h.hexdigest()[:16] == ent["source_sha256_16"] else None
+
+
+# ---------------------------------------------------------------------------
+# workloads (CUDA path)
+# ---------------------------------------------------------------------------
+
+def _events_time(fn, iters, warmup):
+    """Average ms per call of fn(i) with CUDA events on the current stream."""
+    import torch
+
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(iters):
+        fn(i)
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def _sets_for(nbytes):
+    return max(1, -(-2 * L2_BYTES // max(1, nbytes)))  # enough rotating copies to exceed L2 twice
+
+
+def extra_kernels(peak):
+    """Time the other workloads (kernel only, inputs resident in HBM)."""
+    import torch
+
+    import block_scaled_fp4_quantize_gb300 as fq
+    from block_scaled_fp4_quantize_gb300 import workloads as W
+
+    out = {}
+    dev = torch.device("cuda")
+
+    def rec(name, desc, nbytes, ms, launches):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"workload": desc, "bytes": nbytes, "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / peak, 4), "launches": launches}
+
+    # small NVFP4 quantize + dequantize (launch-bound)
+    x = W.small_nvfp4().to(dev)
+    q = fq.quantize(x, mode="outer_block", outer_block_size=64)
+    ms = _events_time(lambda i: fq.quantize(x, mode="outer_block", outer_block_size=64, out=q), 200, 10)
+    rec("small_nvfp4_quantize", "bf16[256,512] 1x64 outer E4M3 RNE rowwise", 262144 + 65536 + 8192 + 8192, ms, 1)
+
+    # activations: row + col, 1-D outer 64 and tensorwise
+    xs = [W.activations().to(dev)]
+    nb_in = xs[0].numel() * 2
+    for _ in range(_sets_for(nb_in) - 1):
+        xs.append(xs[0].clone())
+    M, K = 16384, 2880
+    codes = M * K // 2
+    for mode, kw, nb_out in (
+            ("outer_block", dict(mode="outer_block", outer_block_size=64), 2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4),
+            ("tensorwise", dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4)):
+        qs = [fq.quantize(xx, rowwise=True, columnwise=True, **kw) for xx in xs]
+        ms = _events_time(lambda i: fq.quantize(xs[i % len(xs)], rowwise=True, columnwise=True, out=qs[i % len(xs)],
+                                                **kw), 50, 5)
+        rec("activations_%s" % mode, "bf16[16384,2880] massive activations, %s, rowwise+columnwise" % mode,
+            nb_in + nb_out, ms, 1 if mode == "outer_block" else 3)
+    qd = fq.quantize(xs[0], mode="outer_block", outer_block_size=64)
+    yd = torch.empty(1, M, K, dtype=torch.bfloat16, device=dev)
+    ms = _events_time(lambda i: fq.dequantize(qd, "row", torch.bfloat16, out=yd), 50, 5)
+    rec("dequantize_activations", "codes+scales+S of bf16[16384,2880] -> bf16", codes + M * K // 16 + M * K // 64 * 4 + M * K * 2, ms, 1)
+    del xs, qs, qd, yd
+
+    # MoE experts: 32 x [5760, 2880], 2-D 64x64 outer scales, row + col
+    G, M, K = 32, 5760, 2880
+    g = torch.Generator(dev).manual_seed(0)
+    xe = (torch.randn(G, M, K, generator=g, device=dev) * 0.02)
+    xe = torch.where(torch.rand(G, M, K, generator=g, device=dev) < 0.01, xe * 200, xe).to(torch.bfloat16)
+    for fmt in ("e4m3", "ue5m3"):
+        kw = dict(mode="outer_block", outer_block_size=64, outer_2d=True, scale_format=fmt, rowwise=True,
+                  columnwise=True)
+        qe = fq.quantize(xe, **kw)
+        ms = _events_time(lambda i: fq.quantize(xe, out=qe, **kw), 20, 3)
+        nb = G * M * K * 2 + 2 * (G * M * K // 2) + 2 * (G * M * K // 16) + G * (M // 64) * (K // 64) * 4
+        rec("moe_experts_%s" % fmt, "32 x bf16[5760,2880] 2-D 64x64 outer %s rowwise+columnwise" % fmt, nb, ms, 1)
+        del qe
+    del xe
+
+    # SR + EF stored-weight update step: fp32 [8192, 8192]
+    Wt = torch.randn(8192, 8192, generator=g, device=dev) * 0.02
+    r = torch.zeros_like(Wt)
+    y = torch.empty(1, 8192, 8192, device=dev)
+    ms = _events_time(lambda i: fq.qdq(Wt, stochastic=True, seed=0, step=i, residual=r, out_dtype=torch.float32,
+                                       out=y), 20, 3)
+    rec("sr_ef_weight_qdq", "fp32[8192,8192] qdq, E4M3, SR + error feedback (x, r read; r, y written)",
+        4 * 8192 * 8192 * 4, ms, 1)
+    return out
+
+
+def run_ours(args, dist):
+    import torch
+
+    import block_scaled_fp4_quantize_gb300 as fq
+    from block_scaled_fp4_quantize_gb300 import workloads as W
+
+    fq.build()
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    peak, peak_src = hbm_peak()
+
+    x_host, _ = W.mxfp4_weight()
+    xs = [x_host.to(dev) for _ in range(2)]          # 2 x (134 MB in + 134 MB out) > L2
+    ys = [torch.empty_like(xs[0]) for _ in range(2)]
+
+    def step(i):
+        fq.mxfp4_fake_quantize(xs[i & 1], out=ys[i & 1])
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if dist.rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(args.steps):
+        step(i)
+    ev1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    t1 = time.time()
+    ms_total = dist.max(ev0.elapsed_time(ev1))
+    clocks = sampler.stop(t0, t1) if sampler else None
+    ms_step = ms_total / args.steps
+    value = MXFP4_BYTES * dist.world / (ms_step * 1e-3) / 1e9
+    kernel_gbs = MXFP4_BYTES / (ms_step * 1e-3) / 1e9   # one launch per step: launch time == step time
+
+    # end to end through the public API: pinned host input -> device -> kernel -> pinned host output
+    xh = x_host.pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    xd, yd = torch.empty_like(xs[0]), torch.empty_like(ys[0])
+
+    def e2e_step(i):
+        xd.copy_(xh, non_blocking=True)
+        fq.mxfp4_fake_quantize(xd, out=yd)
+        yh.copy_(yd, non_blocking=True)
+
+    e2e_ms = dist.max(_events_time(e2e_step, args.e2e_steps, 2))
+    torch.cuda.synchronize()
+    del xs, ys, xd, yd
+
+    extras = None
+    if not args.no_extras and dist.rank == 0:
+        extras = extra_kernels(peak)
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x_host, budget_s=12.0)
+
+    if dist.rank != 0:
+        return None
+    line = {
+        "metric": "FP4 quantize GB/s (bytes in+out) and % of GB300 HBM peak, 1 GPU",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / dist.world / B200_CUTE_DSL_GBS, 4),
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "mxfp4_weight: MXFP4 fake-quantize bf16[8192,8192] ~N(0,0.02), 0.1% edge blocks, "
+                               "bf16 out", "shape": [8192, 8192], "bytes_per_step": MXFP4_BYTES,
+                   "l2": "2 rotating input/output sets (537 MB > L2)", "parallelism": "replicas" if dist.world > 1 else "none"},
+        "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(kernel_gbs / peak, 4), "peak_source": peak_src,
+                     "traffic": ncu_traffic("mxfp4_vec_kernel"), "kernel": "mxfp4_vec_kernel<bf16,bf16>"},
+        "e2e": {"value": round(MXFP4_BYTES / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": MXFP4_BYTES // 2, "d2h_bytes_per_step": MXFP4_BYTES // 2},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if extras is not None:
+        line["kernels"] = extras
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings
+# ---------------------------------------------------------------------------
+
+def _oracle_rows_time(orc, xb, rows):
+    t = time.perf_counter()
+    orc.mxfp4_fake_quantize(xb[:rows])
+    return time.perf_counter() - t
+
+
+def cpu_baseline(x_host, budget_s=12.0):
+    """The oracle, as it stands, single-threaded on a bounded sample of the
+    headline workload (leading rows of the same tensor)."""
+    import numpy as np
+
+    import oracle as orc
+
+    orc.build()
+    xb = x_host.contiguous().view(__import__("torch").int16).numpy().view(np.uint16)
+    t64 = _oracle_rows_time(orc, xb, 64)
+    rows = int(max(64, min(xb.shape[0], 64 * budget_s / max(t64, 1e-6) / 2)))
+    dt = _oracle_rows_time(orc, xb, rows)
+    nbytes = rows * xb.shape[1] * 4
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "leading %d of 8192 rows of the bf16[8192,8192] input (%.1f s)" % (rows, dt)}
+
+
+def run_reference(args, dist):
+    """Reference arm: the CPU oracle on the host cores, same metric and workload,
+    each step a bounded sample (leading rows) of the input."""
+    if dist.rank != 0:
+        return None
+    import numpy as np
+    import torch
+
+    import oracle as orc
+    from block_scaled_fp4_quantize_gb300 import workloads as W
+
+    orc.build()
+    x_host, _ = W.mxfp4_weight()
+    xb = x_host.view(torch.int16).numpy().view(np.uint16)
+    t64 = _oracle_rows_time(orc, xb, 64)
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(8192, 64 * per_step_budget / max(t64, 1e-6))))
+    for _ in range(args.warmup):
+        orc.mxfp4_fake_quantize(xb[:rows])
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        orc.mxfp4_fake_quantize(xb[:rows])
+    dt = time.perf_counter() - t
+    nbytes = rows * 8192 * 4 * args.steps
+    value = nbytes / dt / 1e9
+    return {
+        "impl": "reference",
+        "metric": "FP4 quantize GB/s (bytes in+out) and % of GB300 HBM peak, 1 GPU",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "mxfp4_weight: MXFP4 fake-quantize bf16[8192,8192] ~N(0,0.02), 0.1% edge blocks, "
+                               "bf16 out", "shape": [8192, 8192], "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "leading %d of 8192 rows per step" % rows},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; the other ranks exit without work
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        ref = argparse.Namespace(rank=0, world=int(os.environ.get("WORLD_SIZE", "1")), local=0)
+        print(json.dumps(run_reference(args, ref)))
+        return 0
+    dist = Dist()
+    try:
+        line = run_ours(args, dist)
+    finally:
+        dist.close()
+    if line is not None:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

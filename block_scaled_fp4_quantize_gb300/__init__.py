@@ -1,0 +1,234 @@
+"""Block-scaled FP4 quantizer for GB300 (sm_103a): NVFP4, AMD-FP4 and MXFP4.
+
+Thin PyTorch binding over the C ABI of ``include/fp4q.h``: torch provides
+device memory and the current stream, every step of the computation runs in
+the library's CUDA kernels.  The library must be built for the GPU in use
+(``build()``); there is no CPU fallback.
+
+    quantize(x, ...)            -> QuantizedFP4 (rowwise / columnwise codes and scales)
+    dequantize(q, orient="row") -> bf16 / fp32 tensor
+    qdq(x, ...)                 -> (y, outer scales)
+    mxfp4_fake_quantize(x)      -> projected tensor
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _capi
+from ._capi import FP4QError
+
+__all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize", "build", "FP4QError",
+           "query_sizes"]
+
+_MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
+_FMTS = {"e4m3": _capi.SCALE_E4M3, "ue5m3": _capi.SCALE_UE5M3}
+_DT = {torch.bfloat16: _capi.BF16, torch.float32: _capi.FP32, torch.float16: _capi.FP16}
+_ORIENT = {"row": _capi.OUT_ROW, "col": _capi.OUT_COL, -1: _capi.OUT_ROW, 0: _capi.OUT_COL}
+
+
+def build(fast_math: bool = False, force: bool = False) -> str:
+    from . import _builder as _b
+
+    return _b.build(fast_math=fast_math, force=force)
+
+
+def _lib():
+    return _capi.load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(dev):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _view3d(x: torch.Tensor):
+    """(x3, G, M, K, ld) for a [M, K] or [G, M, K] tensor whose rows are
+    contiguous and whose matrices are back to back (batch stride M * ld)."""
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (the library has no CPU path)")
+    if x.dim() == 2:
+        x3 = x.unsqueeze(0)
+    elif x.dim() == 3:
+        x3 = x
+    else:
+        raise ValueError("expected a 2-D or 3-D tensor, got %d-D" % x.dim())
+    G, M, K = x3.shape
+    if K > 1 and x3.stride(2) != 1:
+        raise ValueError("the last dimension must be contiguous")
+    ld = x3.stride(1) if M > 1 else K
+    if G > 1 and x3.stride(0) != M * ld:
+        raise ValueError("matrices must be stored back to back (batch stride M * ld)")
+    return x3, G, M, K, ld
+
+
+def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_size=0, outer_2d=False,
+            inner_2d=False, scale_format="e4m3", stochastic=False, seed=0, step=0, out_mask=_capi.OUT_ROW,
+            use_precomputed_outer=False):
+    p = _capi.new_params(_lib())
+    p.G, p.M, p.K, p.ld = G, M, K, ld
+    p.in_dtype = _DT.get(in_dtype, -1)
+    p.out_dtype = _DT.get(out_dtype if out_dtype is not None else in_dtype, -1)
+    p.mode = _MODES[mode]
+    p.outer_block_size = int(outer_block_size)
+    p.outer_2d = int(bool(outer_2d))
+    p.inner_2d = int(bool(inner_2d))
+    p.scale_format = _FMTS[scale_format]
+    p.rounding = _capi.STOCHASTIC if stochastic else _capi.RNE
+    p.seed = int(seed) & (2 ** 64 - 1)
+    p.step = int(step) & (2 ** 32 - 1)
+    p.out_mask = int(out_mask)
+    p.use_precomputed_outer = int(bool(use_precomputed_outer))
+    return p
+
+
+def query_sizes(p) -> _capi.Sizes:
+    s = _capi.Sizes()
+    _capi.check(_lib().fp4q_query_sizes(ctypes.byref(p), ctypes.byref(s)), "fp4q_query_sizes")
+    return s
+
+
+@dataclass
+class QuantizedFP4:
+    """Outputs of ``quantize``; absent orientations / scales are None."""
+    shape: tuple
+    mode: str
+    outer_block_size: int
+    outer_2d: bool
+    inner_2d: bool
+    scale_format: str
+    row_codes: Optional[torch.Tensor] = None   # uint8 [G, M, K/2]
+    row_scales: Optional[torch.Tensor] = None  # uint8 [G, M, K/16]
+    row_outer: Optional[torch.Tensor] = None   # float32 [G, M, K/ob]
+    col_codes: Optional[torch.Tensor] = None   # uint8 [G, K, M/2]
+    col_scales: Optional[torch.Tensor] = None  # uint8 [G, K, M/16]
+    col_outer: Optional[torch.Tensor] = None   # float32 [G, K, M/ob]
+    tile_outer: Optional[torch.Tensor] = None  # float32 [G, M/ob, K/ob] or [1]
+
+
+def _outer_shapes(G, M, K, mode, ob, outer_2d, row, col):
+    shp = {"row_outer": None, "col_outer": None, "tile_outer": None}
+    if mode == "tensorwise":
+        shp["tile_outer"] = (1,)
+    elif mode == "outer_block":
+        if outer_2d:
+            shp["tile_outer"] = (G, M // ob, K // ob)
+        else:
+            if row:
+                shp["row_outer"] = (G, M, K // ob)
+            if col:
+                shp["col_outer"] = (G, K, M // ob)
+    return shp
+
+
+def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, outer_2d: bool = False,
+             inner_2d: bool = False, scale_format: str = "e4m3", stochastic: bool = False, seed: int = 0,
+             step: int = 0, rowwise: bool = True, columnwise: bool = False,
+             residual: Optional[torch.Tensor] = None, precomputed_outer: Optional[QuantizedFP4] = None,
+             out: Optional[QuantizedFP4] = None) -> QuantizedFP4:
+    """NVFP4 / AMD-FP4 quantize of a CUDA bf16 or fp32 tensor ([M, K] or [G, M, K]).
+
+    ``residual`` (fp32, [G, M, K] contiguous) enables error feedback and is
+    updated in place (rowwise only).  ``precomputed_outer`` supplies outer
+    scales (from an earlier call) instead of computing them.  ``out`` reuses
+    preallocated output buffers."""
+    x3, G, M, K, ld = _view3d(x)
+    mask = (_capi.OUT_ROW if rowwise else 0) | (_capi.OUT_COL if columnwise else 0)
+    p = _params(G, M, K, ld, x.dtype, mode=mode, outer_block_size=outer_block_size, outer_2d=outer_2d,
+                inner_2d=inner_2d, scale_format=scale_format, stochastic=stochastic, seed=seed, step=step,
+                out_mask=mask, use_precomputed_outer=precomputed_outer is not None)
+    s = query_sizes(p)
+    dev = x.device
+    if out is None:
+        u8 = dict(dtype=torch.uint8, device=dev)
+        q = QuantizedFP4((G, M, K), mode, outer_block_size, outer_2d, inner_2d, scale_format)
+        if rowwise:
+            q.row_codes = torch.empty(G, M, K // 2, **u8)
+            q.row_scales = torch.empty(G, M, K // 16, **u8)
+        if columnwise:
+            q.col_codes = torch.empty(G, K, M // 2, **u8)
+            q.col_scales = torch.empty(G, K, M // 16, **u8)
+        for name, shp in _outer_shapes(G, M, K, mode, outer_block_size, outer_2d, rowwise, columnwise).items():
+            if shp is not None:
+                src = getattr(precomputed_outer, name, None) if precomputed_outer is not None else None
+                setattr(q, name, src if src is not None else torch.empty(shp, dtype=torch.float32, device=dev))
+    else:
+        q = out
+    o = _capi.Outputs(*[_ptr(getattr(q, n)) for n in
+                        ("row_codes", "row_scales", "row_outer", "col_codes", "col_scales", "col_outer",
+                         "tile_outer")])
+    ws = torch.empty(max(int(s.workspace), 1), dtype=torch.uint8, device=dev) if s.workspace else None
+    st = _lib().fp4_quantize(ctypes.byref(p), _ptr(x3), ctypes.byref(o), _ptr(residual), _ptr(ws),
+                             int(s.workspace), _stream(dev))
+    _capi.check(st, "fp4_quantize")
+    return q
+
+
+def dequantize(q: QuantizedFP4, orient: str = "row", out_dtype: torch.dtype = torch.bfloat16,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Dequantize one orientation of ``q``: [G, M, K] (row) or [G, K, M] (col)."""
+    G, M, K = q.shape
+    o = _ORIENT[orient]
+    codes = q.row_codes if o == _capi.OUT_ROW else q.col_codes
+    scales = q.row_scales if o == _capi.OUT_ROW else q.col_scales
+    if q.mode == "outer_block" and not q.outer_2d:
+        outer = q.row_outer if o == _capi.OUT_ROW else q.col_outer
+    else:
+        outer = q.tile_outer
+    p = _params(G, M, K, K, torch.bfloat16, out_dtype, mode=q.mode, outer_block_size=q.outer_block_size,
+                outer_2d=q.outer_2d, inner_2d=q.inner_2d, scale_format=q.scale_format, out_mask=o)
+    R, C = (M, K) if o == _capi.OUT_ROW else (K, M)
+    y = out if out is not None else torch.empty(G, R, C, dtype=out_dtype, device=codes.device)
+    st = _lib().fp4_dequantize(ctypes.byref(p), o, _ptr(codes), _ptr(scales), _ptr(outer), _ptr(y),
+                               _stream(codes.device))
+    _capi.check(st, "fp4_dequantize")
+    return y
+
+
+def qdq(x: torch.Tensor, *, axis: int = -1, mode: str = "none", outer_block_size: int = 0,
+        outer_2d: bool = False, inner_2d: bool = False, scale_format: str = "e4m3", stochastic: bool = False,
+        seed: int = 0, step: int = 0, residual: Optional[torch.Tensor] = None,
+        precomputed_outer: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+        out: Optional[torch.Tensor] = None):
+    """Quantize-dequantize along ``axis`` (-1: blocks along K; 0: along M).
+
+    Returns (y, outer) with y [G, M, K] (or [M, K]) in ``out_dtype`` (x's dtype
+    by default) and ``outer`` the outer scales used (None in mode none)."""
+    x3, G, M, K, ld = _view3d(x)
+    o = _ORIENT[axis]
+    out_dtype = out_dtype or x.dtype
+    p = _params(G, M, K, ld, x.dtype, out_dtype, mode=mode, outer_block_size=outer_block_size,
+                outer_2d=outer_2d, inner_2d=inner_2d, scale_format=scale_format, stochastic=stochastic,
+                seed=seed, step=step, out_mask=o, use_precomputed_outer=precomputed_outer is not None)
+    s = query_sizes(p)
+    dev = x.device
+    shp = _outer_shapes(G, M, K, mode, outer_block_size, outer_2d, o == _capi.OUT_ROW, o == _capi.OUT_COL)
+    oshape = next((v for v in shp.values() if v is not None), None)
+    if precomputed_outer is not None:
+        outer = precomputed_outer
+    else:
+        outer = torch.empty(oshape, dtype=torch.float32, device=dev) if oshape is not None else None
+    y = out if out is not None else torch.empty(G, M, K, dtype=out_dtype, device=dev)
+    ws = torch.empty(int(s.workspace), dtype=torch.uint8, device=dev) if s.workspace else None
+    st = _lib().fp4_qdq(ctypes.byref(p), o, _ptr(x3), _ptr(y), _ptr(residual), _ptr(outer), _ptr(ws),
+                        int(s.workspace), _stream(dev))
+    _capi.check(st, "fp4_qdq")
+    return (y if x.dim() == 3 or out is not None else y[0]), outer
+
+
+def mxfp4_fake_quantize(x: torch.Tensor, out_dtype: Optional[torch.dtype] = None,
+                        out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """MXFP4 projection (E2M1 with 1 x 32 power-of-two scales, RNE) of x."""
+    x3, G, M, K, ld = _view3d(x)
+    out_dtype = out_dtype or x.dtype
+    p = _params(G, M, K, ld, x.dtype, out_dtype)
+    y = out if out is not None else torch.empty(G, M, K, dtype=out_dtype, device=x.device)
+    st = _lib().mxfp4_fake_quantize(ctypes.byref(p), _ptr(x3), _ptr(y), _stream(x.device))
+    _capi.check(st, "mxfp4_fake_quantize")
+    return y if (x.dim() == 3 or out is not None) else y[0]

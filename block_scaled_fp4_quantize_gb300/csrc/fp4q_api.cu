@@ -1,0 +1,321 @@
+// fp4q_api.cu -- the C ABI: argument validation, path selection, launches.
+//
+// Nothing here allocates, frees or synchronizes; all work is enqueued on the
+// caller's stream.  Validation happens before any launch, so an error other
+// than FP4Q_ERR_CUDA leaves the stream untouched.
+#include <cstdint>
+
+#include "fp4q.h"
+#include "fp4q_internal.h"
+
+namespace fp4q {
+
+int num_sms() {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int vec_aligned(const void* p, int64_t bytes_stride) {
+  return (reinterpret_cast<uintptr_t>(p) % 16u == 0u) && (bytes_stride % 16 == 0);
+}
+
+}  // namespace fp4q
+
+using namespace fp4q;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0u; }
+
+int esize(int32_t dt) { return dt == FP4Q_BF16 ? 2 : 4; }
+
+int check_dtype(int32_t dt) {
+  if (dt == FP4Q_BF16 || dt == FP4Q_FP32) return FP4Q_OK;
+  return FP4Q_ERR_DTYPE;
+}
+
+// Rules shared by quantize and qdq; `mask` is the set of orientations produced.
+int check_nvfp4(const fp4q_params_t* p, uint32_t mask) {
+  if (!p) return FP4Q_ERR_NULL;
+  if (p->struct_size != sizeof(fp4q_params_t)) return FP4Q_ERR_ABI;
+  int rc = check_dtype(p->in_dtype);
+  if (rc) return rc;
+  if (mask == 0u || (mask & ~3u)) return FP4Q_ERR_MODE;
+  if (p->mode < FP4Q_MODE_NONE || p->mode > FP4Q_MODE_OUTER_BLOCK) return FP4Q_ERR_MODE;
+  if (p->scale_format != FP4Q_SCALE_E4M3 && p->scale_format != FP4Q_SCALE_UE5M3) return FP4Q_ERR_MODE;
+  if (p->rounding != FP4Q_RNE && p->rounding != FP4Q_STOCHASTIC) return FP4Q_ERR_MODE;
+  if ((p->outer_2d & ~1) || (p->inner_2d & ~1) || (p->use_precomputed_outer & ~1)) return FP4Q_ERR_MODE;
+  if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K) return FP4Q_ERR_SHAPE;
+  if (p->K % 16) return FP4Q_ERR_SHAPE;
+  const bool col = (mask & FP4Q_OUT_COL) != 0u;
+  if ((col || p->inner_2d) && p->M % 16) return FP4Q_ERR_SHAPE;
+  if (p->mode == FP4Q_MODE_OUTER_BLOCK) {
+    const int64_t ob = p->outer_block_size;
+    if (ob <= 0 || ob % 16) return FP4Q_ERR_SHAPE;
+    if (p->K % ob) return FP4Q_ERR_SHAPE;
+    if ((col || p->outer_2d) && p->M % ob) return FP4Q_ERR_SHAPE;
+  } else {
+    if (p->outer_block_size != 0 || p->outer_2d != 0) return FP4Q_ERR_MODE;
+    if (p->mode == FP4Q_MODE_NONE && p->use_precomputed_outer) return FP4Q_ERR_MODE;
+  }
+  return FP4Q_OK;
+}
+
+void sizes_for(const fp4q_params_t* p, uint32_t mask, fp4q_sizes_t* s) {
+  const int64_t G = p->G, M = p->M, K = p->K, ob = p->outer_block_size;
+  const bool row = (mask & FP4Q_OUT_ROW) != 0u, col = (mask & FP4Q_OUT_COL) != 0u;
+  const bool outer = p->mode == FP4Q_MODE_OUTER_BLOCK;
+  s->row_codes = row ? (size_t)(G * M * K / 2) : 0;
+  s->row_scales = row ? (size_t)(G * M * K / 16) : 0;
+  s->col_codes = col ? (size_t)(G * K * M / 2) : 0;
+  s->col_scales = col ? (size_t)(G * K * M / 16) : 0;
+  s->row_outer = (outer && !p->outer_2d && row) ? (size_t)(G * M * (K / ob)) * sizeof(float) : 0;
+  s->col_outer = (outer && !p->outer_2d && col) ? (size_t)(G * K * (M / ob)) * sizeof(float) : 0;
+  s->tile_outer = (outer && p->outer_2d) ? (size_t)(G * (M / ob) * (K / ob)) * sizeof(float)
+                  : (p->mode == FP4Q_MODE_TENSORWISE ? sizeof(float) : 0);
+  s->workspace = (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer) ? 256 : 0;
+}
+
+QuantJob base_job(const fp4q_params_t* p, const void* x, float* residual) {
+  QuantJob j{};
+  j.x = x;
+  j.ld = p->ld;
+  j.in_bf16 = p->in_dtype == FP4Q_BF16;
+  j.G = p->G;
+  j.M = p->M;
+  j.K = p->K;
+  j.residual = residual;
+  j.mode = p->mode;
+  j.ob = p->outer_block_size;
+  j.outer_2d = p->outer_2d;
+  j.inner_2d = p->inner_2d;
+  j.ue5m3 = p->scale_format == FP4Q_SCALE_UE5M3;
+  j.sr = p->rounding == FP4Q_STOCHASTIC;
+  j.seed = p->seed;
+  j.step = p->step;
+  j.out_bf16 = p->out_dtype == FP4Q_BF16;
+  return j;
+}
+
+// Pick the outer-scale source, running the amax / pre-pass kernels it needs.
+int prepare_outer(const fp4q_params_t* p, QuantJob& j, void* ws, cudaStream_t st) {
+  if (p->mode == FP4Q_MODE_NONE) {
+    j.s_src = S_ONE;
+    return FP4Q_OK;
+  }
+  if (p->use_precomputed_outer) {
+    j.s_src = S_FROM_BUFFER;
+    return FP4Q_OK;
+  }
+  if (p->mode == FP4Q_MODE_TENSORWISE) {
+    j.s_src = S_TENSORWISE_WS;
+    j.tw_amax = static_cast<uint32_t*>(ws);
+    return launch_tensor_amax(j, static_cast<uint32_t*>(ws), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+  }
+  const int ob = p->outer_block_size;
+  if (ob == 16 || ob == 32 || ob == 64) {
+    j.s_src = S_IN_TILE;
+    return FP4Q_OK;
+  }
+  j.s_src = S_FROM_BUFFER;
+  return launch_outer_prepass(j, st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+bool vec_ok(const fp4q_params_t* p, const void* x, const float* residual, const void* y) {
+  return vec_aligned(x, p->ld * esize(p->in_dtype)) && (!residual || aligned(residual, 16)) && (!y || aligned(y, 16));
+}
+
+}  // namespace
+
+extern "C" {
+
+void fp4q_params_init(fp4q_params_t* p) {
+  if (!p) return;
+  *p = fp4q_params_t{};
+  p->struct_size = sizeof(fp4q_params_t);
+  p->out_mask = FP4Q_OUT_ROW;
+  p->G = 1;
+  p->in_dtype = FP4Q_BF16;
+  p->out_dtype = FP4Q_BF16;
+  p->mode = FP4Q_MODE_NONE;
+  p->scale_format = FP4Q_SCALE_E4M3;
+  p->rounding = FP4Q_RNE;
+}
+
+int fp4q_query_sizes(const fp4q_params_t* p, fp4q_sizes_t* sizes) {
+  if (!p || !sizes) return FP4Q_ERR_NULL;
+  const int rc = check_nvfp4(p, p->out_mask);
+  if (rc) return rc;
+  sizes_for(p, p->out_mask, sizes);
+  return FP4Q_OK;
+}
+
+int fp4_quantize(const fp4q_params_t* p, const void* x, const fp4q_outputs_t* out, float* residual, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  if (!p || !out) return FP4Q_ERR_NULL;
+  int rc = check_nvfp4(p, p->out_mask);
+  if (rc) return rc;
+  const uint32_t mask = p->out_mask;
+  const bool row = mask & FP4Q_OUT_ROW, col = mask & FP4Q_OUT_COL;
+  if (residual && col) return FP4Q_ERR_UNSUPPORTED;
+  fp4q_sizes_t s;
+  sizes_for(p, mask, &s);
+  const bool empty = p->G == 0 || p->M == 0 || p->K == 0;
+  if (!empty) {
+    if (!x) return FP4Q_ERR_NULL;
+    if (row && (!out->row_codes || !out->row_scales)) return FP4Q_ERR_NULL;
+    if (col && (!out->col_codes || !out->col_scales)) return FP4Q_ERR_NULL;
+    if (s.row_outer && !out->row_outer) return FP4Q_ERR_NULL;
+    if (s.col_outer && !out->col_outer) return FP4Q_ERR_NULL;
+  }
+  if (s.tile_outer && !out->tile_outer) return FP4Q_ERR_NULL;
+  if (s.workspace && (!workspace || workspace_bytes < s.workspace)) return FP4Q_ERR_WORKSPACE;
+  if (s.workspace && !aligned(workspace, 16)) return FP4Q_ERR_ALIGN;
+  if (!aligned(x, (uintptr_t)esize(p->in_dtype))) return FP4Q_ERR_ALIGN;
+  if ((row && !aligned(out->row_codes, 8)) || (col && !aligned(out->col_codes, 8))) return FP4Q_ERR_ALIGN;
+  if (!aligned(out->row_outer, 4) || !aligned(out->col_outer, 4) || !aligned(out->tile_outer, 4)) return FP4Q_ERR_ALIGN;
+  if (residual && !aligned(residual, 16)) return FP4Q_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {
+    if (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer)
+      return cudaMemsetAsync(out->tile_outer, 0, sizeof(float), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+    return FP4Q_OK;
+  }
+  QuantJob j = base_job(p, x, residual);
+  j.do_row = row;
+  j.do_col = col;
+  j.row_codes = row ? out->row_codes : nullptr;
+  j.row_scales = row ? out->row_scales : nullptr;
+  j.col_codes = col ? out->col_codes : nullptr;
+  j.col_scales = col ? out->col_scales : nullptr;
+  j.row_outer = s.row_outer ? out->row_outer : nullptr;
+  j.col_outer = s.col_outer ? out->col_outer : nullptr;
+  j.tile_outer = s.tile_outer ? out->tile_outer : nullptr;
+  rc = prepare_outer(p, j, workspace, st);
+  if (rc) return rc;
+  return launch_quant_tile(j, vec_ok(p, x, residual, nullptr), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+int fp4_qdq(const fp4q_params_t* p, int orient, const void* x, void* y, float* residual, float* outer, void* workspace,
+            size_t workspace_bytes, void* stream) {
+  if (!p) return FP4Q_ERR_NULL;
+  if (orient != (int)FP4Q_OUT_ROW && orient != (int)FP4Q_OUT_COL) return FP4Q_ERR_MODE;
+  int rc = check_nvfp4(p, (uint32_t)orient);
+  if (rc) return rc;
+  rc = check_dtype(p->out_dtype);
+  if (rc) return rc;
+  if (residual && orient == (int)FP4Q_OUT_COL) return FP4Q_ERR_UNSUPPORTED;
+  fp4q_sizes_t s;
+  sizes_for(p, (uint32_t)orient, &s);
+  const bool needs_outer = p->mode != FP4Q_MODE_NONE;
+  if (needs_outer && !outer) return FP4Q_ERR_NULL;
+  if (s.workspace && (!workspace || workspace_bytes < s.workspace)) return FP4Q_ERR_WORKSPACE;
+  if (s.workspace && !aligned(workspace, 16)) return FP4Q_ERR_ALIGN;
+  const bool empty = p->G == 0 || p->M == 0 || p->K == 0;
+  if (!empty && (!x || !y)) return FP4Q_ERR_NULL;
+  if (!aligned(x, (uintptr_t)esize(p->in_dtype)) || !aligned(y, (uintptr_t)esize(p->out_dtype))) return FP4Q_ERR_ALIGN;
+  if (!aligned(outer, 4) || (residual && !aligned(residual, 16))) return FP4Q_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {
+    if (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer)
+      return cudaMemsetAsync(outer, 0, sizeof(float), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+    return FP4Q_OK;
+  }
+  QuantJob j = base_job(p, x, residual);
+  j.do_row = orient == (int)FP4Q_OUT_ROW;
+  j.do_col = !j.do_row;
+  j.qdq_orient = j.do_row ? 1 : 2;
+  j.y = y;
+  if (p->mode == FP4Q_MODE_TENSORWISE || (p->mode == FP4Q_MODE_OUTER_BLOCK && p->outer_2d)) j.tile_outer = outer;
+  else if (p->mode == FP4Q_MODE_OUTER_BLOCK) (j.do_row ? j.row_outer : j.col_outer) = outer;
+  rc = prepare_outer(p, j, workspace, st);
+  if (rc) return rc;
+  return launch_quant_tile(j, vec_ok(p, x, residual, y), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+int fp4_dequantize(const fp4q_params_t* p, int orient, const uint8_t* codes, const uint8_t* scales, const float* outer,
+                   void* y, void* stream) {
+  if (!p) return FP4Q_ERR_NULL;
+  if (orient != (int)FP4Q_OUT_ROW && orient != (int)FP4Q_OUT_COL) return FP4Q_ERR_MODE;
+  int rc = check_nvfp4(p, (uint32_t)orient);
+  if (rc) return rc;
+  rc = check_dtype(p->out_dtype);
+  if (rc) return rc;
+  if (p->use_precomputed_outer) return FP4Q_ERR_MODE;
+  const bool empty = p->G == 0 || p->M == 0 || p->K == 0;
+  if (empty) return FP4Q_OK;
+  if (!codes || !scales || !y) return FP4Q_ERR_NULL;
+  if (p->mode != FP4Q_MODE_NONE && !outer) return FP4Q_ERR_NULL;
+  if (!aligned(codes, 8) || !aligned(outer, 4) || !aligned(y, (uintptr_t)esize(p->out_dtype))) return FP4Q_ERR_ALIGN;
+  DequantJob j{};
+  j.codes = codes;
+  j.scales = scales;
+  j.outer = outer;
+  j.y = y;
+  j.G = p->G;
+  j.M = p->M;
+  j.K = p->K;
+  j.col = orient == (int)FP4Q_OUT_COL;
+  j.R = j.col ? p->K : p->M;
+  j.C = j.col ? p->M : p->K;
+  j.mode = p->mode;
+  j.ob = p->outer_block_size;
+  j.outer_2d = p->outer_2d;
+  j.ue5m3 = p->scale_format == FP4Q_SCALE_UE5M3;
+  j.out_bf16 = p->out_dtype == FP4Q_BF16;
+  return launch_dequant(j, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+int mxfp4_fake_quantize(const fp4q_params_t* p, const void* x, void* y, void* stream) {
+  if (!p) return FP4Q_ERR_NULL;
+  if (p->struct_size != sizeof(fp4q_params_t)) return FP4Q_ERR_ABI;
+  int rc = check_dtype(p->in_dtype);
+  if (rc) return rc;
+  rc = check_dtype(p->out_dtype);
+  if (rc) return rc;
+  if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
+      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0)
+    return FP4Q_ERR_MODE;
+  if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
+  if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K || p->K % 32) return FP4Q_ERR_SHAPE;
+  if (p->G == 0 || p->M == 0 || p->K == 0) return FP4Q_OK;
+  if (!x || !y) return FP4Q_ERR_NULL;
+  if (!aligned(x, (uintptr_t)esize(p->in_dtype)) || !aligned(y, (uintptr_t)esize(p->out_dtype))) return FP4Q_ERR_ALIGN;
+  MxJob j{};
+  j.x = x;
+  j.ld = p->ld;
+  j.in_bf16 = p->in_dtype == FP4Q_BF16;
+  j.out_bf16 = p->out_dtype == FP4Q_BF16;
+  j.G = p->G;
+  j.M = p->M;
+  j.K = p->K;
+  j.y = y;
+  return launch_mxfp4(j, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+const char* fp4q_status_string(int status) {
+  switch (status) {
+    case FP4Q_OK: return "FP4Q_OK";
+    case FP4Q_ERR_NULL: return "FP4Q_ERR_NULL: a required pointer is NULL";
+    case FP4Q_ERR_DTYPE: return "FP4Q_ERR_DTYPE: unsupported dtype (bf16 or fp32 only)";
+    case FP4Q_ERR_SHAPE: return "FP4Q_ERR_SHAPE: a size or divisibility rule is violated";
+    case FP4Q_ERR_MODE: return "FP4Q_ERR_MODE: inconsistent mode or knob combination";
+    case FP4Q_ERR_UNSUPPORTED: return "FP4Q_ERR_UNSUPPORTED: combination not defined by the method";
+    case FP4Q_ERR_WORKSPACE: return "FP4Q_ERR_WORKSPACE: workspace missing or too small";
+    case FP4Q_ERR_CUDA: return "FP4Q_ERR_CUDA: a CUDA launch failed";
+    case FP4Q_ERR_ABI: return "FP4Q_ERR_ABI: parameter struct size mismatch";
+    case FP4Q_ERR_ALIGN: return "FP4Q_ERR_ALIGN: a buffer is not naturally aligned";
+    default: return "unknown fp4q status";
+  }
+}
+
+int fp4q_abi_version(void) { return FP4Q_ABI_VERSION; }
+
+}  // extern "C"

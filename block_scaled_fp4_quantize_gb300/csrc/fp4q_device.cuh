@@ -1,0 +1,183 @@
+// fp4q_device.cuh -- device-side numerics of the block-scaled FP4 quantizer.
+//
+// Every floating-point step that decides a bit of the output is written with
+// explicit PTX (div.rn / mul.rn / add.rn / sub.rn without .ftz), so results
+// keep subnormals and do not change under -use_fast_math or -ftz=true.
+// Absolute maxima are integer maxima of |x| bit patterns (monotone for
+// non-negative finite binary32), and scale encoders work on exponent and
+// mantissa bits; nothing here depends on log2/exp2 approximations.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4q {
+
+// ---------------------------------------------------------------------------
+// IEEE binary32, round to nearest even, subnormals preserved
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ieee_div(float a, float b) {
+  float r;
+  asm("div.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float ieee_mul(float a, float b) {
+  float r;
+  asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float ieee_add(float a, float b) {
+  float r;
+  asm("add.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float ieee_sub(float a, float b) {
+  float r;
+  asm("sub.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t fbits(float f) { return __float_as_uint(f); }
+__device__ __forceinline__ float bitsf(uint32_t b) { return __uint_as_float(b); }
+__device__ __forceinline__ uint32_t abs_bits(float f) { return __float_as_uint(f) & 0x7FFFFFFFu; }
+// +-0 carrying the sign of v
+__device__ __forceinline__ float signed_zero(float v) { return bitsf(fbits(v) & 0x80000000u); }
+
+// bf16 <-> binary32
+__device__ __forceinline__ float bf16lo(uint32_t w) { return bitsf(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return bitsf(w & 0xFFFF0000u); }
+// two binary32 -> packed bf16x2 (lo in bits 0-15), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Inner-scale formats: E4M3 (bias 7, max 448, codes 0..0x7E) and UE5M3
+// (bias 15, max 114688, codes 0..0xFE).  Byte c = exponent e (bits 7..3)
+// and mantissa m (bits 2..0): e == 0 -> m * 2^(-2-bias); else
+// (8 + m) * 2^(e - 3 - bias).
+// ---------------------------------------------------------------------------
+struct ScaleFmt {
+  int bias;
+  uint32_t maxcode;
+  uint32_t maxbits;  // binary32 bits of the largest finite value
+  float denom;       // largest finite value * 6 (the outer-scale denominator)
+};
+
+__host__ __device__ inline ScaleFmt scale_fmt(int ue5m3) {
+  ScaleFmt f;
+  if (ue5m3) { f.bias = 15; f.maxcode = 0xFE; f.maxbits = 0x47E00000u; f.denom = 688128.0f; }
+  else       { f.bias = 7;  f.maxcode = 0x7E; f.maxbits = 0x43E00000u; f.denom = 2688.0f; }
+  return f;
+}
+
+// Nearest code to v >= 0 (finite), ties to even, saturating at the maximum.
+__device__ __forceinline__ uint32_t enc_scale(float v, const ScaleFmt& f) {
+  uint32_t b = fbits(v);
+  if (b >= f.maxbits) return f.maxcode;
+  int ev = (int)(b >> 23) - 127;
+  uint32_t sig = b & 0x7FFFFFu;
+  if (b >> 23) sig |= 0x800000u; else ev = -126;
+  const bool normal = ev >= 1 - f.bias;
+  const int sh = normal ? 20 : 21 - f.bias - ev;  // bits below the kept mantissa
+  uint32_t m = 0;
+  if (sh < 32) {
+    m = sig >> sh;
+    const uint32_t rem = sig & ((1u << sh) - 1u);
+    const uint32_t half = 1u << (sh - 1);
+    m += (rem > half || (rem == half && (m & 1u))) ? 1u : 0u;
+  }
+  const uint32_t code = normal ? ((uint32_t)(ev + f.bias) << 3) + m - 8u : m;
+  return code < f.maxcode ? code : f.maxcode;
+}
+
+__device__ __forceinline__ float dec_scale(uint32_t c, const ScaleFmt& f) {
+  const uint32_t e = c >> 3, m = c & 7u;
+  if (e == 0) return ieee_mul((float)m, bitsf((uint32_t)(127 - 2 - f.bias) << 23));
+  return bitsf(((e - f.bias + 127u) << 23) | (m << 20));
+}
+
+// ---------------------------------------------------------------------------
+// E2M1: code = sign << 3 | k, magnitude index k into {0,.5,1,1.5,2,3,4,6}
+// ---------------------------------------------------------------------------
+
+// Round-to-nearest-even with saturation, two values at a time (hardware
+// conversion).  Returns a byte: `lo` in bits 0-3, `hi` in bits 4-7.
+__device__ __forceinline__ uint32_t e2m1x2_rne(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Decode a byte of two codes to binary32 (exact).
+__device__ __forceinline__ void e2m1x2_decode(uint32_t byte, float& lo, float& hi) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+}
+
+// Stochastic rounding of t onto the E2M1 grid with the 32-bit random word w:
+// between neighbours lo < |t| < hi the result is hi iff (w >> 8) < f * 2^24,
+// f = (|t| - lo) / (hi - lo).  Every step is exact in binary32.
+__device__ __forceinline__ uint32_t e2m1_sr(float t, uint32_t w) {
+  const uint32_t sign = (fbits(t) >> 28) & 8u;
+  const float a = bitsf(abs_bits(t));
+  uint32_t k;
+  if (!(a < 6.0f)) {
+    k = 7;
+  } else {
+    float lo, inv_w;
+    uint32_t klo;
+    if (a < 2.0f) {
+      klo = a < 0.5f ? 0u : (a < 1.0f ? 1u : (a < 1.5f ? 2u : 3u));
+      lo = 0.5f * (float)klo;
+      inv_w = 2.0f;
+    } else if (a < 4.0f) {
+      klo = a < 3.0f ? 4u : 5u;
+      lo = a < 3.0f ? 2.0f : 3.0f;
+      inv_w = 1.0f;
+    } else {
+      klo = 6;
+      lo = 4.0f;
+      inv_w = 0.5f;
+    }
+    const float f24 = ieee_mul(ieee_mul(ieee_sub(a, lo), inv_w), 16777216.0f);
+    k = klo + (((float)(w >> 8) < f24) ? 1u : 0u);
+  }
+  return sign | k;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Random words of elements 4*blk .. 4*blk+3 of an orientation's flat index
+// space: counter (blk lo, blk hi, step, orient), key = seed.
+__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint32_t step, uint32_t orient, uint64_t blk) {
+  return philox4x32_10(make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), step, orient), (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+
+// NaN -> +0, +-inf -> +- the largest finite value of the input dtype.
+__device__ __forceinline__ float sanitize(float u, uint32_t maxfinite_bits) {
+  const uint32_t b = fbits(u);
+  if ((b & 0x7F800000u) != 0x7F800000u) return u;
+  if (b & 0x7FFFFFu) return 0.0f;
+  return bitsf((b & 0x80000000u) | maxfinite_bits);
+}
+
+}  // namespace fp4q

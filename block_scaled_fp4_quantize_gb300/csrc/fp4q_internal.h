@@ -1,0 +1,71 @@
+// fp4q_internal.h -- launch interfaces shared by the C ABI and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4q {
+
+// Where a kernel takes the outer scale S from.
+enum SSource : int {
+  S_ONE = 0,            // mode none: S = 1, no normalization
+  S_TENSORWISE_WS = 1,  // S = amax / denom from the tensorwise amax in the workspace
+  S_IN_TILE = 2,        // computed inside the tile kernel (ob divides 64)
+  S_FROM_BUFFER = 3,    // read from the outer-scale buffers (precomputed or pre-pass)
+};
+
+// One quantize / qdq job.  Rowwise quantities are indexed [G, M, K], the
+// columnwise ones [G, K, M].
+struct QuantJob {
+  const void* x;
+  int64_t ld;
+  int in_bf16;
+  int64_t G, M, K;
+  float* residual;  // [G, M, K] contiguous, rowwise only
+  int mode, ob, outer_2d, inner_2d, ue5m3, sr;
+  uint64_t seed;
+  uint32_t step;
+  int do_row, do_col;
+  int s_src;
+  const uint32_t* tw_amax;  // tensorwise amax (binary32 bits), S_TENSORWISE_WS only
+  uint8_t* row_codes;
+  uint8_t* row_scales;
+  float* row_outer;
+  uint8_t* col_codes;
+  uint8_t* col_scales;
+  float* col_outer;
+  float* tile_outer;
+  void* y;          // qdq output [G, M, K] contiguous, or nullptr
+  int out_bf16;
+  int qdq_orient;   // 0: quantize; 1: qdq along K; 2: qdq along M
+};
+
+struct DequantJob {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* outer;
+  void* y;
+  int64_t G, R, C;   // orientation's logical shape
+  int64_t M, K;      // the quantized tensor's shape (2-D scale indexing)
+  int col;           // 1: columnwise buffers (2-D scales read transposed)
+  int mode, ob, outer_2d, ue5m3, out_bf16;
+};
+
+struct MxJob {
+  const void* x;
+  int64_t ld;
+  int in_bf16, out_bf16;
+  int64_t G, M, K;
+  void* y;
+};
+
+int num_sms();
+int vec_aligned(const void* p, int64_t bytes_stride);
+
+cudaError_t launch_quant_tile(const QuantJob& j, bool vec, cudaStream_t st);
+cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st);
+cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st);
+cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st);
+cudaError_t launch_mxfp4(const MxJob& j, cudaStream_t st);
+
+}  // namespace fp4q

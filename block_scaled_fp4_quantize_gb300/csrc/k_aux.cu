@@ -1,0 +1,197 @@
+// k_aux.cu -- tensorwise amax, outer-scale pre-pass and dequantize kernels.
+#include "fp4q_device.cuh"
+#include "fp4q_internal.h"
+
+namespace fp4q {
+namespace {
+
+__device__ __forceinline__ uint32_t umax(uint32_t a, uint32_t b) { return a > b ? a : b; }
+
+// |u| bits of element (g, m, k): u = sanitize(x + residual).
+__device__ __forceinline__ uint32_t abs_u(const QuantJob& j, int64_t g, int64_t m, int64_t k) {
+  const int64_t xi = (g * j.M + m) * j.ld + k;
+  float f = j.in_bf16 ? bitsf((uint32_t)static_cast<const uint16_t*>(j.x)[xi] << 16)
+                      : static_cast<const float*>(j.x)[xi];
+  if (j.residual) f = ieee_add(f, j.residual[(g * j.M + m) * j.K + k]);
+  f = sanitize(f, j.in_bf16 ? 0x7F7F0000u : 0x7F7FFFFFu);
+  return abs_bits(f);
+}
+
+__device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* sh) {
+  for (int o = 16; o > 0; o >>= 1) v = umax(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    v = l < (int)(blockDim.x >> 5) ? sh[l] : 0u;
+    for (int o = 16; o > 0; o >>= 1) v = umax(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  }
+  return v;  // valid in thread 0
+}
+
+// Tensorwise amax: grid-stride over all elements, one atomicMax per CTA.
+__global__ void __launch_bounds__(256) tensor_amax_kernel(const QuantJob j, uint32_t* amax) {
+  __shared__ uint32_t sh[8];
+  const int64_t n = j.G * j.M * j.K;
+  uint32_t v = 0;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k = e % j.K, gm = e / j.K;
+    v = umax(v, abs_u(j, gm / j.M, gm % j.M, k));
+  }
+  v = block_max(v, sh);
+  if (threadIdx.x == 0) atomicMax(amax, v);
+}
+
+// 1-D rowwise outer scales (ob along K): one warp per outer block.
+__global__ void __launch_bounds__(256) outer_row_kernel(const QuantJob j) {
+  const ScaleFmt f = scale_fmt(j.ue5m3);
+  const int64_t nb_k = j.K / j.ob;
+  const int64_t nblk = j.G * j.M * nb_k;
+  const int lane = threadIdx.x & 31;
+  for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblk;
+       b += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t jb = b % nb_k, gm = b / nb_k;
+    uint32_t v = 0;
+    for (int64_t k = jb * j.ob + lane; k < (jb + 1) * j.ob; k += 32) v = umax(v, abs_u(j, gm / j.M, gm % j.M, k));
+    for (int o = 16; o > 0; o >>= 1) v = umax(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    if (lane == 0) j.row_outer[b] = ieee_div(bitsf(v), f.denom);
+  }
+}
+
+// 1-D columnwise outer scales (ob along M): one thread per (g, block, k).
+__global__ void __launch_bounds__(256) outer_col_kernel(const QuantJob j) {
+  const ScaleFmt f = scale_fmt(j.ue5m3);
+  const int64_t nb_m = j.M / j.ob;
+  const int64_t n = j.G * nb_m * j.K;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k = e % j.K, ib = (e / j.K) % nb_m, g = e / (j.K * nb_m);
+    uint32_t v = 0;
+    for (int64_t m = ib * j.ob; m < (ib + 1) * j.ob; ++m) v = umax(v, abs_u(j, g, m, k));
+    j.col_outer[(g * j.K + k) * nb_m + ib] = ieee_div(bitsf(v), f.denom);
+  }
+}
+
+// 2-D outer scales (ob x ob): one CTA per block.
+__global__ void __launch_bounds__(256) outer_2d_kernel(const QuantJob j) {
+  __shared__ uint32_t sh[8];
+  const ScaleFmt f = scale_fmt(j.ue5m3);
+  const int64_t nb_m = j.M / j.ob, nb_k = j.K / j.ob;
+  const int64_t nblk = j.G * nb_m * nb_k;
+  const int64_t ob2 = (int64_t)j.ob * j.ob;
+  for (int64_t b = blockIdx.x; b < nblk; b += gridDim.x) {
+    const int64_t jb = b % nb_k, ib = (b / nb_k) % nb_m, g = b / (nb_k * nb_m);
+    uint32_t v = 0;
+    for (int64_t e = threadIdx.x; e < ob2; e += blockDim.x)
+      v = umax(v, abs_u(j, g, ib * j.ob + e / j.ob, jb * j.ob + e % j.ob));
+    v = block_max(v, sh);
+    if (threadIdx.x == 0) j.tile_outer[b] = ieee_div(bitsf(v), f.denom);
+    __syncthreads();
+  }
+}
+
+// Dequantize: one thread per 1 x 16 microblock.
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256) dequant_kernel(const DequantJob j, int vec_out) {
+  const ScaleFmt f = scale_fmt(j.ue5m3);
+  const int64_t nmb = j.G * j.R * (j.C / 16);
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nmb; b += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t cb = b % (j.C / 16), gr = b / (j.C / 16);
+    const int64_t r = gr % j.R, g = gr / j.R;
+    const int64_t c0 = cb * 16;
+    float S = 1.0f;
+    const bool outer = j.mode != 0;
+    if (j.mode == 1) {
+      S = j.outer[0];
+    } else if (j.mode == 2) {
+      if (!j.outer_2d) {
+        S = j.outer[(g * j.R + r) * (j.C / j.ob) + c0 / j.ob];
+      } else {
+        const int64_t mi = j.col ? c0 : r, kj = j.col ? r : c0;  // element's (m, k) in x
+        S = j.outer[(g * (j.M / j.ob) + mi / j.ob) * (j.K / j.ob) + kj / j.ob];
+      }
+    }
+    const float s = dec_scale(j.scales[b], f);
+    const uint2 cw = *reinterpret_cast<const uint2*>(j.codes + b * 8);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t byte = ((i < 4 ? cw.x : cw.y) >> (8 * (i & 3))) & 0xFFu;
+      float g0, g1;
+      e2m1x2_decode(byte, g0, g1);
+      float d0 = ieee_mul(g0, s), d1 = ieee_mul(g1, s);
+      if (outer) { d0 = ieee_mul(d0, S); d1 = ieee_mul(d1, S); }
+      v[2 * i] = d0;
+      v[2 * i + 1] = d1;
+    }
+    const int64_t yi = b * 16;
+    if (OUT_BF16) {
+      uint16_t* p = static_cast<uint16_t*>(j.y) + yi;
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+      if (vec_out) {
+        reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { p[2 * i] = (uint16_t)(w[i] & 0xFFFFu); p[2 * i + 1] = (uint16_t)(w[i] >> 16); }
+      }
+    } else {
+      float* p = static_cast<float*>(j.y) + yi;
+      if (vec_out) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) reinterpret_cast<float4*>(p)[i / 4] = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p[i] = v[i];
+      }
+    }
+  }
+}
+
+int grid_for(int64_t work_items, int threads, int per_sm) {
+  const int64_t need = (work_items + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms() * per_sm;
+  int64_t g = need < cap ? need : cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  tensor_amax_kernel<<<grid_for(j.G * j.M * j.K, 256, 8), 256, 0, st>>>(j, amax_ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st) {
+  if (j.outer_2d) {
+    const int64_t nblk = j.G * (j.M / j.ob) * (j.K / j.ob);
+    const int64_t cap = (int64_t)num_sms() * 8;
+    outer_2d_kernel<<<(int)(nblk < cap ? nblk : cap), 256, 0, st>>>(j);
+    return cudaGetLastError();
+  }
+  if (j.do_row) {
+    outer_row_kernel<<<grid_for(j.G * j.M * (j.K / j.ob) * 32, 256, 8), 256, 0, st>>>(j);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (j.do_col) {
+    outer_col_kernel<<<grid_for(j.G * (j.M / j.ob) * j.K, 256, 8), 256, 0, st>>>(j);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st) {
+  const int64_t nmb = j.G * j.R * (j.C / 16);
+  const int vec = vec_aligned(j.y, 16);
+  const int grid = grid_for(nmb, 256, 8);
+  if (j.out_bf16) dequant_kernel<true><<<grid, 256, 0, st>>>(j, vec);
+  else dequant_kernel<false><<<grid, 256, 0, st>>>(j, vec);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4q

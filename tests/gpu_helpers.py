@@ -1,0 +1,79 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path and the oracle on
+the same host bytes and compare their outputs bit for bit."""
+import numpy as np
+import torch
+
+import block_scaled_fp4_quantize_gb300 as fq
+
+ROW, COL = 1, 2
+
+
+def host_np(t: torch.Tensor) -> np.ndarray:
+    """Numpy copy of a CPU/CUDA tensor; bf16 as uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_kw(kw):
+    """Translate binding keyword arguments to the oracle's."""
+    o = {}
+    o["mode"] = kw.get("mode", "none")
+    o["ob"] = kw.get("outer_block_size", 0)
+    o["outer_2d"] = kw.get("outer_2d", False)
+    o["inner_2d"] = kw.get("inner_2d", False)
+    o["fmt"] = kw.get("scale_format", "e4m3")
+    o["rounding"] = "sr" if kw.get("stochastic", False) else "rne"
+    o["seed"] = kw.get("seed", 0)
+    o["step"] = kw.get("step", 0)
+    return o
+
+
+def gpu_quantize(x_cpu, residual_cpu=None, **kw):
+    x = x_cpu.cuda()
+    r = residual_cpu.cuda() if residual_cpu is not None else None
+    q = fq.quantize(x, residual=r, **kw)
+    torch.cuda.synchronize()
+    out = {}
+    for k in ("row_codes", "row_scales", "row_outer", "col_codes", "col_scales", "col_outer", "tile_outer"):
+        v = getattr(q, k)
+        out[k] = None if v is None else host_np(v)
+    if r is not None:
+        out["residual"] = host_np(r)
+    return q, out
+
+
+def oracle_quantize(orc, x_cpu, residual_cpu=None, **kw):
+    x = host_np(x_cpu)
+    if x.ndim == 2:
+        x = x[None]
+    mask = (ROW if kw.get("rowwise", True) else 0) | (COL if kw.get("columnwise", False) else 0)
+    r = None if residual_cpu is None else host_np(residual_cpu).copy().reshape(x.shape[0], x.shape[1], -1)
+    out = orc.quantize(x, residual=r, out_mask=mask, **oracle_kw(kw))
+    if r is not None:
+        out["residual"] = r
+    return out
+
+
+def assert_same(gpu: dict, ref: dict, keys=None):
+    keys = keys or [k for k in ref if ref[k] is not None]
+    for k in keys:
+        g, r = gpu.get(k), ref[k]
+        assert g is not None, "missing GPU output %s" % k
+        g = np.asarray(g).reshape(r.shape)
+        if r.dtype == np.float32:
+            g, r = g.view(np.uint32), r.view(np.uint32)
+        bad = np.flatnonzero(g.ravel() != r.ravel())
+        assert bad.size == 0, "%s: %d of %d differ; first at %d: gpu %r oracle %r" % (
+            k, bad.size, r.size, bad[0], g.ravel()[bad[0]], r.ravel()[bad[0]])
+
+
+def snr_db(x: np.ndarray, y: np.ndarray) -> float:
+    x = x.astype(np.float64)
+    e = x - y.astype(np.float64)
+    return float(10.0 * np.log10((x * x).sum() / (e * e).sum()))
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)

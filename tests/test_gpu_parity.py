@@ -1,0 +1,332 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
+element by element on the same seeded inputs.  Integer and byte outputs
+(codes, scale bytes) and every binary32 / bf16 value (outer scales,
+residuals, dequantized data) must agree bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp4_quantize_gb300 as fq
+from block_scaled_fp4_quantize_gb300 import workloads as W
+
+from gpu_helpers import (COL, ROW, assert_same, bf16_to_f32, gpu_quantize, host_np, oracle_kw, oracle_quantize,
+                         snr_db)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fq.build()
+
+
+# ----------------------------------------------------------------------------
+# small-shape matrix over every knob (several tiles, ragged tails)
+# ----------------------------------------------------------------------------
+
+SHAPES = {16: (2, 80, 112), 32: (1, 96, 160), 48: (1, 96, 144), 64: (1, 192, 320), 128: (1, 256, 384),
+          0: (2, 80, 176)}
+
+
+def _cases():
+    cases = []
+    for ob in (0, 16, 32, 48, 64, 128):
+        modes = ["none", "tensorwise"] if ob == 0 else ["outer_block"]
+        for mode in modes:
+            for outer_2d in ([False] if ob == 0 else [False, True]):
+                for inner_2d in (False, True):
+                    for fmt in ("e4m3", "ue5m3"):
+                        cases.append(dict(mode=mode, outer_block_size=ob, outer_2d=outer_2d, inner_2d=inner_2d,
+                                          scale_format=fmt))
+    return cases
+
+
+def _id(c):
+    return "%s-ob%d-%s-%s-%s" % (c["mode"], c["outer_block_size"], "2d" if c["outer_2d"] else "1d",
+                                 "in2d" if c["inner_2d"] else "in1d", c["scale_format"])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("case", _cases(), ids=_id)
+def test_quantize_matrix(orc, case, dtype):
+    G, M, K = SHAPES[case["outer_block_size"]]
+    x = W.lognormal((G, M, K), 21, sigma=2.0, dtype=dtype)
+    for mask in ((True, False), (False, True), (True, True)):
+        for stochastic in (False, True):
+            kw = dict(case, rowwise=mask[0], columnwise=mask[1], stochastic=stochastic, seed=7, step=3)
+            _, g = gpu_quantize(x, **kw)
+            r = oracle_quantize(orc, x, **kw)
+            assert_same(g, r)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
+                                dict(mode="outer_block", outer_block_size=64),
+                                dict(mode="outer_block", outer_block_size=48),
+                                dict(mode="outer_block", outer_block_size=32, outer_2d=True),
+                                dict(mode="outer_block", outer_block_size=16, inner_2d=True)],
+                         ids=["none", "tensorwise", "ob64", "ob48", "ob32-2d", "ob16-in2d"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_error_feedback_matrix(orc, kw, dtype, stochastic):
+    G, M, K = 1, 96, 192
+    x = W.lognormal((G, M, K), 22, sigma=1.0, dtype=dtype)
+    r0 = (torch.randn(G, M, K, generator=torch.Generator().manual_seed(5)) * 0.01).float()
+    kw = dict(kw, stochastic=stochastic, seed=11, step=2)
+    _, g = gpu_quantize(x, residual_cpu=r0, **kw)
+    r = oracle_quantize(orc, x, residual_cpu=r0, **kw)
+    assert_same(g, r)
+
+
+@pytest.mark.parametrize("axis", [-1, 0])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
+                                dict(mode="outer_block", outer_block_size=64),
+                                dict(mode="outer_block", outer_block_size=64, outer_2d=True),
+                                dict(mode="outer_block", outer_block_size=32, inner_2d=True),
+                                dict(mode="outer_block", outer_block_size=128)],
+                         ids=["none", "tensorwise", "ob64", "ob64-2d", "ob32-in2d", "ob128"])
+def test_qdq_matrix(orc, kw, axis, out_dtype):
+    x = W.lognormal((2, 128, 256), 23, sigma=1.5)
+    orient = ROW if axis == -1 else COL
+    for stochastic in (False, True):
+        k2 = dict(kw, stochastic=stochastic, seed=3, step=9)
+        y, outer = fq.qdq(x.cuda(), axis=axis, out_dtype=out_dtype, **k2)
+        ref, bufs = orc.qdq(host_np(x), orient=orient, out_dtype="bf16" if out_dtype == torch.bfloat16 else "fp32",
+                            **oracle_kw(k2))
+        assert_same({"y": host_np(y)}, {"y": ref})
+        ob = [v for v in bufs.values() if v is not None]
+        if ob:
+            assert_same({"o": host_np(outer)}, {"o": ob[0]})
+
+
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_qdq_error_feedback(orc, stochastic):
+    x = W.lognormal((1, 64, 512), 24, sigma=1.0, dtype=torch.float32)
+    r0 = (torch.randn(1, 64, 512, generator=torch.Generator().manual_seed(6)) * 0.05).float()
+    rd = r0.cuda()
+    kw = dict(mode="outer_block", outer_block_size=64, stochastic=stochastic, seed=1, step=4)
+    y, _ = fq.qdq(x.cuda(), residual=rd, **kw)
+    ro = host_np(r0).copy()
+    ref, _ = orc.qdq(host_np(x), residual=ro, **oracle_kw(kw))
+    assert_same({"y": host_np(y), "r": host_np(rd)}, {"y": ref, "r": ro})
+
+
+@pytest.mark.parametrize("orient", ["row", "col"])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
+                                dict(mode="outer_block", outer_block_size=64),
+                                dict(mode="outer_block", outer_block_size=32, outer_2d=True),
+                                dict(mode="outer_block", outer_block_size=64, scale_format="ue5m3")],
+                         ids=["none", "tensorwise", "ob64", "ob32-2d", "ob64-ue5m3"])
+def test_dequantize_matrix(orc, kw, orient, out_dtype):
+    G, M, K = 2, 128, 192
+    x = W.lognormal((G, M, K), 25, sigma=2.0)
+    q, g = gpu_quantize(x, rowwise=True, columnwise=True, **kw)
+    y = fq.dequantize(q, orient=orient, out_dtype=out_dtype)
+    name = "row" if orient == "row" else "col"
+    okw = oracle_kw(kw)
+    ref = orc.dequantize(g[name + "_codes"], g[name + "_scales"], g, G=G, M=M, K=K,
+                         orient=ROW if orient == "row" else COL,
+                         out_dtype="bf16" if out_dtype == torch.bfloat16 else "fp32",
+                         mode=okw["mode"], ob=okw["ob"], outer_2d=okw["outer_2d"], fmt=okw["fmt"])
+    assert_same({"y": host_np(y)}, {"y": ref})
+
+
+def test_precomputed_outer_scale_round_trip(orc):
+    x = W.activations(M=128, K=256, n_cols=2, n_rows=1)
+    for kw in (dict(mode="outer_block", outer_block_size=64, outer_2d=True),
+               dict(mode="outer_block", outer_block_size=64), dict(mode="tensorwise")):
+        q1, g1 = gpu_quantize(x, rowwise=True, columnwise=True, **kw)
+        q2 = fq.quantize(x.cuda(), rowwise=True, columnwise=True, precomputed_outer=q1, **kw)
+        for k in ("row_codes", "row_scales", "col_codes", "col_scales"):
+            assert torch.equal(getattr(q2, k).cpu(), torch.from_numpy(g1[k]))
+
+
+# ----------------------------------------------------------------------------
+# views, alignment, empties, the fast-math build
+# ----------------------------------------------------------------------------
+
+def test_strided_and_misaligned_views(orc):
+    base = W.lognormal((1, 96, 208), 26, sigma=1.0)
+    base_d = base.cuda()
+    # ld = 208 with the base pointer offset by one bf16 element; ld = 208 aligned
+    for sl in (slice(1, 193), slice(0, 192)):
+        xv, xv_d = base[:, :, sl], base_d[:, :, sl]
+        for kw in (dict(mode="outer_block", outer_block_size=32, columnwise=True), dict(mode="tensorwise")):
+            q = fq.quantize(xv_d, **kw)
+            ref = oracle_quantize(orc, xv.contiguous(), **kw)
+            got = {k: host_np(getattr(q, k)) for k in ref if getattr(q, k) is not None}
+            assert_same(got, ref)
+        y = fq.mxfp4_fake_quantize(xv_d)
+        ref = orc.mxfp4_fake_quantize(host_np(xv.contiguous()))
+        assert_same({"y": host_np(y)}, {"y": ref})
+
+
+def test_empty_inputs():
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    q = fq.quantize(x, mode="tensorwise")
+    torch.cuda.synchronize()
+    assert q.tile_outer.item() == 0.0
+    assert fq.mxfp4_fake_quantize(x).numel() == 0
+    y, _ = fq.qdq(torch.empty(16, 0, device="cuda"))
+    assert y.numel() == 0
+
+
+def test_fast_math_build_gives_identical_bits():
+    """MXFP4 QAT page, 'Correctness': a fast-math dual-build bit-parity gate."""
+    from block_scaled_fp4_quantize_gb300 import _capi
+
+    std = _capi.load()
+    fm = _capi.load(fast_math=True)
+    xa = W.lognormal((1, 192, 320), 27, sigma=3.0)
+    outs = []
+    for lib in (std, fm):
+        _capi._libs["std"] = lib
+        q = fq.quantize(xa.cuda(), mode="outer_block", outer_block_size=64, rowwise=True, columnwise=True,
+                        stochastic=True, seed=5)
+        y = fq.mxfp4_fake_quantize(W.all_bf16_patterns().cuda())
+        yq, _ = fq.qdq(xa.cuda().float(), mode="tensorwise")
+        outs.append([host_np(t) for t in (q.row_codes, q.row_scales, q.row_outer, q.col_codes, q.col_scales,
+                                          q.col_outer, y, yq)])
+    _capi._libs["std"] = std
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------
+# the five workloads
+# ----------------------------------------------------------------------------
+
+def test_small_nvfp4_quantize_dequantize(orc):
+    """bf16 [256, 512] ~ N(0,1): 1x64 outer blocks, E4M3, RNE, rowwise; then
+    dequantize to bf16."""
+    x = W.small_nvfp4()
+    kw = dict(mode="outer_block", outer_block_size=64)
+    q, g = gpu_quantize(x, **kw)
+    r = oracle_quantize(orc, x, **kw)
+    assert_same(g, r)
+    y = fq.dequantize(q, out_dtype=torch.bfloat16)
+    ref = orc.dequantize(r["row_codes"], r["row_scales"], r, G=1, M=256, K=512, mode="outer_block", ob=64)
+    assert_same({"y": host_np(y)}, {"y": ref})
+
+
+def test_mxfp4_all_bf16_patterns(orc):
+    x = W.all_bf16_patterns()
+    for out_dtype in (torch.bfloat16, torch.float32):
+        y = fq.mxfp4_fake_quantize(x.cuda(), out_dtype=out_dtype)
+        ref = orc.mxfp4_fake_quantize(host_np(x), out_dtype="bf16" if out_dtype == torch.bfloat16 else "fp32")
+        assert_same({"y": host_np(y)}, {"y": ref[0]})
+
+
+def test_mxfp4_fp32_raw_bit_fuzz(orc):
+    """fp32 inputs drawn as raw bit patterns (MXFP4 QAT page, 'Correctness')."""
+    bits = np.random.default_rng(28).integers(0, 2 ** 32, size=(512, 1024), dtype=np.uint64).astype(np.uint32)
+    x = torch.from_numpy(bits.view(np.float32).copy())
+    for out_dtype in (torch.float32, torch.bfloat16):
+        y = fq.mxfp4_fake_quantize(x.cuda(), out_dtype=out_dtype)
+        ref = orc.mxfp4_fake_quantize(bits.view(np.float32), out_dtype="fp32" if out_dtype == torch.float32 else "bf16")
+        assert_same({"y": host_np(y)}, {"y": ref[0]})
+
+
+def test_mxfp4_weight_full_size(orc):
+    """bf16 [8192, 8192] ~ N(0, 0.02) with 0.1 % edge blocks, whole tensor."""
+    x, ids = W.mxfp4_weight()
+    y = fq.mxfp4_fake_quantize(x.cuda())
+    ref = orc.mxfp4_fake_quantize(host_np(x))
+    assert_same({"y": host_np(y)}, {"y": ref[0]})
+    assert len(ids) == 2097
+
+
+def test_activations_full_size(orc):
+    """bf16 [16384, 2880] massive activations: 1x64 outer blocks vs tensorwise,
+    rowwise + columnwise; outer-block SNR is at least the tensorwise one."""
+    x = W.activations()
+    xf = bf16_to_f32(host_np(x))
+    snr = {}
+    for kw in (dict(mode="outer_block", outer_block_size=64), dict(mode="tensorwise")):
+        kw = dict(kw, rowwise=True, columnwise=True)
+        q, g = gpu_quantize(x, **kw)
+        r = oracle_quantize(orc, x, **kw)
+        assert_same(g, r)
+        yr = host_np(fq.dequantize(q, "row", torch.float32))[0]
+        yc = host_np(fq.dequantize(q, "col", torch.float32))[0].T
+        snr[kw["mode"]] = (snr_db(xf, yr), snr_db(xf, yc))
+    assert snr["outer_block"][0] >= snr["tensorwise"][0]
+    assert snr["outer_block"][1] >= snr["tensorwise"][1]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
+def test_moe_experts_full_size(orc, fmt):
+    """32 experts x bf16 [5760, 2880], 1 % outliers x 200: 2-D 64x64 outer
+    scales shared by rowwise and columnwise outputs; experts 0 and 31 are
+    checked against the oracle."""
+    G = 32
+    x = torch.empty(G, 5760, 2880, dtype=torch.bfloat16)
+    for e in range(G):
+        x[e] = W.moe_expert(e)
+    kw = dict(mode="outer_block", outer_block_size=64, outer_2d=True, scale_format=fmt, rowwise=True,
+              columnwise=True)
+    q, g = gpu_quantize(x, **kw)
+    for e in (0, 31):
+        r = oracle_quantize(orc, x[e:e + 1], **kw)
+        ge = {k: (None if v is None else v[e:e + 1]) for k, v in g.items()}
+        assert_same(ge, r)
+
+
+def test_sr_ef_weight_loop(orc):
+    """fp32 [8192, 8192] stored-weight loop W <- qdq(W - 1e-4 g), SR + EF,
+    seed 0, step t; 32 rows checked against the oracle at every step."""
+    T = 500
+    M = K = 8192
+    W0, r0 = W.sr_ef_weight()
+    rows = [0, M - 1] + [int(i) + 1 for i in torch.randperm(M - 2, generator=torch.Generator().manual_seed(3))[:30]]
+    Wd, rd = W0.cuda(), r0.cuda()
+    Wo = host_np(W0)[rows].copy()
+    ro = np.zeros_like(Wo)
+    lr = np.float32(1e-4)
+    idx = torch.tensor(rows, device="cuda")
+    for t in range(T):
+        gd = W.sr_ef_gradient(t, M, K, device="cuda")
+        x = Wd - gd * 1e-4
+        Wd, _ = fq.qdq(x, mode="none", stochastic=True, seed=0, step=t, residual=rd, out_dtype=torch.float32)
+        g_rows = host_np(gd.index_select(0, idx))
+        xo = (Wo - lr * g_rows).astype(np.float32)
+        for n, i in enumerate(rows):
+            r_row = ro[n:n + 1].reshape(1, 1, K)
+            y, _ = orc.qdq(xo[n:n + 1], residual=r_row, mode="none", rounding="sr", seed=0, step=t,
+                           sr_index_base=i * K)
+            Wo[n] = y[0, 0]
+        assert_same({"W": host_np(Wd.index_select(0, idx)), "r": host_np(rd.index_select(0, idx))},
+                    {"W": Wo, "r": ro})
+
+
+def test_sr_mean_on_gpu():
+    """fp4-train 'Correctness': SR of 2.3 averages 2.300 (RTN 2.000)."""
+    blk = torch.full((16,), 2.3)
+    blk[0] = 6.0
+    x = blk.repeat(62500, 2).cuda()
+    for stochastic, want, tol in ((True, 2.3, 0.005), (False, 2.0, 0.0)):
+        y, _ = fq.qdq(x, stochastic=stochastic, seed=0)
+        vals = y.view(62500, 2, 16)[:, :, 1:].double()
+        assert abs(vals.mean().item() - want) <= tol
+
+
+# ----------------------------------------------------------------------------
+# sizes beyond 2^31 elements (64-bit indexing), sampled against the oracle
+# ----------------------------------------------------------------------------
+
+def test_beyond_2p31_elements(orc):
+    M, K = 262400, 8192   # 2.15e9 elements
+    g = torch.Generator("cuda").manual_seed(29)
+    x = torch.randn(M, K, generator=g, device="cuda").to(torch.bfloat16)
+    y = fq.mxfp4_fake_quantize(x)
+    rows = [0, M // 2 + 3, M - 1]
+    xs = host_np(x[rows])
+    assert_same({"y": host_np(y[rows])}, {"y": orc.mxfp4_fake_quantize(xs)[0]})
+    del y
+    q = fq.quantize(x, mode="outer_block", outer_block_size=64)
+    r = orc.quantize(xs, mode="outer_block", ob=64)
+    assert_same({k: host_np(getattr(q, k)[0][rows]) for k in ("row_codes", "row_scales", "row_outer")},
+                {k: r[k][0] for k in ("row_codes", "row_scales", "row_outer")})
