@@ -203,6 +203,29 @@ int fp4_qdq(const fp4q_params_t *p, int orient, const void *x, void *y, float *r
  * scale_format must be at their defaults and rounding RNE. */
 int mxfp4_fake_quantize(const fp4q_params_t *p, const void *x, void *y, void *stream);
 
+/* Bytes of static device scratch behind fp4_quantize_noalloc. */
+#define FP4Q_NOALLOC_SCRATCH_BYTES 256
+
+/* fp4_quantize without a workspace argument, for callers that cannot call
+ * cudaMalloc: code whose device memory is entirely owned by another pool
+ * (a framework's caching allocator, a plugin host that hands out buffers but
+ * no allocator), or code on a path where an allocation is not allowed to
+ * block (cudaMalloc / cudaFree may synchronize the device).  The pages
+ * describe no counterpart of this entry point; it is a deployment
+ * convenience.
+ *   Same parameters, outputs and results as fp4_quantize.  The scratch comes
+ *   from a static device array of FP4Q_NOALLOC_SCRATCH_BYTES bytes that every
+ *   device loading the library holds until the process exits; a call whose
+ *   parameters need more returns FP4Q_ERR_WORKSPACE.  The call allocates
+ *   nothing.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   All calls share the array and leave their last contents in it; the part
+ *   that must start at zero is cleared by every call, but calls that overlap
+ *   on the GPU (for example on two streams) race on it. */
+int fp4_quantize_noalloc(const fp4q_params_t *p, const void *x, const fp4q_outputs_t *out, float *residual,
+                         void *stream);
+
 /* Static string naming a status code. */
 const char *fp4q_status_string(int status);
 
