@@ -4,6 +4,7 @@
 // caller's stream.  Validation happens before any launch, so an error other
 // than FP4Q_ERR_CUDA leaves the stream untouched.
 #include <cstdint>
+#include <cstdlib>
 
 #include "fp4q.h"
 #include "fp4q_internal.h"
@@ -33,6 +34,11 @@ using namespace fp4q;
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0u; }
+
+bool getenv_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v && v[0] && v[0] != '0';
+}
 
 int esize(int32_t dt) { return dt == FP4Q_BF16 ? 2 : 4; }
 
@@ -128,6 +134,15 @@ int prepare_outer(const fp4q_params_t* p, QuantJob& j, void* ws, cudaStream_t st
   return launch_outer_prepass(j, st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }
 
+// The fast cast-transpose kernel takes 16-byte-aligned data with 1 x 16
+// inner blocks; everything else (16 x 16 inner blocks, unaligned views) runs
+// in the general tile kernel.
+int launch_quantizer(const QuantJob& j, bool vec, cudaStream_t st) {
+  const bool fast = vec && ct_supports(j) && !getenv_flag("FP4Q_GENERAL_KERNEL");
+  const cudaError_t e = fast ? launch_ct(j, st) : launch_quant_tile(j, vec, st);
+  return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
 bool vec_ok(const fp4q_params_t* p, const void* x, const float* residual, const void* y) {
   return vec_aligned(x, p->ld * esize(p->in_dtype)) && (!residual || aligned(residual, 16)) && (!y || aligned(y, 16));
 }
@@ -200,7 +215,7 @@ int fp4_quantize(const fp4q_params_t* p, const void* x, const fp4q_outputs_t* ou
   j.tile_outer = s.tile_outer ? out->tile_outer : nullptr;
   rc = prepare_outer(p, j, workspace, st);
   if (rc) return rc;
-  return launch_quant_tile(j, vec_ok(p, x, residual, nullptr), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+  return launch_quantizer(j, vec_ok(p, x, residual, nullptr), st);
 }
 
 int fp4_qdq(const fp4q_params_t* p, int orient, const void* x, void* y, float* residual, float* outer, void* workspace,
@@ -237,7 +252,7 @@ int fp4_qdq(const fp4q_params_t* p, int orient, const void* x, void* y, float* r
   else if (p->mode == FP4Q_MODE_OUTER_BLOCK) (j.do_row ? j.row_outer : j.col_outer) = outer;
   rc = prepare_outer(p, j, workspace, st);
   if (rc) return rc;
-  return launch_quant_tile(j, vec_ok(p, x, residual, y), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+  return launch_quantizer(j, vec_ok(p, x, residual, y), st);
 }
 
 int fp4_dequantize(const fp4q_params_t* p, int orient, const uint8_t* codes, const uint8_t* scales, const float* outer,

@@ -172,6 +172,74 @@ __device__ __forceinline__ uint4 sr_words(uint64_t seed, uint32_t step, uint32_t
                        (uint32_t)(seed >> 32));
 }
 
+// ---------------------------------------------------------------------------
+// Exact binary32 division without div.rn
+// ---------------------------------------------------------------------------
+
+// RN(1 / s), the IEEE reciprocal.
+__device__ __forceinline__ float ieee_rcp(float s) {
+  float r;
+  asm("rcp.rn.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
+}
+
+// RN(u / S) from r = RN(1 / S) by Markstein's correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): q = RN(u r), e = RN(q S - u)
+// (exact), result RN(q - e r).  Written with the remainder negated so that a
+// zero quotient keeps the sign of u.  Exact whenever S is normal, |u / S| <
+// 2^126 and |u| >= 2^-100 (the remainder is then representable); callers
+// take div.rn outside that range.
+__device__ __forceinline__ float div_markstein(float u, float S, float r) {
+  float x;
+  asm("{\n\t.reg .f32 q, e, nu, nr;\n\tmul.rn.f32 q, %1, %3;\n\tneg.f32 nu, %1;\n\t"
+      "fma.rn.f32 e, q, %2, nu;\n\tneg.f32 nr, %3;\n\tfma.rn.f32 %0, e, nr, q;\n\t}"
+      : "=f"(x) : "f"(u), "f"(S), "f"(r));
+  return x;
+}
+
+// RN(y / d) for a divisor d known in advance through zh = RD(1 / d) and
+// zl = RN(1 / d - zh) (N. Brisebarre, J.-M. Muller, S. K. Raina,
+// "Accelerating correctly rounded floating-point division when the divisor is
+// known in advance", IEEE Trans. Computers 53(8), 2004): RN(y zh + RN(y zl)).
+// Exact for every y whose product y zl does not underflow, for the divisor
+// significands this library uses (integers 1..15 and 21, checked over every
+// dividend significand); zh, zl >= 0 keep the sign of a zero y.
+__device__ __forceinline__ float div_bmr(float y, float zh, float zl) {
+  float r;
+  asm("{\n\t.reg .f32 p;\n\tmul.rn.f32 p, %1, %3;\n\tfma.rn.f32 %0, %1, %2, p;\n\t}"
+      : "=f"(r) : "f"(y), "f"(zh), "f"(zl));
+  return r;
+}
+
+// max(m, |a|, |b|) with NaN propagating and subnormals kept.
+__device__ __forceinline__ float amax3(float m, float a, float b) {
+  float r;
+  asm("{\n\t.reg .f32 x, y;\n\tabs.f32 x, %2;\n\tabs.f32 y, %3;\n\tmax.NaN.f32 %0, %1, x, y;\n\t}"
+      : "=f"(r) : "f"(m), "f"(a), "f"(b));
+  return r;
+}
+
+// S > 0 for a binary32 bit pattern (NaN and negative values are not), without
+// a float compare that -ftz could flush.
+__device__ __forceinline__ bool positive(float S) {
+  const int b = (int)fbits(S);
+  return b > 0 && b <= 0x7F800000;
+}
+// S is a normal, finite, positive binary32.
+__device__ __forceinline__ bool positive_normal(float S) {
+  const uint32_t b = fbits(S);
+  return b >= 0x00800000u && b < 0x7F800000u;
+}
+
+// E4M3 code of v >= 0 (RNE, saturating at 448) by the hardware conversion.
+__device__ __forceinline__ uint32_t enc_e4m3_hw(float v) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, 0f00000000, %1;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(r) : "f"(v));
+  return r & 0xFFu;
+}
+
 // NaN -> +0, +-inf -> +- the largest finite value of the input dtype.
 __device__ __forceinline__ float sanitize(float u, uint32_t maxfinite_bits) {
   const uint32_t b = fbits(u);

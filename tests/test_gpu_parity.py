@@ -48,9 +48,20 @@ def _id(c):
                                  "in2d" if c["inner_2d"] else "in1d", c["scale_format"])
 
 
+@pytest.fixture(params=["fast", "general"])
+def kernel(request, monkeypatch):
+    """Run a test on the fast cast-transpose kernel (where it applies) and on
+    the general tile kernel."""
+    if request.param == "general":
+        monkeypatch.setenv("FP4Q_GENERAL_KERNEL", "1")
+    else:
+        monkeypatch.delenv("FP4Q_GENERAL_KERNEL", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("case", _cases(), ids=_id)
-def test_quantize_matrix(orc, case, dtype):
+def test_quantize_matrix(orc, case, dtype, kernel):
     G, M, K = SHAPES[case["outer_block_size"]]
     x = W.lognormal((G, M, K), 21, sigma=2.0, dtype=dtype)
     for mask in ((True, False), (False, True), (True, True)):
@@ -69,7 +80,7 @@ def test_quantize_matrix(orc, case, dtype):
                                 dict(mode="outer_block", outer_block_size=16, inner_2d=True)],
                          ids=["none", "tensorwise", "ob64", "ob48", "ob32-2d", "ob16-in2d"])
 @pytest.mark.parametrize("stochastic", [False, True])
-def test_error_feedback_matrix(orc, kw, dtype, stochastic):
+def test_error_feedback_matrix(orc, kw, dtype, stochastic, kernel):
     G, M, K = 1, 96, 192
     x = W.lognormal((G, M, K), 22, sigma=1.0, dtype=dtype)
     r0 = (torch.randn(G, M, K, generator=torch.Generator().manual_seed(5)) * 0.01).float()
@@ -87,7 +98,7 @@ def test_error_feedback_matrix(orc, kw, dtype, stochastic):
                                 dict(mode="outer_block", outer_block_size=32, inner_2d=True),
                                 dict(mode="outer_block", outer_block_size=128)],
                          ids=["none", "tensorwise", "ob64", "ob64-2d", "ob32-in2d", "ob128"])
-def test_qdq_matrix(orc, kw, axis, out_dtype):
+def test_qdq_matrix(orc, kw, axis, out_dtype, kernel):
     x = W.lognormal((2, 128, 256), 23, sigma=1.5)
     orient = ROW if axis == -1 else COL
     for stochastic in (False, True):
@@ -239,7 +250,7 @@ def test_mxfp4_weight_full_size(orc):
     assert len(ids) == 2097
 
 
-def test_activations_full_size(orc):
+def test_activations_full_size(orc, kernel):
     """bf16 [16384, 2880] massive activations: 1x64 outer blocks vs tensorwise,
     rowwise + columnwise; outer-block SNR is at least the tensorwise one."""
     x = W.activations()
@@ -258,7 +269,7 @@ def test_activations_full_size(orc):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
-def test_moe_experts_full_size(orc, fmt):
+def test_moe_experts_full_size(orc, fmt, kernel):
     """32 experts x bf16 [5760, 2880], 1 % outliers x 200: 2-D 64x64 outer
     scales shared by rowwise and columnwise outputs; experts 0 and 31 are
     checked against the oracle."""
