@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-kernel table of other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--only", default=None,
+                    help="time only this named non-headline workload (--steps iterations) and print its record")
+    ap.add_argument("--experts", type=int, default=32, help="expert count of the MoE workload with --only")
     return ap.parse_args()
 
 
@@ -192,71 +195,97 @@ def _sets_for(nbytes):
     return max(1, -(-2 * L2_BYTES // max(1, nbytes)))  # enough rotating copies to exceed L2 twice
 
 
-def extra_kernels(peak):
-    """Time the other workloads (kernel only, inputs resident in HBM)."""
+def _extra_workloads():
+    """Named workloads other than the headline, each a function
+    (iters, warmup, opts) -> (description, algorithmic bytes, ms per call,
+    kernel launches per call).  Kernel only, inputs resident in HBM."""
     import torch
 
     import block_scaled_fp4_quantize_gb300 as fq
     from block_scaled_fp4_quantize_gb300 import workloads as W
 
-    out = {}
     dev = torch.device("cuda")
 
-    def rec(name, desc, nbytes, ms, launches):
+    def small_nvfp4_quantize(iters, warmup, opts):
+        x = W.small_nvfp4().to(dev)
+        q = fq.quantize(x, mode="outer_block", outer_block_size=64)
+        ms = _events_time(lambda i: fq.quantize(x, mode="outer_block", outer_block_size=64, out=q), iters, warmup)
+        return "bf16[256,512] 1x64 outer E4M3 RNE rowwise", 262144 + 65536 + 8192 + 8192, ms, 1
+
+    def _activations(mode_kw, nb_out, launches):
+        def run(iters, warmup, opts):
+            xs = [W.activations().to(dev)]
+            nb_in = xs[0].numel() * 2
+            for _ in range(_sets_for(nb_in) - 1):
+                xs.append(xs[0].clone())
+            qs = [fq.quantize(xx, rowwise=True, columnwise=True, **mode_kw) for xx in xs]
+            ms = _events_time(lambda i: fq.quantize(xs[i % len(xs)], rowwise=True, columnwise=True,
+                                                    out=qs[i % len(xs)], **mode_kw), iters, warmup)
+            return ("bf16[16384,2880] massive activations, %s, rowwise+columnwise" % mode_kw["mode"],
+                    nb_in + nb_out, ms, launches)
+        return run
+
+    M, K = 16384, 2880
+    codes = M * K // 2
+
+    def dequantize_activations(iters, warmup, opts):
+        x = W.activations().to(dev)
+        qd = fq.quantize(x, mode="outer_block", outer_block_size=64)
+        yd = torch.empty(1, M, K, dtype=torch.bfloat16, device=dev)
+        ms = _events_time(lambda i: fq.dequantize(qd, "row", torch.bfloat16, out=yd), iters, warmup)
+        return ("codes+scales+S of bf16[16384,2880] -> bf16", codes + M * K // 16 + M * K // 64 * 4 + M * K * 2,
+                ms, 1)
+
+    def _moe(fmt):
+        def run(iters, warmup, opts):
+            G, Me, Ke = opts.get("experts", 32), 5760, 2880
+            g = torch.Generator(dev).manual_seed(0)
+            xe = torch.randn(G, Me, Ke, generator=g, device=dev) * 0.02
+            xe = torch.where(torch.rand(G, Me, Ke, generator=g, device=dev) < 0.01, xe * 200, xe).to(torch.bfloat16)
+            kw = dict(mode="outer_block", outer_block_size=64, outer_2d=True, scale_format=fmt, rowwise=True,
+                      columnwise=True)
+            qe = fq.quantize(xe, **kw)
+            ms = _events_time(lambda i: fq.quantize(xe, out=qe, **kw), iters, warmup)
+            nb = G * Me * Ke * 2 + 2 * (G * Me * Ke // 2) + 2 * (G * Me * Ke // 16) + G * (Me // 64) * (Ke // 64) * 4
+            return "%d x bf16[5760,2880] 2-D 64x64 outer %s rowwise+columnwise" % (G, fmt), nb, ms, 1
+        return run
+
+    def sr_ef_weight_qdq(iters, warmup, opts):
+        g = torch.Generator(dev).manual_seed(0)
+        Wt = torch.randn(8192, 8192, generator=g, device=dev) * 0.02
+        r = torch.zeros_like(Wt)
+        y = torch.empty(1, 8192, 8192, device=dev)
+        ms = _events_time(lambda i: fq.qdq(Wt, stochastic=True, seed=0, step=i, residual=r, out_dtype=torch.float32,
+                                           out=y), iters, warmup)
+        return ("fp32[8192,8192] qdq, E4M3, SR + error feedback (x, r read; r, y written)", 4 * 8192 * 8192 * 4,
+                ms, 1)
+
+    return {
+        "small_nvfp4_quantize": (small_nvfp4_quantize, 200, 10),
+        "activations_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64),
+                                                 2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1), 50, 5),
+        "activations_tensorwise": (_activations(dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4, 3),
+                                   50, 5),
+        "dequantize_activations": (dequantize_activations, 50, 5),
+        "moe_experts_e4m3": (_moe("e4m3"), 20, 3),
+        "moe_experts_ue5m3": (_moe("ue5m3"), 20, 3),
+        "sr_ef_weight_qdq": (sr_ef_weight_qdq, 20, 3),
+    }
+
+
+def extra_kernels(peak, only=None, iters=None, warmup=None, opts=None):
+    """Time the other workloads; returns {name: record}."""
+    import torch
+
+    out = {}
+    for name, (fn, it, wu) in _extra_workloads().items():
+        if only and name != only:
+            continue
+        desc, nbytes, ms, launches = fn(iters or it, wu if warmup is None else warmup, opts or {})
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"workload": desc, "bytes": nbytes, "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
                      "frac_of_hbm": round(gbs / peak, 4), "launches": launches}
-
-    # small NVFP4 quantize + dequantize (launch-bound)
-    x = W.small_nvfp4().to(dev)
-    q = fq.quantize(x, mode="outer_block", outer_block_size=64)
-    ms = _events_time(lambda i: fq.quantize(x, mode="outer_block", outer_block_size=64, out=q), 200, 10)
-    rec("small_nvfp4_quantize", "bf16[256,512] 1x64 outer E4M3 RNE rowwise", 262144 + 65536 + 8192 + 8192, ms, 1)
-
-    # activations: row + col, 1-D outer 64 and tensorwise
-    xs = [W.activations().to(dev)]
-    nb_in = xs[0].numel() * 2
-    for _ in range(_sets_for(nb_in) - 1):
-        xs.append(xs[0].clone())
-    M, K = 16384, 2880
-    codes = M * K // 2
-    for mode, kw, nb_out in (
-            ("outer_block", dict(mode="outer_block", outer_block_size=64), 2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4),
-            ("tensorwise", dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4)):
-        qs = [fq.quantize(xx, rowwise=True, columnwise=True, **kw) for xx in xs]
-        ms = _events_time(lambda i: fq.quantize(xs[i % len(xs)], rowwise=True, columnwise=True, out=qs[i % len(xs)],
-                                                **kw), 50, 5)
-        rec("activations_%s" % mode, "bf16[16384,2880] massive activations, %s, rowwise+columnwise" % mode,
-            nb_in + nb_out, ms, 1 if mode == "outer_block" else 3)
-    qd = fq.quantize(xs[0], mode="outer_block", outer_block_size=64)
-    yd = torch.empty(1, M, K, dtype=torch.bfloat16, device=dev)
-    ms = _events_time(lambda i: fq.dequantize(qd, "row", torch.bfloat16, out=yd), 50, 5)
-    rec("dequantize_activations", "codes+scales+S of bf16[16384,2880] -> bf16", codes + M * K // 16 + M * K // 64 * 4 + M * K * 2, ms, 1)
-    del xs, qs, qd, yd
-
-    # MoE experts: 32 x [5760, 2880], 2-D 64x64 outer scales, row + col
-    G, M, K = 32, 5760, 2880
-    g = torch.Generator(dev).manual_seed(0)
-    xe = (torch.randn(G, M, K, generator=g, device=dev) * 0.02)
-    xe = torch.where(torch.rand(G, M, K, generator=g, device=dev) < 0.01, xe * 200, xe).to(torch.bfloat16)
-    for fmt in ("e4m3", "ue5m3"):
-        kw = dict(mode="outer_block", outer_block_size=64, outer_2d=True, scale_format=fmt, rowwise=True,
-                  columnwise=True)
-        qe = fq.quantize(xe, **kw)
-        ms = _events_time(lambda i: fq.quantize(xe, out=qe, **kw), 20, 3)
-        nb = G * M * K * 2 + 2 * (G * M * K // 2) + 2 * (G * M * K // 16) + G * (M // 64) * (K // 64) * 4
-        rec("moe_experts_%s" % fmt, "32 x bf16[5760,2880] 2-D 64x64 outer %s rowwise+columnwise" % fmt, nb, ms, 1)
-        del qe
-    del xe
-
-    # SR + EF stored-weight update step: fp32 [8192, 8192]
-    Wt = torch.randn(8192, 8192, generator=g, device=dev) * 0.02
-    r = torch.zeros_like(Wt)
-    y = torch.empty(1, 8192, 8192, device=dev)
-    ms = _events_time(lambda i: fq.qdq(Wt, stochastic=True, seed=0, step=i, residual=r, out_dtype=torch.float32,
-                                       out=y), 20, 3)
-    rec("sr_ef_weight_qdq", "fp32[8192,8192] qdq, E4M3, SR + error feedback (x, r read; r, y written)",
-        4 * 8192 * 8192 * 4, ms, 1)
+        torch.cuda.empty_cache()
     return out
 
 
@@ -428,6 +457,17 @@ def main():
             return 0
         ref = argparse.Namespace(rank=0, world=int(os.environ.get("WORLD_SIZE", "1")), local=0)
         print(json.dumps(run_reference(args, ref)))
+        return 0
+    if args.only:
+        import block_scaled_fp4_quantize_gb300 as fq
+
+        fq.build()
+        peak, _ = hbm_peak()
+        rec = extra_kernels(peak, only=args.only, iters=args.steps, warmup=args.warmup,
+                            opts={"experts": args.experts})
+        if not rec:
+            raise SystemExit("unknown workload %r" % args.only)
+        print(json.dumps({"only": args.only, **rec[args.only]}))
         return 0
     dist = Dist()
     try:

@@ -240,6 +240,77 @@ __device__ __forceinline__ uint32_t enc_e4m3_hw(float v) {
   return r & 0xFFu;
 }
 
+// ---------------------------------------------------------------------------
+// Packed binary32 pairs (f32x2, one 64-bit register): two lanes of the same
+// IEEE operation per instruction, round to nearest even, subnormals kept.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Markstein's quotient (see div_markstein) for a pair, from the NEGATED
+// dividends nu = -u: q = RN(nu * -r) = RN(u r), e = RN(q S + nu), x =
+// RN(e * -r + q).  S2 = (S, S), NR2 = (-r, -r).  The zero quotient keeps the
+// sign of u.
+__device__ __forceinline__ uint64_t markstein2(uint64_t nu, uint64_t S2, uint64_t NR2) {
+  const uint64_t q = mul2(nu, NR2);
+  const uint64_t e = fma2(q, S2, nu);
+  return fma2(e, NR2, q);
+}
+
+// Brisebarre-Muller-Raina quotient (see div_bmr) for a pair: RN(y zh + RN(y zl)).
+__device__ __forceinline__ uint64_t bmr2(uint64_t y, uint64_t ZH2, uint64_t ZL2) {
+  return fma2(y, ZH2, mul2(y, ZL2));
+}
+
+// Negated bf16 -> binary32 (low / high half of a bf16x2 word): -(w << 16) and
+// -(w & 0xFFFF0000), one integer instruction each.
+__device__ __forceinline__ float nbf16lo(uint32_t w) { return bitsf(w * 65536u + 0x80000000u); }
+__device__ __forceinline__ float nbf16hi(uint32_t w) { return bitsf((w & 0xFFFF0000u) ^ 0x80000000u); }
+
+// max(|a|, |b|) of bf16x2 lanes with NaN propagating (lane signs garbage).
+__device__ __forceinline__ uint32_t bf16x2_amax(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// max(|a|, |b|) of binary32 (sign garbage), subnormals kept.
+__device__ __forceinline__ float f32_amax(float a, float b) {
+  float r;
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Four pairs -> one word of eight E2M1 codes, RNE with saturation; pair i
+// goes to byte i, its first value in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x8_rne(const float* t) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(t[0]), "f"(t[1]), "f"(t[2]), "f"(t[3]), "f"(t[4]), "f"(t[5]), "f"(t[6]), "f"(t[7]));
+  return r;
+}
+
 // NaN -> +0, +-inf -> +- the largest finite value of the input dtype.
 __device__ __forceinline__ float sanitize(float u, uint32_t maxfinite_bits) {
   const uint32_t b = fbits(u);
