@@ -64,6 +64,8 @@ int vec_aligned(const void* p, int64_t bytes_stride);
 
 cudaError_t launch_quant_tile(const QuantJob& j, bool vec, cudaStream_t st);
 bool ct_supports(const QuantJob& j);
+bool row_supports(const QuantJob& j);
+cudaError_t launch_row(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_ct(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st);
 cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st);

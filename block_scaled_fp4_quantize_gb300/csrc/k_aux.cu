@@ -42,6 +42,95 @@ __global__ void __launch_bounds__(256) tensor_amax_kernel(const QuantJob j, uint
   if (threadIdx.x == 0) atomicMax(amax, v);
 }
 
+// |max| without NaN propagation (a NaN operand yields the other one); the
+// sign of the result is not meaningful.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float absmax_f32(float a, float b) {
+  float r;
+  asm("max.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Sanitized |u| bits from an accumulated NaN-ignoring magnitude maximum of
+// raw inputs: infinity stands for the largest finite value, a NaN (every
+// input NaN) for zero.  Exact because no finite input exceeds that value.
+__device__ __forceinline__ uint32_t fix_abs(uint32_t a, uint32_t inf_bits, uint32_t max_bits) {
+  return a > inf_bits ? 0u : (a == inf_bits ? max_bits : a);
+}
+
+// Vector body of the contiguous tensorwise amax: one 16-byte unit of x (8
+// bf16 or 4 binary32 values), plus its residual, folded into the running
+// maxima.  Without a residual, `acc` is a packed NaN-ignoring maximum
+// (bf16x2 bits, or binary32 bits); with one, sanitized |u| bits.
+template <bool IN_BF16, bool RES>
+__device__ __forceinline__ void amax_unit(const uint4 w, const float* res, uint32_t& acc) {
+  if (!RES) {
+    if (IN_BF16) {
+      acc = absmax_bf16x2(acc, absmax_bf16x2(absmax_bf16x2(w.x, w.y), absmax_bf16x2(w.z, w.w)));
+    } else {
+      acc = fbits(absmax_f32(bitsf(acc), absmax_f32(absmax_f32(bitsf(w.x), bitsf(w.y)),
+                                                     absmax_f32(bitsf(w.z), bitsf(w.w)))));
+    }
+    return;
+  }
+  constexpr int EPV = IN_BF16 ? 8 : 4;
+  const uint32_t mx = IN_BF16 ? 0x7F7F0000u : 0x7F7FFFFFu;
+  float u[EPV];
+  if (IN_BF16) {
+    u[0] = bf16lo(w.x); u[1] = bf16hi(w.x); u[2] = bf16lo(w.y); u[3] = bf16hi(w.y);
+    u[4] = bf16lo(w.z); u[5] = bf16hi(w.z); u[6] = bf16lo(w.w); u[7] = bf16hi(w.w);
+  } else {
+    u[0] = bitsf(w.x); u[1] = bitsf(w.y); u[2] = bitsf(w.z); u[3] = bitsf(w.w);
+  }
+#pragma unroll
+  for (int q = 0; q < EPV / 4; ++q) {
+    const float4 r = reinterpret_cast<const float4*>(res)[q];
+    u[4 * q] = ieee_add(u[4 * q], r.x); u[4 * q + 1] = ieee_add(u[4 * q + 1], r.y);
+    u[4 * q + 2] = ieee_add(u[4 * q + 2], r.z); u[4 * q + 3] = ieee_add(u[4 * q + 3], r.w);
+  }
+#pragma unroll
+  for (int i = 0; i < EPV; ++i) acc = umax(acc, abs_bits(sanitize(u[i], mx)));
+}
+
+// Tensorwise amax of a contiguous tensor (leading dimension K, 16-byte
+// aligned x and residual): four 16-byte loads in flight per thread per
+// iteration, a scalar tail, one atomicMax per CTA.
+template <bool IN_BF16, bool RES>
+__global__ void __launch_bounds__(256) tensor_amax_flat_kernel(const QuantJob j, uint32_t* amax) {
+  __shared__ uint32_t sh[8];
+  constexpr int EPV = IN_BF16 ? 8 : 4;
+  const int64_t n = j.G * j.M * j.K;
+  const int64_t nv = n / EPV;
+  const uint4* xv = static_cast<const uint4*>(j.x);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + 3 * stride < nv; i += 4 * stride) {
+    uint4 w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = __ldcs(xv + i + q * stride);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) amax_unit<IN_BF16, RES>(w[q], RES ? j.residual + (i + q * stride) * EPV : nullptr, acc);
+  }
+  for (; i < nv; i += stride) amax_unit<IN_BF16, RES>(__ldcs(xv + i), RES ? j.residual + i * EPV : nullptr, acc);
+  uint32_t v;
+  if (RES) {
+    v = acc;
+  } else if (IN_BF16) {
+    v = umax(fix_abs(acc & 0x7FFFu, 0x7F80u, 0x7F7Fu), fix_abs((acc >> 16) & 0x7FFFu, 0x7F80u, 0x7F7Fu)) << 16;
+  } else {
+    v = fix_abs(acc & 0x7FFFFFFFu, 0x7F800000u, 0x7F7FFFFFu);
+  }
+  const int64_t e = nv * EPV + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // scalar tail
+  if (e < n) v = umax(v, abs_u(j, 0, 0, e));
+  v = block_max(v, sh);
+  if (threadIdx.x == 0) atomicMax(amax, v);
+}
+
 // 1-D rowwise outer scales (ob along K): one warp per outer block.
 __global__ void __launch_bounds__(256) outer_row_kernel(const QuantJob j) {
   const ScaleFmt f = scale_fmt(j.ue5m3);
@@ -161,7 +250,21 @@ int grid_for(int64_t work_items, int threads, int per_sm) {
 cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  tensor_amax_kernel<<<grid_for(j.G * j.M * j.K, 256, 8), 256, 0, st>>>(j, amax_ws);
+  const int64_t n = j.G * j.M * j.K;
+  const bool flat = (j.ld == j.K || j.M * j.G == 1) && vec_aligned(j.x, 0) &&
+                    (!j.residual || vec_aligned(j.residual, 0));
+  if (flat) {
+    const int grid = grid_for(n / (j.in_bf16 ? 8 : 4) / 4 + 1, 256, 4);
+    if (j.in_bf16) {
+      if (j.residual) tensor_amax_flat_kernel<true, true><<<grid, 256, 0, st>>>(j, amax_ws);
+      else tensor_amax_flat_kernel<true, false><<<grid, 256, 0, st>>>(j, amax_ws);
+    } else {
+      if (j.residual) tensor_amax_flat_kernel<false, true><<<grid, 256, 0, st>>>(j, amax_ws);
+      else tensor_amax_flat_kernel<false, false><<<grid, 256, 0, st>>>(j, amax_ws);
+    }
+    return cudaGetLastError();
+  }
+  tensor_amax_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(j, amax_ws);
   return cudaGetLastError();
 }
 

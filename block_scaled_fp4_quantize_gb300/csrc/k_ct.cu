@@ -25,140 +25,12 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
 
 namespace fp4q {
 namespace {
-
-constexpr int TK = 64;
-
-// RD(1/M) and RN(1/M - RD(1/M)) for M = 0..15 (M = 0 unused); see div_bmr.
-__constant__ uint32_t kRcpHi[16] = {0x00000000u, 0x3F800000u, 0x3F000000u, 0x3EAAAAAAu, 0x3E800000u, 0x3E4CCCCCu,
-                                    0x3E2AAAAAu, 0x3E124924u, 0x3E000000u, 0x3DE38E38u, 0x3DCCCCCCu, 0x3DBA2E8Bu,
-                                    0x3DAAAAAAu, 0x3D9D89D8u, 0x3D924924u, 0x3D888888u};
-__constant__ uint32_t kRcpLo[16] = {0x00000000u, 0x00000000u, 0x00000000u, 0x32AAAAABu, 0x00000000u, 0x324CCCCDu,
-                                    0x322AAAABu, 0x32124925u, 0x00000000u, 0x31E38E39u, 0x31CCCCCDu, 0x31A2E8BAu,
-                                    0x31AAAAABu, 0x319D89D9u, 0x31924925u, 0x31888889u};
-// 1/6 split the same way (a / 6 for the inner scale)
-constexpr uint32_t kSixHi = 0x3E2AAAAAu, kSixLo = 0x322AAAABu;
-// 1/2688 (E4M3: 448 * 6 = 21 * 2^7) and 1/688128 (UE5M3: 114688 * 6 = 21 * 2^15)
-constexpr uint32_t kDenHiE4 = 0x39C30C30u, kDenLoE4 = 0x2DC30C31u;
-constexpr uint32_t kDenHiU5 = 0x35C30C30u, kDenLoU5 = 0x29C30C31u;
-
-// amax bits below which the FMA division paths are not used (2^-90)
-constexpr uint32_t kTiny = 0x12800000u;
-
-__device__ __forceinline__ uint32_t umax(uint32_t a, uint32_t b) { return a > b ? a : b; }
-
-// outer scale amax / (scale_max * 6)
-template <bool UE5M3>
-__device__ __forceinline__ float outer_scale(float A) {
-  if (fbits(A) >= kTiny)
-    return div_bmr(A, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
-  return ieee_div(A, UE5M3 ? 688128.0f : 2688.0f);
-}
-
-template <bool UE5M3>
-__device__ __forceinline__ uint32_t encode_scale(float v) {
-  if (UE5M3) return enc_scale(v, scale_fmt(1));
-  return enc_e4m3_hw(v);
-}
-
-// Per-block state of the normalization u -> x' = u / S.
-struct Norm {
-  float S, r;
-  bool none, pos, fast;
-};
-
-// Inner scale of a block with |u| maximum `am` (binary32, finite): returns
-// the code and fills (s, zh, zl) from the table; `n.fast` is narrowed to the
-// range where the Markstein path is exact.
-template <bool UE5M3, class SM>
-__device__ __forceinline__ uint32_t block_scale(const SM& sm, float am, Norm& n, float4& T) {
-  float a;
-  if (n.none) {
-    a = am;
-  } else if (!n.pos) {
-    a = 0.0f;
-  } else {
-    n.fast = n.fast && fbits(am) >= kTiny;
-    a = n.fast ? div_markstein(am, n.S, n.r) : ieee_div(am, n.S);
-    n.fast = n.fast && fbits(a) < 0x7E800000u;
-  }
-  const float v = div_bmr(a, bitsf(kSixHi), bitsf(kSixLo));
-  const uint32_t sc = encode_scale<UE5M3>(v);
-  T = sm.tab[sc];
-  return sc;
-}
-
-
-// Rare path of normalize16 (tiny, subnormal or non-positive scales).
-__device__ __noinline__ float div_slow(float u, float S, bool pos) { return pos ? ieee_div(u, S) : signed_zero(u); }
-
-// x' = u / S for a whole block: one block-uniform branch, the fast path two
-// values per instruction.
-__device__ __forceinline__ void normalize16(const float (&u)[16], float (&x)[16], const Norm& n) {
-  if (n.none) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = u[i];
-  } else if (n.fast) {
-    const float nr = bitsf(fbits(n.r) ^ 0x80000000u);
-    const uint64_t S2 = pk2(n.S, n.S), NR2 = pk2(nr, nr);
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-      const uint64_t nu = pk2(bitsf(fbits(u[i]) ^ 0x80000000u), bitsf(fbits(u[i + 1]) ^ 0x80000000u));
-      upk2(markstein2(nu, S2, NR2), x[i], x[i + 1]);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = div_slow(u[i], n.S, n.pos);
-  }
-}
-
-// 16 values -> 16 codes (two 32-bit words, element 2i in the low nibble of
-// byte i); optional dequantized values (e2m1 * s) * S.
-template <bool SR, bool DEQ>
-__device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, const Norm& n, uint64_t seed,
-                                         uint32_t step, uint32_t orient, uint64_t n0, uint32_t& w0, uint32_t& w1,
-                                         float (&deq)[16]) {
-  float t[16];
-  {
-    const uint64_t ZH2 = pk2(T.y, T.y), ZL2 = pk2(T.z, T.z);
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) upk2(bmr2(pk2(x[i], x[i + 1]), ZH2, ZL2), t[i], t[i + 1]);
-  }
-  uint32_t byte[8];
-  if (!SR && !DEQ) {
-    w0 = e2m1x8_rne(t);
-    w1 = e2m1x8_rne(t + 8);
-    return;
-  }
-  if (SR) {
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint4 rw = sr_words(seed, step, orient, (n0 >> 2) + (uint64_t)w);
-      byte[2 * w] = e2m1_sr(t[4 * w], rw.x) | (e2m1_sr(t[4 * w + 1], rw.y) << 4);
-      byte[2 * w + 1] = e2m1_sr(t[4 * w + 2], rw.z) | (e2m1_sr(t[4 * w + 3], rw.w) << 4);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) byte[i] = e2m1x2_rne(t[2 * i], t[2 * i + 1]);
-  }
-  w0 = __byte_perm(__byte_perm(byte[0], byte[1], 0x0040), __byte_perm(byte[2], byte[3], 0x0040), 0x5410);
-  w1 = __byte_perm(__byte_perm(byte[4], byte[5], 0x0040), __byte_perm(byte[6], byte[7], 0x0040), 0x5410);
-  if (DEQ) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float g0, g1;
-      e2m1x2_decode(byte[i], g0, g1);
-      float d0 = ieee_mul(g0, T.x), d1 = ieee_mul(g1, T.x);
-      if (!n.none) { d0 = ieee_mul(d0, n.S); d1 = ieee_mul(d1, n.S); }
-      deq[2 * i] = d0;
-      deq[2 * i + 1] = d1;
-    }
-  }
-}
 
 template <bool IN_BF16>
 __device__ __forceinline__ void load16(const QuantJob& j, int64_t g, int64_t m, int64_t k, float (&u)[16]) {
@@ -186,26 +58,6 @@ __device__ __forceinline__ void load16(const QuantJob& j, int64_t g, int64_t m, 
       u[4 * q + 2] = ieee_add(u[4 * q + 2], v.z); u[4 * q + 3] = ieee_add(u[4 * q + 3], v.w);
     }
   }
-}
-
-// max |u| over 16 values (NaN propagates), as a tree of magnitude maxima.
-__device__ __forceinline__ float amax_pair(float a, float b) {
-  float r;
-  asm("{\n\t.reg .f32 x, y;\n\tabs.f32 x, %1;\n\tabs.f32 y, %2;\n\tmax.NaN.f32 %0, x, y;\n\t}" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float max_nan(float a, float b) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float amax16(const float (&u)[16]) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = amax_pair(u[2 * i], u[2 * i + 1]);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = max_nan(m[2 * i], m[2 * i + 1]);
-  return max_nan(max_nan(m[0], m[1]), max_nan(m[2], m[3]));
 }
 
 __device__ __forceinline__ void store16(void* y, int out_bf16, int64_t idx, const float (&v)[16]) {
@@ -261,17 +113,23 @@ __device__ __forceinline__ int stage_swz(int row, int unit) {
   return (unit & 8) | ((unit & 7) ^ ((2 * row + (unit >> 3)) & 7));
 }
 
-// Shared memory: [raw 0][raw 1][x' staging][table (s, zh, zl)][2-D and 1-D
-// reductions]
-template <bool IN_BF16>
+// Shared memory: [raw tiles 0 .. NS - 1][x' staging][table (s, zh, zl)]
+// [2-D and 1-D reductions][tile-arrival barriers]
+template <bool IN_BF16, int NS>
 struct Layout {
-  static constexpr int raw0 = 0;
-  static constexpr int raw1 = Geo<IN_BF16>::RAW;
-  static constexpr int stage = 2 * Geo<IN_BF16>::RAW;
+  __host__ __device__ static constexpr int raw(int s) { return s * Geo<IN_BF16>::RAW; }
+  static constexpr int stage = NS * Geo<IN_BF16>::RAW;
   static constexpr int stage_bytes = Geo<IN_BF16>::TM * 64 * 4;
   __host__ __device__ static int tab(bool staged) { return stage + (staged ? stage_bytes : 0); }
   __host__ __device__ static int red(bool staged) { return tab(staged) + 256 * 16; }
-  __host__ __device__ static int total(bool staged) { return red(staged) + (32 + 128 + 2 * 32) * 4 + 16 + 1024; }
+  __host__ __device__ static int total(bool staged) { return red(staged) + (32 + 128 + 2 * 32) * 4 + 8 * NS + 1024; }
+};
+
+// Tile copies in flight per CTA: enough bytes per SM to cover HBM latency
+// at the CTA counts each variant runs (2 with the columnwise pass, 3 without).
+template <bool COL>
+struct Stages {
+  static constexpr int NS = COL ? 3 : 4;
 };
 
 // Set when a tile copy did not arrive within the wait limit (the kernel then
@@ -314,6 +172,12 @@ struct TileIter {
   template <bool IN_BF16>
   __device__ __forceinline__ TilePos pos() const {
     return TilePos{(int64_t)g, (int64_t)tm * Geo<IN_BF16>::TM, (int64_t)tk * 64};
+  }
+  // position of tile `i` (the copy issuer looks ahead of the walk)
+  template <bool IN_BF16>
+  __device__ __forceinline__ TilePos pos_of(int i) const {
+    const int q = i / tiles_k;
+    return TilePos{(int64_t)(q / tiles_m), (int64_t)(q % tiles_m) * Geo<IN_BF16>::TM, (int64_t)(i - q * tiles_k) * 64};
   }
 };
 
@@ -455,7 +319,8 @@ struct OuterCtx {
 template <bool IN_BF16, bool SR, bool COL, bool UE5M3>
 __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
   using G = Geo<IN_BF16>;
-  using L = Layout<IN_BF16>;
+  constexpr int NS = Stages<COL>::NS;
+  using L = Layout<IN_BF16, NS>;
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   // the 128-byte swizzle of the tensor copies needs 1024-byte aligned tiles
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -468,7 +333,7 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
   uint32_t* red2d = reinterpret_cast<uint32_t*>(smem + L::red(staged));  // [32]
   uint32_t* redcol = red2d + 32;                                          // [2][64]
   float2* sr2d = reinterpret_cast<float2*>(redcol + 128);                 // [32]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sr2d + 32);                // [2] tile-arrival barriers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sr2d + 32);                // [NS] tile-arrival barriers
   struct {
     const float4* tab;
   } tv{tab};
@@ -476,24 +341,22 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
   TileIter cur;
   cur.init<IN_BF16>(j);
   if (t == 0) {
-    mbar_init(&bars[0]);
-    mbar_init(&bars[1]);
+#pragma unroll
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (t == 0 && cur.valid()) issue_tile<IN_BF16>(&tmap, cur.pos<IN_BF16>(), smem + L::raw0, &bars[0]);
+  // prologue: the first NS - 1 tiles of this CTA's walk
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < NS - 1; ++s) {
+      const int i = cur.idx + s * (int)gridDim.x;
+      if (i < cur.ntiles) issue_tile<IN_BF16>(&tmap, cur.pos_of<IN_BF16>(i), smem + L::raw(s), &bars[s]);
+    }
+  }
 
   // inner-scale table: value and the divisor split of its reciprocal
-  for (int c = t; c < 256; c += NT) {
-    const int bias = UE5M3 ? 15 : 7;
-    const uint32_t e = (uint32_t)c >> 3, m = (uint32_t)c & 7u;
-    const uint32_t M = e ? 8u + m : m;
-    const int ex = e ? (int)e - 3 - bias : -2 - bias;
-    const uint32_t hi = kRcpHi[M], lo = kRcpLo[M];
-    reinterpret_cast<float4*>(smem + L::tab(staged))[c] =
-        make_float4(dec_scale((uint32_t)c, scale_fmt(UE5M3 ? 1 : 0)), M ? bitsf((uint32_t)((int)hi - ex * 8388608)) : 0.0f,
-                    lo ? bitsf((uint32_t)((int)lo - ex * 8388608)) : 0.0f, 0.0f);
-  }
+  build_scale_table<UE5M3>(reinterpret_cast<float4*>(smem + L::tab(staged)), t, NT);
   if (t < 32) red2d[t] = 0u;
   if (t < 128) redcol[t] = 0u;
   const int ob = j.ob;
@@ -516,20 +379,35 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
                            ((reinterpret_cast<uintptr_t>(j.row_scales) | reinterpret_cast<uintptr_t>(j.col_scales)) & 3u) == 0;
   __syncthreads();
 
+  int slot = 0;
+  uint32_t phase = 0;
   for (int it = 0; cur.valid(); ++it) {
-    unsigned char* raw = smem + ((it & 1) ? L::raw1 : L::raw0);
+    unsigned char* raw = smem + L::raw(slot);
     const TilePos p = cur.pos<IN_BF16>();
+    // refill the slot the previous tile used (every thread has left it)
+    if (t == 0) {
+      const int i = cur.idx + (NS - 1) * (int)gridDim.x;
+      const int s = slot == 0 ? NS - 1 : slot - 1;
+      if (i < cur.ntiles) issue_tile<IN_BF16>(&tmap, cur.pos_of<IN_BF16>(i), smem + L::raw(s), &bars[s]);
+    }
     cur.next();
-    if (t == 0 && cur.valid())
-      issue_tile<IN_BF16>(&tmap, cur.pos<IN_BF16>(), smem + ((it & 1) ? L::raw0 : L::raw1), &bars[(it + 1) & 1]);
     // bounded wait for this tile's copy; on a timeout every thread leaves
-    const bool arrived = mbar_wait(&bars[it & 1], (uint32_t)(it >> 1) & 1u, 1u << 22);
+    const bool arrived = mbar_wait(&bars[slot], phase, 1u << 22);
     if (!__syncthreads_and(arrived)) {
       if (t == 0) {
         atomicExch(&g_tile_timeout, 1u);
-        mbar_wait(&bars[(it + 1) & 1], (uint32_t)((it + 1) >> 1) & 1u, 1u << 22);  // copy in flight
+        // let the later copies still in flight land before the CTA exits
+        for (int d = 1; d < NS; ++d) {
+          const int i = it + d;
+          if (cur.idx + (d - 1) * (int)gridDim.x < cur.ntiles)
+            mbar_wait(&bars[i % NS], (uint32_t)(i / NS) & 1u, 1u << 22);
+        }
       }
       return;
+    }
+    if (++slot == NS) {
+      slot = 0;
+      phase ^= 1u;
     }
 
     const int K32 = (int)j.K, M32 = (int)j.M;
@@ -875,7 +753,7 @@ bool make_tensor_map(const QuantJob& j, CUtensorMap* map) {
 
 template <bool IN_BF16, bool SR, bool COL, bool UE5M3>
 cudaError_t launch_cp(const QuantJob& j, cudaStream_t st) {
-  using L = Layout<IN_BF16>;
+  using L = Layout<IN_BF16, Stages<COL>::NS>;
   CUtensorMap map;
   if (!make_tensor_map<IN_BF16>(j, &map)) return launch_quant_tile(j, true, st);
   auto kern = cp_kernel<IN_BF16, SR, COL, UE5M3>;

@@ -48,14 +48,18 @@ def _id(c):
                                  "in2d" if c["inner_2d"] else "in1d", c["scale_format"])
 
 
-@pytest.fixture(params=["fast", "general"])
+@pytest.fixture(params=["fast", "tile", "general"])
 def kernel(request, monkeypatch):
-    """Run a test on the fast cast-transpose kernel (where it applies) and on
+    """Run a test on each quantizer kernel that can take it: the default
+    choice (flat rowwise kernel for rowwise-only packed inputs, else the
+    cast-transpose tile kernel), the cast-transpose tile kernel alone, and
     the general tile kernel."""
+    monkeypatch.delenv("FP4Q_GENERAL_KERNEL", raising=False)
+    monkeypatch.delenv("FP4Q_NO_ROW_KERNEL", raising=False)
     if request.param == "general":
         monkeypatch.setenv("FP4Q_GENERAL_KERNEL", "1")
-    else:
-        monkeypatch.delenv("FP4Q_GENERAL_KERNEL", raising=False)
+    elif request.param == "tile":
+        monkeypatch.setenv("FP4Q_NO_ROW_KERNEL", "1")
     return request.param
 
 
@@ -183,6 +187,53 @@ def test_empty_inputs():
     assert fq.mxfp4_fake_quantize(x).numel() == 0
     y, _ = fq.qdq(torch.empty(16, 0, device="cuda"))
     assert y.numel() == 0
+
+
+def _plant(x, seed, n_nan=0, n_pinf=0, n_ninf=0):
+    """Copy of x with NaN / +inf / -inf planted at seeded positions."""
+    x = x.clone()
+    g = torch.Generator("cpu").manual_seed(seed)
+    flat = x.view(-1)
+    pos = torch.randperm(flat.numel(), generator=g)
+    at = 0
+    for val, cnt in ((float("nan"), n_nan), (float("inf"), n_pinf), (float("-inf"), n_ninf)):
+        flat[pos[at:at + cnt]] = val
+        at += cnt
+    return x
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(1, 96, 208), (2, 1024, 8192)], ids=["small", "multi-wave"])
+def test_tensorwise_amax_special_values(orc, dtype, shape):
+    """The tensorwise outer scale over inputs with NaN (ignored), infinities
+    (the largest finite value), a negative extreme, subnormal-only and
+    all-NaN tensors; small and multi-wave sizes of the contiguous amax."""
+    base = W.lognormal(shape, 31, sigma=2.0, dtype=dtype)
+    tiny = (W.lognormal(shape, 32, sigma=0.5) * 1e-39).to(dtype) if dtype == torch.bfloat16 else \
+        (W.lognormal(shape, 32, sigma=0.5, dtype=torch.float32) * 1e-42)
+    neg = base.clone()
+    neg.view(-1)[12345 % neg.numel()] = -3.0e4
+    cases = [base, _plant(base, 1, n_nan=7), _plant(base, 2, n_nan=3, n_pinf=1),
+             _plant(base, 3, n_ninf=2), neg, tiny, torch.full(shape, float("nan"), dtype=dtype)]
+    for x in cases:
+        kw = dict(mode="tensorwise", rowwise=True)
+        _, g = gpu_quantize(x, **kw)
+        r = oracle_quantize(orc, x, **kw)
+        assert_same(g, r)
+
+
+def test_tensorwise_amax_with_residual_beyond_bf16_range(orc):
+    """x + residual in binary32 can exceed the largest finite bf16 while an
+    infinite input saturates to it: the sum is the tensor maximum."""
+    x = W.lognormal((1, 64, 256), 33, sigma=1.0)
+    x.view(-1)[5] = 3.3e38
+    x.view(-1)[900] = float("inf")
+    res = torch.zeros(1, 64, 256, dtype=torch.float32)
+    res.view(-1)[5] = 1.0e37
+    kw = dict(mode="tensorwise", rowwise=True)
+    _, g = gpu_quantize(x, res.clone(), **kw)
+    r = oracle_quantize(orc, x, res.clone(), **kw)
+    assert_same(g, r)
 
 
 def test_fast_math_build_gives_identical_bits():
