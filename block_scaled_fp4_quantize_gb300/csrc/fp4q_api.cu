@@ -138,12 +138,15 @@ int prepare_outer(const fp4q_params_t* p, QuantJob& j, void* ws, cudaStream_t st
 // streams through the flat rowwise kernel; other 16-byte-aligned work with
 // 1 x 16 inner blocks runs in the cast-transpose tile kernel; everything
 // else (16 x 16 inner blocks, unaligned views) in the general tile kernel.
-// FP4Q_GENERAL_KERNEL=1 forces the general kernel, FP4Q_NO_ROW_KERNEL=1 skips
-// the flat one (both for parity testing of each path).
+// Columnwise bf16 quantize takes the bf16 cast-transpose kernel.
+// FP4Q_GENERAL_KERNEL=1 forces the general kernel; FP4Q_NO_ROW_KERNEL=1 and
+// FP4Q_NO_CTB_KERNEL=1 skip the flat and the bf16 cast-transpose kernels
+// (for parity testing of each path).
 int launch_quantizer(const QuantJob& j, bool vec, cudaStream_t st) {
   const bool fast = vec && ct_supports(j) && !getenv_flag("FP4Q_GENERAL_KERNEL");
   cudaError_t e;
   if (fast && row_supports(j) && !getenv_flag("FP4Q_NO_ROW_KERNEL")) e = launch_row(j, st);
+  else if (fast && ctb_supports(j) && !getenv_flag("FP4Q_NO_CTB_KERNEL") && launch_ctb(j, st, &e)) {}
   else if (fast) e = launch_ct(j, st);
   else e = launch_quant_tile(j, vec, st);
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;

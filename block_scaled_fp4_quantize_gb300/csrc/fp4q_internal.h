@@ -65,6 +65,8 @@ int vec_aligned(const void* p, int64_t bytes_stride);
 cudaError_t launch_quant_tile(const QuantJob& j, bool vec, cudaStream_t st);
 bool ct_supports(const QuantJob& j);
 bool row_supports(const QuantJob& j);
+bool ctb_supports(const QuantJob& j);
+bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 cudaError_t launch_row(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_ct(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st);

@@ -1,0 +1,107 @@
+// fp4q_tma.cuh -- tile walk and tensor-memory-access (TMA) copies shared by
+// the tile kernels: a grid-stride walk over TM x 64 tiles of a [G, M, K]
+// tensor, mbarrier-completed 3-D tensor copies with bounded waits, and the
+// driver entry point that encodes tensor maps.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "fp4q_internal.h"
+
+namespace fp4q {
+namespace {
+
+struct TilePos {
+  int64_t g, m0, k0;
+};
+
+// Grid-stride walk over tiles without per-tile divisions (tile counts fit
+// 32 bits: 2^31 tiles would be 2^44 elements).
+struct TileIter {
+  int tiles_k, tiles_m, ntiles, idx, tk, tm, g, dk, dm, dg;
+  template <int TM>
+  __device__ __forceinline__ void init(const QuantJob& j) {
+    tiles_k = (int)((j.K + 63) / 64);
+    tiles_m = (int)((j.M + TM - 1) / TM);
+    ntiles = (int)(j.G * tiles_m * tiles_k);
+    idx = (int)blockIdx.x;
+    tk = idx % tiles_k;
+    tm = (idx / tiles_k) % tiles_m;
+    g = idx / (tiles_k * tiles_m);
+    const int step = (int)gridDim.x;
+    dk = step % tiles_k;
+    dm = (step / tiles_k) % tiles_m;
+    dg = step / (tiles_k * tiles_m);
+  }
+  __device__ __forceinline__ bool valid() const { return idx < ntiles; }
+  __device__ __forceinline__ void next() {
+    idx += (int)gridDim.x;
+    tk += dk;
+    int c = 0;
+    if (tk >= tiles_k) { tk -= tiles_k; c = 1; }
+    tm += dm + c;
+    c = 0;
+    if (tm >= tiles_m) { tm -= tiles_m; c = 1; }
+    g += dg + c;
+  }
+  template <int TM>
+  __device__ __forceinline__ TilePos pos() const {
+    return TilePos{(int64_t)g, (int64_t)tm * TM, (int64_t)tk * 64};
+  }
+  // position of tile `i` (the copy issuer looks ahead of the walk)
+  template <int TM>
+  __device__ __forceinline__ TilePos pos_of(int i) const {
+    const int q = i / tiles_k;
+    return TilePos{(int64_t)(q / tiles_m), (int64_t)(q % tiles_m) * TM, (int64_t)(i - q * tiles_k) * 64};
+  }
+};
+
+// ---- tensor-memory-access (TMA) tile loads, completion on an mbarrier ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// Wait for phase `parity` of the barrier, giving up after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// One 3-D tensor copy (K, M, G) of a box into shared memory.
+__device__ __forceinline__ void tma_load3(void* dst, const CUtensorMap* map, int k, int m, int g, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(k), "r"(m), "r"(g), "r"(smem_u32(bar))
+      : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+}  // namespace fp4q

@@ -51,15 +51,17 @@ def _id(c):
 @pytest.fixture(params=["fast", "tile", "general"])
 def kernel(request, monkeypatch):
     """Run a test on each quantizer kernel that can take it: the default
-    choice (flat rowwise kernel for rowwise-only packed inputs, else the
-    cast-transpose tile kernel), the cast-transpose tile kernel alone, and
-    the general tile kernel."""
-    monkeypatch.delenv("FP4Q_GENERAL_KERNEL", raising=False)
-    monkeypatch.delenv("FP4Q_NO_ROW_KERNEL", raising=False)
+    choice (flat rowwise kernel for rowwise-only packed inputs, the bf16
+    cast-transpose kernel for columnwise bf16, else the cast-transpose tile
+    kernel), the cast-transpose tile kernel alone, and the general tile
+    kernel."""
+    for v in ("FP4Q_GENERAL_KERNEL", "FP4Q_NO_ROW_KERNEL", "FP4Q_NO_CTB_KERNEL"):
+        monkeypatch.delenv(v, raising=False)
     if request.param == "general":
         monkeypatch.setenv("FP4Q_GENERAL_KERNEL", "1")
     elif request.param == "tile":
         monkeypatch.setenv("FP4Q_NO_ROW_KERNEL", "1")
+        monkeypatch.setenv("FP4Q_NO_CTB_KERNEL", "1")
     return request.param
 
 
@@ -220,6 +222,25 @@ def test_tensorwise_amax_special_values(orc, dtype, shape):
         _, g = gpu_quantize(x, **kw)
         r = oracle_quantize(orc, x, **kw)
         assert_same(g, r)
+
+
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
+                                dict(mode="outer_block", outer_block_size=16),
+                                dict(mode="outer_block", outer_block_size=64),
+                                dict(mode="outer_block", outer_block_size=32, outer_2d=True),
+                                dict(mode="outer_block", outer_block_size=64, outer_2d=True, scale_format="ue5m3")],
+                         ids=["none", "tensorwise", "ob16", "ob64", "ob32-2d", "ob64-2d-ue5m3"])
+def test_nonfinite_inputs_every_orientation(orc, kw, kernel):
+    """Every bf16 bit pattern (NaN, infinities, subnormals, both zeros) as a
+    [256, 256] tensor, rowwise and columnwise, RNE and SR: the sanitizing
+    rule (NaN -> +0, +-inf -> +-largest finite) on each kernel path."""
+    x = W.all_bf16_patterns()
+    for mask in ((True, False), (False, True), (True, True)):
+        for stochastic in (False, True):
+            k = dict(kw, rowwise=mask[0], columnwise=mask[1], stochastic=stochastic, seed=11, step=2)
+            _, g = gpu_quantize(x, **k)
+            r = oracle_quantize(orc, x, **k)
+            assert_same(g, r)
 
 
 def test_tensorwise_amax_with_residual_beyond_bf16_range(orc):
