@@ -122,33 +122,22 @@ __device__ __forceinline__ void e2m1x2_decode(uint32_t byte, float& lo, float& h
 
 // Stochastic rounding of t onto the E2M1 grid with the 32-bit random word w:
 // between neighbours lo < |t| < hi the result is hi iff (w >> 8) < f * 2^24,
-// f = (|t| - lo) / (hi - lo).  Every step is exact in binary32.
+// f = (|t| - lo) / (hi - lo).  Branch-free: the grid spacing is 1/2 on
+// [0, 2), 1 on [2, 4) and 2 on [4, 6), so y = |t| / spacing (exact) has
+// lo / spacing = floor(y) and f = y - floor(y) (exact); floor(y) comes from
+// one add rounded toward -inf onto 1.5 * 2^23, whose low bits then hold it.
 __device__ __forceinline__ uint32_t e2m1_sr(float t, uint32_t w) {
   const uint32_t sign = (fbits(t) >> 28) & 8u;
   const float a = bitsf(abs_bits(t));
-  uint32_t k;
-  if (!(a < 6.0f)) {
-    k = 7;
-  } else {
-    float lo, inv_w;
-    uint32_t klo;
-    if (a < 2.0f) {
-      klo = a < 0.5f ? 0u : (a < 1.0f ? 1u : (a < 1.5f ? 2u : 3u));
-      lo = 0.5f * (float)klo;
-      inv_w = 2.0f;
-    } else if (a < 4.0f) {
-      klo = a < 3.0f ? 4u : 5u;
-      lo = a < 3.0f ? 2.0f : 3.0f;
-      inv_w = 1.0f;
-    } else {
-      klo = 6;
-      lo = 4.0f;
-      inv_w = 0.5f;
-    }
-    const float f24 = ieee_mul(ieee_mul(ieee_sub(a, lo), inv_w), 16777216.0f);
-    k = klo + (((float)(w >> 8) < f24) ? 1u : 0u);
-  }
-  return sign | k;
+  const bool lt2 = a < 2.0f, lt4 = a < 4.0f;
+  const float y = ieee_mul(a, lt2 ? 2.0f : (lt4 ? 1.0f : 0.5f));
+  float tmp;
+  asm("add.rm.f32 %0, %1, 0f4B400000;" : "=f"(tmp) : "f"(y));
+  const float fl = ieee_sub(tmp, 12582912.0f);
+  const float f24 = ieee_mul(ieee_sub(y, fl), 16777216.0f);
+  const uint32_t up = ((float)(w >> 8) < f24) ? 1u : 0u;
+  const uint32_t k = (fbits(tmp) & 3u) + (lt2 ? 0u : (lt4 ? 2u : 4u)) + up;
+  return sign | (a < 6.0f ? k : 7u);
 }
 
 // ---------------------------------------------------------------------------
@@ -158,9 +147,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x, p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
   }
   return c;
 }
