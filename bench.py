@@ -212,17 +212,19 @@ def _extra_workloads():
         ms = _events_time(lambda i: fq.quantize(x, mode="outer_block", outer_block_size=64, out=q), iters, warmup)
         return "bf16[256,512] 1x64 outer E4M3 RNE rowwise", 262144 + 65536 + 8192 + 8192, ms, 1
 
-    def _activations(mode_kw, nb_out, launches):
+    def _activations(mode_kw, nb_out, launches, columnwise=True):
         def run(iters, warmup, opts):
             xs = [W.activations().to(dev)]
             nb_in = xs[0].numel() * 2
             for _ in range(_sets_for(nb_in) - 1):
                 xs.append(xs[0].clone())
-            qs = [fq.quantize(xx, rowwise=True, columnwise=True, **mode_kw) for xx in xs]
-            ms = _events_time(lambda i: fq.quantize(xs[i % len(xs)], rowwise=True, columnwise=True,
+            qs = [fq.quantize(xx, rowwise=True, columnwise=columnwise, **mode_kw) for xx in xs]
+            ms = _events_time(lambda i: fq.quantize(xs[i % len(xs)], rowwise=True, columnwise=columnwise,
                                                     out=qs[i % len(xs)], **mode_kw), iters, warmup)
-            return ("bf16[16384,2880] massive activations, %s, rowwise+columnwise" % mode_kw["mode"],
-                    nb_in + nb_out, ms, launches)
+            what = ", ".join("%s=%s" % kv for kv in mode_kw.items() if kv[0] != "mode")
+            return ("bf16[16384,2880] massive activations, %s%s, %s" % (
+                mode_kw["mode"], " " + what if what else "", "rowwise+columnwise" if columnwise else "rowwise"),
+                nb_in + nb_out, ms, launches)
         return run
 
     M, K = 16384, 2880
@@ -266,6 +268,12 @@ def _extra_workloads():
                                                  2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1), 50, 5),
         "activations_tensorwise": (_activations(dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4, 3),
                                    50, 5),
+        "activations_none": (_activations(dict(mode="none"), 2 * codes + 2 * (M * K // 16), 1), 50, 5),
+        "activations_rowwise_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64),
+                                                         codes + M * K // 16 + (M * K // 64) * 4, 1,
+                                                         columnwise=False), 50, 5),
+        "activations_rowwise_sr": (_activations(dict(mode="none", stochastic=True), codes + M * K // 16, 1,
+                                                columnwise=False), 50, 5),
         "dequantize_activations": (dequantize_activations, 50, 5),
         "moe_experts_e4m3": (_moe("e4m3"), 20, 3),
         "moe_experts_ue5m3": (_moe("ue5m3"), 20, 3),

@@ -9,6 +9,7 @@ the library's CUDA kernels.  The library must be built for the GPU in use
     dequantize(q, orient="row") -> bf16 / fp32 tensor
     qdq(x, ...)                 -> (y, outer scales)
     mxfp4_fake_quantize(x)      -> projected tensor
+    tensor_amax(x)              -> max |x| (sanitized) as a 1-element fp32 tensor
 """
 from __future__ import annotations
 
@@ -21,8 +22,8 @@ import torch
 from . import _capi
 from ._capi import FP4QError
 
-__all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize", "build", "FP4QError",
-           "query_sizes"]
+__all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize", "tensor_amax", "build",
+           "FP4QError", "query_sizes"]
 
 _MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
 _FMTS = {"e4m3": _capi.SCALE_E4M3, "ue5m3": _capi.SCALE_UE5M3}
@@ -232,3 +233,16 @@ def mxfp4_fake_quantize(x: torch.Tensor, out_dtype: Optional[torch.dtype] = None
     st = _lib().mxfp4_fake_quantize(ctypes.byref(p), _ptr(x3), _ptr(y), _stream(x.device))
     _capi.check(st, "mxfp4_fake_quantize")
     return y if (x.dim() == 3 or out is not None) else y[0]
+
+
+def tensor_amax(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """max |sanitize(x + residual)| over a CUDA bf16 / fp32 tensor, as a
+    1-element float32 device tensor (the tensorwise outer scale is this
+    value / (scale_max * 6))."""
+    x3, G, M, K, ld = _view3d(x)
+    p = _params(G, M, K, ld, x.dtype)
+    a = out if out is not None else torch.empty(1, dtype=torch.float32, device=x.device)
+    st = _lib().fp4_tensor_amax(ctypes.byref(p), _ptr(x3), _ptr(residual), _ptr(a), _stream(x.device))
+    _capi.check(st, "fp4_tensor_amax")
+    return a

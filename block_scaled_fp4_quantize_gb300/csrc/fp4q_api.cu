@@ -27,6 +27,11 @@ int vec_aligned(const void* p, int64_t bytes_stride) {
   return (reinterpret_cast<uintptr_t>(p) % 16u == 0u) && (bytes_stride % 16 == 0);
 }
 
+bool getenv_flag(const char* name) {
+  const char* v = std::getenv(name);
+  return v && v[0] && v[0] != '0';
+}
+
 }  // namespace fp4q
 
 using namespace fp4q;
@@ -34,11 +39,6 @@ using namespace fp4q;
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0u; }
-
-bool getenv_flag(const char* name) {
-  const char* v = std::getenv(name);
-  return v && v[0] && v[0] != '0';
-}
 
 int esize(int32_t dt) { return dt == FP4Q_BF16 ? 2 : 4; }
 
@@ -322,6 +322,23 @@ int mxfp4_fake_quantize(const fp4q_params_t* p, const void* x, void* y, void* st
   j.K = p->K;
   j.y = y;
   return launch_mxfp4(j, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+int fp4_tensor_amax(const fp4q_params_t* p, const void* x, const float* residual, float* amax, void* stream) {
+  if (!p || !amax) return FP4Q_ERR_NULL;
+  if (p->struct_size != sizeof(fp4q_params_t)) return FP4Q_ERR_ABI;
+  const int rc = check_dtype(p->in_dtype);
+  if (rc) return rc;
+  if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K) return FP4Q_ERR_SHAPE;
+  if (!aligned(amax, 4)) return FP4Q_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->G == 0 || p->M == 0 || p->K == 0)
+    return cudaMemsetAsync(amax, 0, sizeof(float), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+  if (!x) return FP4Q_ERR_NULL;
+  if (!aligned(x, (uintptr_t)esize(p->in_dtype)) || (residual && !aligned(residual, 4))) return FP4Q_ERR_ALIGN;
+  QuantJob j = base_job(p, x, const_cast<float*>(residual));
+  // the maximum of non-negative binary32 values is the maximum of their bits
+  return launch_tensor_amax(j, reinterpret_cast<uint32_t*>(amax), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }
 
 const char* fp4q_status_string(int status) {

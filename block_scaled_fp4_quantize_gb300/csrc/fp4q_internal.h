@@ -61,6 +61,9 @@ struct MxJob {
 
 int num_sms();
 int vec_aligned(const void* p, int64_t bytes_stride);
+// true when the environment variable is set to a value other than "" or "0"
+// (kernel-selection switches used by the parity tests)
+bool getenv_flag(const char* name);
 
 cudaError_t launch_quant_tile(const QuantJob& j, bool vec, cudaStream_t st);
 bool ct_supports(const QuantJob& j);

@@ -25,6 +25,25 @@ __device__ __forceinline__ int mx_exponent(uint32_t amax_bits) {
   return e < 125 ? e : 125;
 }
 
+// A 32-byte unit (two 16-byte halves) for the 256-bit access path.
+struct U32B {
+  uint4 a, b;
+};
+
+__device__ __forceinline__ U32B ld256_stream(const void* p) {
+  U32B r;
+  asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r.a.x), "=r"(r.a.y), "=r"(r.a.z), "=r"(r.a.w), "=r"(r.b.x), "=r"(r.b.y), "=r"(r.b.z),
+                 "=r"(r.b.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st256(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 template <typename TI>
 struct InTraits;
 template <>
@@ -112,6 +131,64 @@ __global__ void __launch_bounds__(NT) mxfp4_vec_kernel(const MxJob j) {
   }
 }
 
+// bf16 in, bf16 out, contiguous and 32-byte aligned: every lane owns a
+// 32-byte unit (half a 1 x 32 block), 256-bit loads and stores, one
+// xor-shuffle per block.
+__global__ void __launch_bounds__(NT) mxfp4_wide_kernel(const MxJob j) {
+  const int64_t U = j.G * j.M * j.K / 16;
+  const uint16_t* x = static_cast<const uint16_t*>(j.x);
+  uint16_t* y = static_cast<uint16_t*>(j.y);
+  for (int64_t base = (int64_t)blockIdx.x * NT * UNR; base < U; base += (int64_t)gridDim.x * NT * UNR) {
+    U32B w[UNR];
+#pragma unroll
+    for (int p = 0; p < UNR; ++p) {
+      const int64_t u = base + p * NT + threadIdx.x;
+      if (u < U) w[p] = ld256_stream(x + u * 16);
+      else w[p] = U32B{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    }
+#pragma unroll
+    for (int p = 0; p < UNR; ++p) {
+      const int64_t u = base + p * NT + threadIdx.x;
+      float v[16];
+      InTraits<uint16_t>::unpack(w[p].a, v);
+      InTraits<uint16_t>::unpack(w[p].b, v + 8);
+      uint32_t am = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { const uint32_t a = abs_bits(v[i]); am = a > am ? a : am; }
+      { const uint32_t b = __shfl_xor_sync(0xFFFFFFFFu, am, 1); am = b > am ? b : am; }
+      if (u < U) {
+        const int E = mx_exponent(am);
+        const bool poison = am >= 0x7F800000u;
+        const float inv = bitsf((uint32_t)(127 - E) << 23);
+        const float sc = bitsf((uint32_t)(127 + E) << 23);
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const uint32_t b = e2m1x2_rne(ieee_mul(v[i], inv), ieee_mul(v[i + 1], inv));
+          float g0, g1;
+          e2m1x2_decode(b, g0, g1);
+          o[i / 2] = poison ? 0x7FC07FC0u : pack_bf16x2(ieee_mul(g0, sc), ieee_mul(g1, sc));
+        }
+        st256(y + u * 16, o);
+      }
+    }
+  }
+}
+
+// Resident CTAs per SM of a kernel (cached per kernel and device).
+template <class K>
+int resident_ctas(K kern, int* cache) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, 0) != cudaSuccess || n < 1) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 // Any alignment: one thread per 1 x 32 block, scalar accesses.
 template <typename TI, bool OUT_BF16>
 __global__ void __launch_bounds__(NT) mxfp4_scalar_kernel(const MxJob j) {
@@ -157,12 +234,26 @@ cudaError_t launch_typed(const MxJob& j, cudaStream_t st) {
   const int esz = (int)sizeof(TI);
   const bool vec = vec_aligned(j.x, j.ld * esz) && vec_aligned(j.y, 16) &&
                    (OUT_BF16 ? (EPU * 2) % 8 == 0 : true);
-  if (vec) {
+  const bool wide = sizeof(TI) == 2 && OUT_BF16 && (j.ld == j.K || j.G * j.M == 1) &&
+                    ((reinterpret_cast<uintptr_t>(j.x) | reinterpret_cast<uintptr_t>(j.y)) & 31u) == 0 &&
+                    !getenv_flag("FP4Q_MXFP4_NARROW");
+  if (wide) {
+    // grid = the CTAs that are resident at once, so no CTA waits for a slot
+    static int cache[128] = {0};
+    const int64_t U = j.G * j.M * j.K / 16;
+    const int64_t need = (U + NT * UNR - 1) / (NT * UNR);
+    const int64_t cap = (int64_t)num_sms() * resident_ctas(mxfp4_wide_kernel, cache);
+    mxfp4_wide_kernel<<<(int)(need < cap ? need : cap), NT, 0, st>>>(j);
+  } else if (vec) {
+    static int cache_c[128] = {0}, cache_s[128] = {0};
     const int64_t U = j.G * j.M * (j.K / EPU);
     const int64_t need = (U + NT * UNR - 1) / (NT * UNR);
-    const int64_t cap = (int64_t)num_sms() * 8;
+    const bool contig = j.ld == j.K;
+    const int per_sm = contig ? resident_ctas(mxfp4_vec_kernel<TI, OUT_BF16, true>, cache_c)
+                              : resident_ctas(mxfp4_vec_kernel<TI, OUT_BF16, false>, cache_s);
+    const int64_t cap = (int64_t)num_sms() * per_sm;
     const int grid = (int)(need < cap ? need : cap);
-    if (j.ld == j.K) mxfp4_vec_kernel<TI, OUT_BF16, true><<<grid, NT, 0, st>>>(j);
+    if (contig) mxfp4_vec_kernel<TI, OUT_BF16, true><<<grid, NT, 0, st>>>(j);
     else mxfp4_vec_kernel<TI, OUT_BF16, false><<<grid, NT, 0, st>>>(j);
   } else {
     const int64_t nblk = j.G * j.M * (j.K / 32);

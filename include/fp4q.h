@@ -203,6 +203,19 @@ int fp4_qdq(const fp4q_params_t *p, int orient, const void *x, void *y, float *r
  * scale_format must be at their defaults and rounding RNE. */
 int mxfp4_fake_quantize(const fp4q_params_t *p, const void *x, void *y, void *stream);
 
+/* The tensorwise amax alone: *amax (a device float) = max |u| over the
+ * [G, M, K] tensor, u = sanitize(x + residual) as in fp4_quantize (residual
+ * may be NULL; NaN reads as +0, +-inf as the largest finite value of the
+ * input dtype), 0 for an empty tensor.  The tensorwise outer scale is
+ * S = amax / (scale_max * 6), one binary32 division ("NVFP4 / AMD-FP4
+ * outer-block (two-level) scaling for FP4 training", "Background": the
+ * per-tensor scale).  With a tensor split by rows across processes, the
+ * maximum of the parts' amax values is the whole tensor's, so each part can
+ * be quantized with that S passed as a precomputed tensorwise scale.  Only
+ * p->in_dtype, G, M, K and ld are read.  Overwrites *amax (it is first set
+ * to 0 on the stream, then combined with atomic maxima). */
+int fp4_tensor_amax(const fp4q_params_t *p, const void *x, const float *residual, float *amax, void *stream);
+
 /* Bytes of static device scratch behind fp4_quantize_noalloc. */
 #define FP4Q_NOALLOC_SCRATCH_BYTES 256
 
