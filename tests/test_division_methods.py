@@ -13,7 +13,7 @@ from fractions import Fraction
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-KERNEL = os.path.join(ROOT, "block_scaled_fp4_quantize_gb300", "csrc", "k_ct.cu")
+KERNEL = os.path.join(ROOT, "block_scaled_fp4_quantize_gb300", "csrc", "fp4q_block.cuh")
 CHECK = os.path.join(os.path.dirname(os.path.abspath(__file__)), "division_methods_check.c")
 
 
