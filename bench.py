@@ -379,7 +379,7 @@ def run_ours(args, dist):
                    "l2": "2 rotating input/output sets (537 MB > L2)", "parallelism": "replicas" if dist.world > 1 else "none"},
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": peak_src,
-                     "traffic": ncu_traffic("mxfp4_vec_kernel"), "kernel": "mxfp4_vec_kernel<bf16,bf16>"},
+                     "traffic": ncu_traffic("mxfp4_wide_kernel"), "kernel": "mxfp4_wide_kernel"},
         "e2e": {"value": round(MXFP4_BYTES / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": MXFP4_BYTES // 2, "d2h_bytes_per_step": MXFP4_BYTES // 2},
         "gpu_launches": args.steps,

@@ -1,27 +1,21 @@
-// k_ct.cu -- fast fused quantize / cast-transpose / QDQ kernel.
+// k_ct.cu -- generic cast-transpose quantize / QDQ kernel (binary32 or bf16
+// input; the columnwise bf16 quantize has its own kernel in k_ctb.cu).
 //
-// One CTA of 256 threads owns a 128 (M) x 64 (K) tile at a time (grid-stride
-// over tiles, grid sized to the resident CTAs).  Rowwise pass: thread t owns
-// the 1 x 16 blocks (row t/4, block t%4) and (row t/4 + 64, block t%4), loaded
-// straight from HBM with 128-bit loads; a 1 x 64 outer block is the 4 lanes
-// of one row, reduced with two xor-shuffles.  The columnwise pass reads the
-// tile back from a swizzled binary32 staging buffer in shared memory (thread
-// owns 2 columns x 16 rows), so x is read from HBM once for both
-// orientations ("Block-Scaled FP8 and FP4 Weight Quantization", section 3).
-// With a 2-D outer scale, tensorwise or no outer scale, the normalized value
-// x' = u / S is computed once and staged; with 1-D outer scales u is staged
-// and each orientation normalizes by its own scale.
+// A CTA of 256 threads walks TM x 64 tiles of x (bf16: 128 rows, binary32:
+// 64 rows; 16 KB either way), fed by 3-D tensor copies with the 128-byte
+// swizzle, several tiles in flight on mbarriers with bounded waits.  Rowwise
+// pass: a thread owns consecutive 1 x 16 blocks of one row.  Columnwise pass:
+// a thread owns one column and a quarter of the tile's rows.  With a 2-D
+// outer scale, tensorwise or no outer scale, x' = u / S is computed once in
+// the rowwise pass and staged in shared memory (binary32) for the columnwise
+// pass; with 1-D outer scales each orientation normalizes by its own scale
+// ("Block-Scaled FP8 and FP4 Weight Quantization", sections 3 and 6).
 //
-// Division: every quotient the method defines is one IEEE binary32 division.
-// Here they are computed exactly with FMA sequences: u / S with Markstein's
-// correction from RN(1/S), x' / s and a / 6 and amax / (scale_max * 6) with
-// the Brisebarre-Muller-Raina method for divisors known in advance (the inner
-// scale s has a 4-bit significand).  Blocks outside the proven range (tiny or
-// subnormal scales) take div.rn.
-//
-// Covers: inner 1 x 16 blocks, 16-byte-aligned inputs; modes none, tensorwise,
-// outer-block 1-D / 2-D with ob in {16, 32, 64} computed in the tile or any ob
-// read from the outer buffers; RNE / SR; error feedback; QDQ along K or M.
+// Covers: inner 1 x 16 blocks, 16-byte-aligned inputs; modes none,
+// tensorwise, outer-block 1-D / 2-D with ob in {16, 32, 64} computed in the
+// tile or any ob read from the outer buffers; RNE / SR; error feedback; QDQ
+// along K or M.  The per-block arithmetic (exact division sequences, scale
+// encode, E2M1 encode) is in fp4q_block.cuh.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -13,7 +13,8 @@ namespace fp4q {
 namespace {
 
 constexpr int NT = 256;
-constexpr int UNR = 4;  // independent 16-byte loads in flight per thread
+constexpr int UNR = 4;   // independent 16-byte loads in flight per thread (16-byte path)
+constexpr int WUNR = 2;  // independent 32-byte loads in flight per thread (32-byte path)
 
 // Block exponent E for the block maximum |x| bits (finite): least E with
 // 6 * 2^E >= max(A, 6 * 2^-126), capped at 125.  Writing the clamped maximum
@@ -134,20 +135,28 @@ __global__ void __launch_bounds__(NT) mxfp4_vec_kernel(const MxJob j) {
 // bf16 in, bf16 out, contiguous and 32-byte aligned: every lane owns a
 // 32-byte unit (half a 1 x 32 block), 256-bit loads and stores, one
 // xor-shuffle per block.
+//
+// Launched with programmatic dependent launch: the kernel first waits for the
+// previous grid on the stream to complete (griddepcontrol.wait: its writes are
+// then visible), then lets the next grid be scheduled, so back-to-back calls
+// overlap launch latency with the previous call's tail instead of idling.
+// Without the launch attribute both instructions are no-ops.
 __global__ void __launch_bounds__(NT) mxfp4_wide_kernel(const MxJob j) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t U = j.G * j.M * j.K / 16;
   const uint16_t* x = static_cast<const uint16_t*>(j.x);
   uint16_t* y = static_cast<uint16_t*>(j.y);
-  for (int64_t base = (int64_t)blockIdx.x * NT * UNR; base < U; base += (int64_t)gridDim.x * NT * UNR) {
-    U32B w[UNR];
+  for (int64_t base = (int64_t)blockIdx.x * NT * WUNR; base < U; base += (int64_t)gridDim.x * NT * WUNR) {
+    U32B w[WUNR];
 #pragma unroll
-    for (int p = 0; p < UNR; ++p) {
+    for (int p = 0; p < WUNR; ++p) {
       const int64_t u = base + p * NT + threadIdx.x;
       if (u < U) w[p] = ld256_stream(x + u * 16);
       else w[p] = U32B{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
     }
 #pragma unroll
-    for (int p = 0; p < UNR; ++p) {
+    for (int p = 0; p < WUNR; ++p) {
       const int64_t u = base + p * NT + threadIdx.x;
       float v[16];
       InTraits<uint16_t>::unpack(w[p].a, v);
@@ -173,20 +182,6 @@ __global__ void __launch_bounds__(NT) mxfp4_wide_kernel(const MxJob j) {
       }
     }
   }
-}
-
-// Resident CTAs per SM of a kernel (cached per kernel and device).
-template <class K>
-int resident_ctas(K kern, int* cache) {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 128) dev = 0;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NT, 0) != cudaSuccess || n < 1) n = 1;
-    cache[dev] = n;
-  }
-  return cache[dev];
 }
 
 // Any alignment: one thread per 1 x 32 block, scalar accesses.
@@ -237,28 +232,32 @@ cudaError_t launch_typed(const MxJob& j, cudaStream_t st) {
   const bool wide = sizeof(TI) == 2 && OUT_BF16 && (j.ld == j.K || j.G * j.M == 1) &&
                     ((reinterpret_cast<uintptr_t>(j.x) | reinterpret_cast<uintptr_t>(j.y)) & 31u) == 0 &&
                     !getenv_flag("FP4Q_MXFP4_NARROW");
+  // grids of 8 CTAs per SM: more than are resident at once, which measured
+  // faster than exactly the resident count (the hardware balances the tail)
+  const int64_t cap = (int64_t)num_sms() * 8;
   if (wide) {
-    // grid = the CTAs that are resident at once, so no CTA waits for a slot
-    static int cache[128] = {0};
     const int64_t U = j.G * j.M * j.K / 16;
-    const int64_t need = (U + NT * UNR - 1) / (NT * UNR);
-    const int64_t cap = (int64_t)num_sms() * resident_ctas(mxfp4_wide_kernel, cache);
-    mxfp4_wide_kernel<<<(int)(need < cap ? need : cap), NT, 0, st>>>(j);
+    const int64_t need = (U + NT * WUNR - 1) / (NT * WUNR);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(need < cap ? need : cap));
+    cfg.blockDim = dim3(NT);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mxfp4_wide_kernel, j);
+    if (e != cudaSuccess) return e;
   } else if (vec) {
-    static int cache_c[128] = {0}, cache_s[128] = {0};
     const int64_t U = j.G * j.M * (j.K / EPU);
     const int64_t need = (U + NT * UNR - 1) / (NT * UNR);
-    const bool contig = j.ld == j.K;
-    const int per_sm = contig ? resident_ctas(mxfp4_vec_kernel<TI, OUT_BF16, true>, cache_c)
-                              : resident_ctas(mxfp4_vec_kernel<TI, OUT_BF16, false>, cache_s);
-    const int64_t cap = (int64_t)num_sms() * per_sm;
     const int grid = (int)(need < cap ? need : cap);
-    if (contig) mxfp4_vec_kernel<TI, OUT_BF16, true><<<grid, NT, 0, st>>>(j);
+    if (j.ld == j.K) mxfp4_vec_kernel<TI, OUT_BF16, true><<<grid, NT, 0, st>>>(j);
     else mxfp4_vec_kernel<TI, OUT_BF16, false><<<grid, NT, 0, st>>>(j);
   } else {
     const int64_t nblk = j.G * j.M * (j.K / 32);
     const int64_t need = (nblk + NT - 1) / NT;
-    const int64_t cap = (int64_t)num_sms() * 8;
     mxfp4_scalar_kernel<TI, OUT_BF16><<<(int)(need < cap ? need : cap), NT, 0, st>>>(j);
   }
   return cudaGetLastError();

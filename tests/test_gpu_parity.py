@@ -303,6 +303,24 @@ def test_mxfp4_all_bf16_patterns(orc):
         assert_same({"y": host_np(y)}, {"y": ref[0]})
 
 
+def test_mxfp4_back_to_back_dependent_calls():
+    """Each call reads the previous call's output (launches may overlap the
+    previous kernel's tail): the projection is idempotent, so every link of
+    the chain equals the first output, bit for bit."""
+    x, _ = W.mxfp4_weight()
+    x = x[:2048].cuda()
+    y1 = fq.mxfp4_fake_quantize(x)
+    fin = torch.isfinite(y1.float()).view(2048, -1, 32).all(dim=2)  # non-poisoned 1 x 32 blocks
+    ys = [y1]
+    for _ in range(64):
+        ys.append(fq.mxfp4_fake_quantize(ys[-1]))
+        ys[-1] = ys[-1] * 1 if len(ys) % 7 == 0 else ys[-1]  # a torch kernel between some links
+    torch.cuda.synchronize()
+    a = y1.view(torch.int16).view(2048, -1, 32)[fin]
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int16).view(2048, -1, 32)[fin], a)
+
+
 def test_mxfp4_fp32_raw_bit_fuzz(orc):
     """fp32 inputs drawn as raw bit patterns (MXFP4 QAT page, 'Correctness')."""
     bits = np.random.default_rng(28).integers(0, 2 ** 32, size=(512, 1024), dtype=np.uint64).astype(np.uint32)
