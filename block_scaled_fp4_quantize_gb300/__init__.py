@@ -9,6 +9,7 @@ the library's CUDA kernels.  The library must be built for the GPU in use
     dequantize(q, orient="row") -> bf16 / fp32 tensor
     qdq(x, ...)                 -> (y, outer scales)
     mxfp4_fake_quantize(x)      -> projected tensor
+    mxfp4_fake_quantize_host(x) -> the same for a host tensor, streamed through the GPU
     tensor_amax(x)              -> max |x| (sanitized) as a 1-element fp32 tensor
 """
 from __future__ import annotations
@@ -22,8 +23,8 @@ import torch
 from . import _capi
 from ._capi import FP4QError
 
-__all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize", "tensor_amax", "build",
-           "FP4QError", "query_sizes"]
+__all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize", "mxfp4_fake_quantize_host",
+           "tensor_amax", "build", "FP4QError", "query_sizes", "host_workspace_bytes"]
 
 _MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
 _FMTS = {"e4m3": _capi.SCALE_E4M3, "ue5m3": _capi.SCALE_UE5M3}
@@ -232,6 +233,57 @@ def mxfp4_fake_quantize(x: torch.Tensor, out_dtype: Optional[torch.dtype] = None
     y = out if out is not None else torch.empty(G, M, K, dtype=out_dtype, device=x.device)
     st = _lib().mxfp4_fake_quantize(ctypes.byref(p), _ptr(x3), _ptr(y), _stream(x.device))
     _capi.check(st, "mxfp4_fake_quantize")
+    return y if (x.dim() == 3 or out is not None) else y[0]
+
+
+HOST_CHUNK_BYTES = 16 << 20
+
+
+def host_workspace_bytes(K: int, in_dtype: torch.dtype = torch.bfloat16, out_dtype: Optional[torch.dtype] = None) -> int:
+    """Device staging bytes mxfp4_fake_quantize_host needs for full-size
+    chunks of rows of K elements."""
+    out_dtype = out_dtype or in_dtype
+    ein, eout = torch.empty(0, dtype=in_dtype).element_size(), torch.empty(0, dtype=out_dtype).element_size()
+    rows = max(1, HOST_CHUNK_BYTES // (K * ein))
+    r256 = lambda v: (v + 255) // 256 * 256
+    return 2 * (r256(rows * K * ein) + r256(rows * K * eout))
+
+
+def mxfp4_fake_quantize_host(x: torch.Tensor, out_dtype: Optional[torch.dtype] = None,
+                             out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                             device=None, synchronize: bool = True) -> torch.Tensor:
+    """MXFP4 projection of a tensor in HOST memory (pinned for overlap),
+    streamed through the GPU in chunks: host-to-device copy, kernel and
+    device-to-host copy of consecutive chunks overlap.  Returns a host
+    tensor; with synchronize=False it is complete when the current stream of
+    `device` reaches this point."""
+    if x.is_cuda:
+        raise ValueError("x must be a host tensor (use mxfp4_fake_quantize for device tensors)")
+    if x.dim() == 2:
+        x3 = x.unsqueeze(0)
+    elif x.dim() == 3:
+        x3 = x
+    else:
+        raise ValueError("expected a 2-D or 3-D tensor")
+    G, M, K = x3.shape
+    if K > 1 and x3.stride(2) != 1:
+        raise ValueError("the last dimension must be contiguous")
+    ld = x3.stride(1) if M > 1 else K
+    if G > 1 and x3.stride(0) != M * ld:
+        raise ValueError("matrices must be stored back to back (batch stride M * ld)")
+    out_dtype = out_dtype or x.dtype
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    y = out if out is not None else torch.empty(G, M, K, dtype=out_dtype, pin_memory=x.is_pinned())
+    if workspace is None:
+        workspace = torch.empty(host_workspace_bytes(K, x.dtype, out_dtype), dtype=torch.uint8, device=dev)
+    p = _params(G, M, K, ld, x.dtype, out_dtype)
+    with torch.cuda.device(dev):
+        st = _lib().mxfp4_fake_quantize_host(ctypes.byref(p), ctypes.c_void_p(x3.data_ptr()),
+                                             ctypes.c_void_p(y.data_ptr()), _ptr(workspace),
+                                             workspace.numel(), _stream(dev))
+        _capi.check(st, "mxfp4_fake_quantize_host")
+        if synchronize:
+            torch.cuda.current_stream(dev).synchronize()
     return y if (x.dim() == 3 or out is not None) else y[0]
 
 

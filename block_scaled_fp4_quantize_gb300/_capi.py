@@ -20,8 +20,8 @@ OUT_ROW, OUT_COL = 1, 2
 
 # every symbol include/fp4q.h declares
 EXPORTS = ("fp4q_params_init", "fp4q_query_sizes", "fp4_quantize", "fp4_dequantize", "fp4_qdq",
-           "mxfp4_fake_quantize", "fp4_tensor_amax", "fp4q_status_string", "fp4q_abi_version",
-           "fp4_quantize_noalloc")
+           "mxfp4_fake_quantize", "mxfp4_fake_quantize_host", "fp4_tensor_amax", "fp4q_status_string",
+           "fp4q_abi_version", "fp4_quantize_noalloc")
 
 
 class Params(ctypes.Structure):
@@ -80,6 +80,8 @@ def load(fast_math: bool = False, path: str | None = None):
     L.fp4_qdq.argtypes = [PP, I, P, P, P, P, P, ctypes.c_size_t, P]
     L.mxfp4_fake_quantize.restype = I
     L.mxfp4_fake_quantize.argtypes = [PP, P, P, P]
+    L.mxfp4_fake_quantize_host.restype = I
+    L.mxfp4_fake_quantize_host.argtypes = [PP, P, P, P, ctypes.c_size_t, P]
     L.fp4_tensor_amax.restype = I
     L.fp4_tensor_amax.argtypes = [PP, P, P, P, P]
     L.fp4_quantize_noalloc.restype = I
