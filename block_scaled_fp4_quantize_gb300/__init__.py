@@ -28,6 +28,7 @@ __all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize
 
 _MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
 _FMTS = {"e4m3": _capi.SCALE_E4M3, "ue5m3": _capi.SCALE_UE5M3}
+_LAYOUTS = {"linear": _capi.SCALE_LAYOUT_LINEAR, "mma": _capi.SCALE_LAYOUT_MMA}
 _DT = {torch.bfloat16: _capi.BF16, torch.float32: _capi.FP32, torch.float16: _capi.FP16}
 _ORIENT = {"row": _capi.OUT_ROW, "col": _capi.OUT_COL, -1: _capi.OUT_ROW, 0: _capi.OUT_COL}
 
@@ -72,7 +73,7 @@ def _view3d(x: torch.Tensor):
 
 def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_size=0, outer_2d=False,
             inner_2d=False, scale_format="e4m3", stochastic=False, seed=0, step=0, out_mask=_capi.OUT_ROW,
-            use_precomputed_outer=False):
+            use_precomputed_outer=False, scale_layout="linear"):
     p = _capi.new_params(_lib())
     p.G, p.M, p.K, p.ld = G, M, K, ld
     p.in_dtype = _DT.get(in_dtype, -1)
@@ -87,6 +88,7 @@ def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_s
     p.step = int(step) & (2 ** 32 - 1)
     p.out_mask = int(out_mask)
     p.use_precomputed_outer = int(bool(use_precomputed_outer))
+    p.scale_layout = _LAYOUTS[scale_layout]
     return p
 
 
@@ -106,12 +108,13 @@ class QuantizedFP4:
     inner_2d: bool
     scale_format: str
     row_codes: Optional[torch.Tensor] = None   # uint8 [G, M, K/2]
-    row_scales: Optional[torch.Tensor] = None  # uint8 [G, M, K/16]
+    row_scales: Optional[torch.Tensor] = None  # uint8 [G, M, K/16] (linear layout; flat padded tiles for "mma")
     row_outer: Optional[torch.Tensor] = None   # float32 [G, M, K/ob]
     col_codes: Optional[torch.Tensor] = None   # uint8 [G, K, M/2]
     col_scales: Optional[torch.Tensor] = None  # uint8 [G, K, M/16]
     col_outer: Optional[torch.Tensor] = None   # float32 [G, K, M/ob]
     tile_outer: Optional[torch.Tensor] = None  # float32 [G, M/ob, K/ob] or [1]
+    scale_layout: str = "linear"               # inner-scale layout: "linear" or "mma" (128 x 4 tiles)
 
 
 def _outer_shapes(G, M, K, mode, ob, outer_2d, row, col):
@@ -133,29 +136,34 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
              inner_2d: bool = False, scale_format: str = "e4m3", stochastic: bool = False, seed: int = 0,
              step: int = 0, rowwise: bool = True, columnwise: bool = False,
              residual: Optional[torch.Tensor] = None, precomputed_outer: Optional[QuantizedFP4] = None,
-             out: Optional[QuantizedFP4] = None) -> QuantizedFP4:
+             out: Optional[QuantizedFP4] = None, scale_layout: str = "linear") -> QuantizedFP4:
     """NVFP4 / AMD-FP4 quantize of a CUDA bf16 or fp32 tensor ([M, K] or [G, M, K]).
 
     ``residual`` (fp32, [G, M, K] contiguous) enables error feedback and is
     updated in place (rowwise only).  ``precomputed_outer`` supplies outer
     scales (from an earlier call) instead of computing them.  ``out`` reuses
-    preallocated output buffers."""
+    preallocated output buffers.  ``scale_layout="mma"`` writes the inner
+    scales in the 128 x 4 tiled layout block-scaled tensor-core MMAs read
+    (see include/fp4q.h); the scale tensors are then flat padded byte
+    buffers."""
     x3, G, M, K, ld = _view3d(x)
     mask = (_capi.OUT_ROW if rowwise else 0) | (_capi.OUT_COL if columnwise else 0)
     p = _params(G, M, K, ld, x.dtype, mode=mode, outer_block_size=outer_block_size, outer_2d=outer_2d,
                 inner_2d=inner_2d, scale_format=scale_format, stochastic=stochastic, seed=seed, step=step,
-                out_mask=mask, use_precomputed_outer=precomputed_outer is not None)
+                out_mask=mask, use_precomputed_outer=precomputed_outer is not None, scale_layout=scale_layout)
     s = query_sizes(p)
     dev = x.device
     if out is None:
         u8 = dict(dtype=torch.uint8, device=dev)
-        q = QuantizedFP4((G, M, K), mode, outer_block_size, outer_2d, inner_2d, scale_format)
+        q = QuantizedFP4((G, M, K), mode, outer_block_size, outer_2d, inner_2d, scale_format,
+                         scale_layout=scale_layout)
+        mma = scale_layout == "mma"
         if rowwise:
             q.row_codes = torch.empty(G, M, K // 2, **u8)
-            q.row_scales = torch.empty(G, M, K // 16, **u8)
+            q.row_scales = torch.empty(int(s.row_scales), **u8) if mma else torch.empty(G, M, K // 16, **u8)
         if columnwise:
             q.col_codes = torch.empty(G, K, M // 2, **u8)
-            q.col_scales = torch.empty(G, K, M // 16, **u8)
+            q.col_scales = torch.empty(int(s.col_scales), **u8) if mma else torch.empty(G, K, M // 16, **u8)
         for name, shp in _outer_shapes(G, M, K, mode, outer_block_size, outer_2d, rowwise, columnwise).items():
             if shp is not None:
                 src = getattr(precomputed_outer, name, None) if precomputed_outer is not None else None
@@ -184,7 +192,8 @@ def dequantize(q: QuantizedFP4, orient: str = "row", out_dtype: torch.dtype = to
     else:
         outer = q.tile_outer
     p = _params(G, M, K, K, torch.bfloat16, out_dtype, mode=q.mode, outer_block_size=q.outer_block_size,
-                outer_2d=q.outer_2d, inner_2d=q.inner_2d, scale_format=q.scale_format, out_mask=o)
+                outer_2d=q.outer_2d, inner_2d=q.inner_2d, scale_format=q.scale_format, out_mask=o,
+                scale_layout=q.scale_layout)
     R, C = (M, K) if o == _capi.OUT_ROW else (K, M)
     y = out if out is not None else torch.empty(G, R, C, dtype=out_dtype, device=codes.device)
     st = _lib().fp4_dequantize(ctypes.byref(p), o, _ptr(codes), _ptr(scales), _ptr(outer), _ptr(y),

@@ -15,6 +15,8 @@ STATUS = {
 BF16, FP32, FP16 = 1, 2, 3
 MODE_NONE, MODE_TENSORWISE, MODE_OUTER_BLOCK = 0, 1, 2
 SCALE_E4M3, SCALE_UE5M3 = 0, 1
+SCALE_LAYOUT_LINEAR, SCALE_LAYOUT_MMA = 0, 1
+ABI_VERSION = 2  # FP4Q_ABI_VERSION of include/fp4q.h
 RNE, STOCHASTIC = 0, 1
 OUT_ROW, OUT_COL = 1, 2
 
@@ -32,6 +34,7 @@ class Params(ctypes.Structure):
         ("outer_block_size", ctypes.c_int32), ("outer_2d", ctypes.c_int32), ("inner_2d", ctypes.c_int32),
         ("scale_format", ctypes.c_int32), ("rounding", ctypes.c_int32),
         ("seed", ctypes.c_uint64), ("step", ctypes.c_uint32), ("use_precomputed_outer", ctypes.c_int32),
+        ("scale_layout", ctypes.c_int32),
     ]
 
 
@@ -90,7 +93,7 @@ def load(fast_math: bool = False, path: str | None = None):
     L.fp4q_status_string.argtypes = [I]
     L.fp4q_abi_version.restype = I
     L.fp4q_abi_version.argtypes = []
-    if L.fp4q_abi_version() != 1:
+    if L.fp4q_abi_version() != ABI_VERSION:
         raise RuntimeError("libfp4q ABI version mismatch")
     _libs[key] = L
     return L

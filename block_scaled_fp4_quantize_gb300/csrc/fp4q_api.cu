@@ -58,6 +58,7 @@ int check_nvfp4(const fp4q_params_t* p, uint32_t mask) {
   if (p->scale_format != FP4Q_SCALE_E4M3 && p->scale_format != FP4Q_SCALE_UE5M3) return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE && p->rounding != FP4Q_STOCHASTIC) return FP4Q_ERR_MODE;
   if ((p->outer_2d & ~1) || (p->inner_2d & ~1) || (p->use_precomputed_outer & ~1)) return FP4Q_ERR_MODE;
+  if (p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR && p->scale_layout != FP4Q_SCALE_LAYOUT_MMA) return FP4Q_ERR_MODE;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K) return FP4Q_ERR_SHAPE;
   if (p->K % 16) return FP4Q_ERR_SHAPE;
   const bool col = (mask & FP4Q_OUT_COL) != 0u;
@@ -79,9 +80,10 @@ void sizes_for(const fp4q_params_t* p, uint32_t mask, fp4q_sizes_t* s) {
   const bool row = (mask & FP4Q_OUT_ROW) != 0u, col = (mask & FP4Q_OUT_COL) != 0u;
   const bool outer = p->mode == FP4Q_MODE_OUTER_BLOCK;
   s->row_codes = row ? (size_t)(G * M * K / 2) : 0;
-  s->row_scales = row ? (size_t)(G * M * K / 16) : 0;
+  const int mma = p->scale_layout == FP4Q_SCALE_LAYOUT_MMA;
+  s->row_scales = row ? (size_t)sf_bytes(make_scale_layout(mma, M, K / 16), G) : 0;
   s->col_codes = col ? (size_t)(G * K * M / 2) : 0;
-  s->col_scales = col ? (size_t)(G * K * M / 16) : 0;
+  s->col_scales = col ? (size_t)sf_bytes(make_scale_layout(mma, K, M / 16), G) : 0;
   s->row_outer = (outer && !p->outer_2d && row) ? (size_t)(G * M * (K / ob)) * sizeof(float) : 0;
   s->col_outer = (outer && !p->outer_2d && col) ? (size_t)(G * K * (M / ob)) * sizeof(float) : 0;
   s->tile_outer = (outer && p->outer_2d) ? (size_t)(G * (M / ob) * (K / ob)) * sizeof(float)
@@ -107,6 +109,9 @@ QuantJob base_job(const fp4q_params_t* p, const void* x, float* residual) {
   j.seed = p->seed;
   j.step = p->step;
   j.out_bf16 = p->out_dtype == FP4Q_BF16;
+  const int mma = p->scale_layout == FP4Q_SCALE_LAYOUT_MMA;
+  j.rsl = make_scale_layout(mma, p->M, p->K / 16);
+  j.csl = make_scale_layout(mma, p->K, p->M / 16);
   return j;
 }
 
@@ -222,6 +227,14 @@ int fp4_quantize(const fp4q_params_t* p, const void* x, const fp4q_outputs_t* ou
   j.row_outer = s.row_outer ? out->row_outer : nullptr;
   j.col_outer = s.col_outer ? out->col_outer : nullptr;
   j.tile_outer = s.tile_outer ? out->tile_outer : nullptr;
+  // tensor-core scale layout: the kernels write every real scale; the padding
+  // of partial 128 x 4 tiles is zero
+  if (j.rsl.mma && row && (p->M % 128 || (p->K / 16) % 4) &&
+      cudaMemsetAsync(j.row_scales, 0, s.row_scales, st) != cudaSuccess)
+    return FP4Q_ERR_CUDA;
+  if (j.csl.mma && col && (p->K % 128 || (p->M / 16) % 4) &&
+      cudaMemsetAsync(j.col_scales, 0, s.col_scales, st) != cudaSuccess)
+    return FP4Q_ERR_CUDA;
   rc = prepare_outer(p, j, workspace, st);
   if (rc) return rc;
   return launch_quantizer(j, vec_ok(p, x, residual, nullptr), st);
@@ -294,6 +307,7 @@ int fp4_dequantize(const fp4q_params_t* p, int orient, const uint8_t* codes, con
   j.outer_2d = p->outer_2d;
   j.ue5m3 = p->scale_format == FP4Q_SCALE_UE5M3;
   j.out_bf16 = p->out_dtype == FP4Q_BF16;
+  j.sl = make_scale_layout(p->scale_layout == FP4Q_SCALE_LAYOUT_MMA, j.R, j.C / 16);
   return launch_dequant(j, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }
 
@@ -305,7 +319,7 @@ int mxfp4_fake_quantize(const fp4q_params_t* p, const void* x, void* y, void* st
   rc = check_dtype(p->out_dtype);
   if (rc) return rc;
   if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
-      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0)
+      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0)
     return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K || p->K % 32) return FP4Q_ERR_SHAPE;

@@ -92,6 +92,21 @@ __device__ __forceinline__ void normalize16(const float (&u)[16], float (&x)[16]
   }
 }
 
+// normalize16 from the NEGATED values nu = -u (bf16 inputs widen to -u in
+// one instruction, so the negation the sign-safe Markstein form needs costs
+// nothing); same results.  Not for mode none.
+__device__ __forceinline__ void normalize16_neg(const float (&nu)[16], float (&x)[16], const Norm& n) {
+  if (n.fast) {
+    const float nr = bitsf(fbits(n.r) ^ 0x80000000u);
+    const uint64_t S2 = pk2(n.S, n.S), NR2 = pk2(nr, nr);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) upk2(markstein2(pk2(nu[i], nu[i + 1]), S2, NR2), x[i], x[i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = div_slow(bitsf(fbits(nu[i]) ^ 0x80000000u), n.S, n.pos);
+  }
+}
+
 // 16 values -> 16 codes (two 32-bit words, element 2i in the low nibble of
 // byte i); optional dequantized values (e2m1 * s) * S.
 template <bool SR, bool DEQ>

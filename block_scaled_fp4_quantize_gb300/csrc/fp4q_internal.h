@@ -14,6 +14,38 @@ enum SSource : int {
   S_FROM_BUFFER = 3,    // read from the outer-scale buffers (precomputed or pre-pass)
 };
 
+// Inner-scale buffer layout of one orientation: per matrix an R x C16 byte
+// matrix, linear, or in 128 x 4 tiles of 512 bytes (tile-row-major; inside a
+// tile byte (r, c) at (r mod 32) * 16 + (r / 32) * 4 + c), R padded to 128
+// and C16 to 4 per matrix.
+struct ScaleLayout {
+  int mma;
+  int64_t R, C16, nrb, ncb;  // rows, scales per row, tile rows, tile columns
+};
+
+inline ScaleLayout make_scale_layout(int mma, int64_t R, int64_t C16) {
+  return ScaleLayout{mma, R, C16, (R + 127) / 128, (C16 + 3) / 4};
+}
+
+// Byte offset of scale (g, r, c).
+__host__ __device__ __forceinline__ int64_t sf_offset(const ScaleLayout& L, int64_t g, int64_t r, int64_t c) {
+  if (!L.mma) return (g * L.R + r) * L.C16 + c;
+  return ((g * L.nrb + (r >> 7)) * L.ncb + (c >> 2)) * 512 + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (c & 3);
+}
+
+// Byte offset of the scale whose linear index is `lin` ((g R + r) C16 + c).
+__host__ __device__ __forceinline__ int64_t sf_from_linear(const ScaleLayout& L, int64_t lin) {
+  if (!L.mma) return lin;
+  const int64_t row = lin / L.C16, c = lin - row * L.C16;
+  const int64_t g = row / L.R, r = row - g * L.R;
+  return sf_offset(L, g, r, c);
+}
+
+// Bytes of an orientation's scale buffer for G matrices.
+inline int64_t sf_bytes(const ScaleLayout& L, int64_t G) {
+  return L.mma ? G * L.nrb * L.ncb * 512 : G * L.R * L.C16;
+}
+
 // One quantize / qdq job.  Rowwise quantities are indexed [G, M, K], the
 // columnwise ones [G, K, M].
 struct QuantJob {
@@ -38,6 +70,7 @@ struct QuantJob {
   void* y;          // qdq output [G, M, K] contiguous, or nullptr
   int out_bf16;
   int qdq_orient;   // 0: quantize; 1: qdq along K; 2: qdq along M
+  ScaleLayout rsl, csl;  // rowwise / columnwise inner-scale layouts
 };
 
 struct DequantJob {
@@ -49,6 +82,7 @@ struct DequantJob {
   int64_t M, K;      // the quantized tensor's shape (2-D scale indexing)
   int col;           // 1: columnwise buffers (2-D scales read transposed)
   int mode, ob, outer_2d, ue5m3, out_bf16;
+  ScaleLayout sl;    // the scale buffer's layout (R x C/16 per matrix)
 };
 
 struct MxJob {

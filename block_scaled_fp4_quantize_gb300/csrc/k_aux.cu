@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantJob j, int ve
         S = j.outer[(g * (j.M / j.ob) + mi / j.ob) * (j.K / j.ob) + kj / j.ob];
       }
     }
-    const float s = dec_scale(j.scales[b], f);
+    const float s = dec_scale(j.scales[sf_from_linear(j.sl, b)], f);
     const uint2 cw = *reinterpret_cast<const uint2*>(j.codes + b * 8);
     float v[16];
 #pragma unroll

@@ -478,12 +478,12 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
           for (int q = 0; q < G::RPT; ++q)
             if (q < nb) *reinterpret_cast<uint2*>(j.row_codes + (c0 + 16 * q) / 2) = make_uint2(cw[2 * q], cw[2 * q + 1]);
         }
-        if (nb == G::RPT && wide_scales && G::RPT == 2) {
+        if (nb == G::RPT && wide_scales && G::RPT == 2 && !j.rsl.mma) {
           *reinterpret_cast<uint16_t*>(j.row_scales + c0 / 16) = (uint16_t)scw;
         } else {
 #pragma unroll
           for (int q = 0; q < G::RPT; ++q)
-            if (q < nb) j.row_scales[c0 / 16 + q] = (uint8_t)(scw >> (8 * q));
+            if (q < nb) j.row_scales[sf_from_linear(j.rsl, c0 / 16 + q)] = (uint8_t)(scw >> (8 * q));
         }
       }
     }
@@ -626,12 +626,12 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
         for (int q = 0; q < G::CB; ++q)
           if (q < nb) *reinterpret_cast<uint2*>(j.col_codes + (c0 + 16 * q) / 2) = make_uint2(ccw[2 * q], ccw[2 * q + 1]);
       }
-      if (nb == G::CB && wide_scales && G::CB == 2) {
+      if (nb == G::CB && wide_scales && G::CB == 2 && !j.csl.mma) {
         *reinterpret_cast<uint16_t*>(j.col_scales + c0 / 16) = (uint16_t)cscw;
       } else {
 #pragma unroll
         for (int q = 0; q < G::CB; ++q)
-          if (q < nb) j.col_scales[c0 / 16 + q] = (uint8_t)(cscw >> (8 * q));
+          if (q < nb) j.col_scales[sf_from_linear(j.csl, c0 / 16 + q)] = (uint8_t)(cscw >> (8 * q));
       }
     }
     __syncthreads();

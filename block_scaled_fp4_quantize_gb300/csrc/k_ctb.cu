@@ -1,7 +1,8 @@
 // k_ctb.cu -- bf16 cast-transpose quantize: rowwise and columnwise NVFP4 /
 // AMD-FP4 codes from one TMA-staged 128 x 64 tile
-// ("Block-Scaled FP8 and FP4 Weight Quantization", the fused cast-transpose;
-// "NVFP4 quantization recipe", outer and inner scaling).
+// ("Block-Scaled FP8 and FP4 Weight Quantization", section 3, the fused
+// cast-transpose; "NVFP4 / AMD-FP4 outer-block (two-level) scaling for FP4
+// training", "Technical design", outer and inner scales).
 //
 // A CTA of 256 threads walks 128 (M) x 64 (K) tiles of x; each tile arrives
 // by a 3-D tensor copy with the 128-byte swizzle, three tiles in flight.
@@ -82,8 +83,9 @@ __device__ __forceinline__ float bf16x2_hmax(uint32_t m) {
 }
 
 // Per-block steps shared by both passes: inner scale, x' = u / S, codes.
-template <bool SR, bool UE5M3>
-__device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (&u)[16], float am, float S, float r,
+// With an outer scale (NEG) the block arrives negated, v = -u.
+template <bool SR, bool UE5M3, bool NEG>
+__device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (&v)[16], float am, float S, float r,
                                                 bool none, const QuantJob& j, uint32_t orient, uint64_t n0,
                                                 uint32_t& w0, uint32_t& w1) {
   Norm n;
@@ -98,7 +100,8 @@ __device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (
   float4 T;
   const uint32_t sc = block_scale<UE5M3>(tv, am, n, T);
   float x[16], dq[16];
-  normalize16(u, x, n);
+  if (NEG) normalize16_neg(v, x, n);
+  else normalize16(v, x, n);
   encode16<SR, false>(x, T, n, j.seed, j.step, orient, n0, w0, w1, dq);
   return sc;
 }
@@ -304,35 +307,46 @@ __global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __gr
       uint32_t cw[4], scw = 0;
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
-        float u[16];
-        const uint4 w0 = a[2 * b], w1 = a[2 * b + 1];
-        u[0] = bf16lo(w0.x); u[1] = bf16hi(w0.x); u[2] = bf16lo(w0.y); u[3] = bf16hi(w0.y);
-        u[4] = bf16lo(w0.z); u[5] = bf16hi(w0.z); u[6] = bf16lo(w0.w); u[7] = bf16hi(w0.w);
-        u[8] = bf16lo(w1.x); u[9] = bf16hi(w1.x); u[10] = bf16lo(w1.y); u[11] = bf16hi(w1.y);
-        u[12] = bf16lo(w1.z); u[13] = bf16hi(w1.z); u[14] = bf16lo(w1.w); u[15] = bf16hi(w1.w);
-        const uint32_t sc =
-            quant_block<SR, UE5M3>(tab, u, am[b], S[b], R[b], none, j, 0u, (uint64_t)(rel + 16 * b), cw[2 * b], cw[2 * b + 1]);
+        float u[16];  // u, or -u with an outer scale
+        const uint32_t wd[8] = {a[2 * b].x, a[2 * b].y, a[2 * b].z, a[2 * b].w,
+                                a[2 * b + 1].x, a[2 * b + 1].y, a[2 * b + 1].z, a[2 * b + 1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          u[2 * i] = BO == BO_NONE ? bf16lo(wd[i]) : nbf16lo(wd[i]);
+          u[2 * i + 1] = BO == BO_NONE ? bf16hi(wd[i]) : nbf16hi(wd[i]);
+        }
+        const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, am[b], S[b], R[b], none, j, 0u,
+                                                                  (uint64_t)(rel + 16 * b), cw[2 * b], cw[2 * b + 1]);
         scw |= sc << (8 * b);
       }
       if (rvalid) {
         const int nb = (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
+        // scale byte offset: linear rel / 16; tensor-core tiles: the tile of
+        // (m0 / 128, k0 / 64), row rr of it, columns 2 rh and 2 rh + 1
+        const int64_t so = j.rsl.mma ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
+                                           ((rr & 31) << 4) + ((rr >> 5) << 2) + 2 * rh
+                                     : rel / 16;
         if (nb == 2 && row_wide) {
           *reinterpret_cast<uint4*>(j.row_codes + rel / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          *reinterpret_cast<uint16_t*>(j.row_scales + rel / 16) = (uint16_t)scw;
+          *reinterpret_cast<uint16_t*>(j.row_scales + so) = (uint16_t)scw;
         } else {
           if (nb >= 1) {
             *reinterpret_cast<uint2*>(j.row_codes + rel / 2) = make_uint2(cw[0], cw[1]);
-            j.row_scales[rel / 16] = (uint8_t)scw;
+            j.row_scales[so] = (uint8_t)scw;
           }
           if (nb >= 2) {
             *reinterpret_cast<uint2*>(j.row_codes + rel / 2 + 8) = make_uint2(cw[2], cw[3]);
-            j.row_scales[rel / 16 + 1] = (uint8_t)(scw >> 8);
+            j.row_scales[so + 1] = (uint8_t)(scw >> 8);
           }
         }
       }
     }
 
     // --------------------------------------------------------- columnwise
+    if (!j.do_col) {  // rowwise-only call (tensor-core scale layout)
+      __syncthreads();
+      continue;
+    }
     uint32_t wv[16];
     {
       const unsigned char* rb = raw + warp * 16 * 128 + cbyte;
@@ -396,13 +410,14 @@ __global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __gr
     }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      float u[16];
+      float u[16];  // u, or -u with an outer scale
 #pragma unroll
-      for (int i = 0; i < 16; ++i) u[i] = c ? bf16hi(wv[i]) : bf16lo(wv[i]);
+      for (int i = 0; i < 16; ++i)
+        u[i] = BO == BO_NONE ? (c ? bf16hi(wv[i]) : bf16lo(wv[i])) : (c ? nbf16hi(wv[i]) : nbf16lo(wv[i]));
       const int64_t k = p.k0 + 2 * lane + c;
       uint32_t w0, w1;
-      const uint32_t sc = quant_block<SR, UE5M3>(tab, u, cam[c], S[c], R[c], none, j, 1u,
-                                                 (uint64_t)((p.g * K + k) * M + mb), w0, w1);
+      const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, cam[c], S[c], R[c], none, j, 1u,
+                                                                (uint64_t)((p.g * K + k) * M + mb), w0, w1);
       *reinterpret_cast<uint2*>(cst + (2 * lane + c) * CST + 8 * warp) = make_uint2(w0, w1);
       sst[(2 * lane + c) * 8 + warp] = (uint8_t)sc;
     }
@@ -432,12 +447,25 @@ __global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __gr
         const int64_t kk = p.k0 + t;
         if (kk < K) {
           const int nbm = (int)min((int64_t)8, (M - p.m0) / 16);
-          uint8_t* d = j.col_scales + ((p.g * K + kk) * M + p.m0) / 16;
           const uint2 v = *reinterpret_cast<const uint2*>(sst + t * 8);
-          if (nbm == 8 && cs_wide) {
-            *reinterpret_cast<uint2*>(d) = v;
+          if (j.csl.mma) {
+            // scale columns m0 / 16 + 4 h .. + 3 of row kk: 4 bytes of tile
+            // (kk / 128, m0 / 64 + h)
+            uint8_t* d = j.col_scales + ((p.g * j.csl.nrb + (kk >> 7)) * j.csl.ncb + (p.m0 >> 6)) * 512 +
+                         ((kk & 31) << 4) + (((kk >> 5) & 3) << 2);
+            if (nbm == 8) {
+              *reinterpret_cast<uint32_t*>(d) = v.x;
+              *reinterpret_cast<uint32_t*>(d + 512) = v.y;
+            } else {
+              for (int q = 0; q < nbm; ++q) d[(q >> 2) * 512 + (q & 3)] = (uint8_t)((q < 4 ? v.x : v.y) >> (8 * (q & 3)));
+            }
           } else {
-            for (int q = 0; q < nbm; ++q) d[q] = (uint8_t)((q < 4 ? v.x : v.y) >> (8 * (q & 3)));
+            uint8_t* d = j.col_scales + ((p.g * K + kk) * M + p.m0) / 16;
+            if (nbm == 8 && cs_wide) {
+              *reinterpret_cast<uint2*>(d) = v;
+            } else {
+              for (int q = 0; q < nbm; ++q) d[q] = (uint8_t)((q < 4 ? v.x : v.y) >> (8 * (q & 3)));
+            }
           }
         }
       }
@@ -491,7 +519,9 @@ cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, cudaStream_t
 }  // namespace
 
 bool ctb_supports(const QuantJob& j) {
-  return j.in_bf16 && j.do_col && j.qdq_orient == 0 && !j.residual && !j.inner_2d &&
+  // columnwise bf16 quantize, and rowwise-only bf16 quantize into the
+  // tensor-core scale layout (tile-aligned scale addressing)
+  return j.in_bf16 && (j.do_col || j.rsl.mma) && j.qdq_orient == 0 && !j.residual && !j.inner_2d &&
          (reinterpret_cast<uintptr_t>(j.x) & 15u) == 0 && (j.ld * 2) % 16 == 0;
 }
 

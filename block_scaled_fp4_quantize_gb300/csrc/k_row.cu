@@ -6,8 +6,9 @@
 // row index: element n = (g M + i) K + j is the flat index, its codes sit at
 // byte n / 2, its inner scale at n / 16, a 1 x ob outer scale at n / ob, and
 // the stochastic-rounding counter and the residual are indexed by n too
-// ("NVFP4 quantization recipe", outer and inner scaling; "Four Over Six /
-// error feedback" residual).  So the kernel streams blocks: lane l of a warp
+// ("NVFP4 / AMD-FP4 outer-block (two-level) scaling for FP4 training",
+// "Technical design"; fp4-train README, "Method" and "API" for the residual).
+// So the kernel streams blocks: lane l of a warp
 // owns block 32 w + l of its step, loads its 32 bytes (bf16) or 64 bytes
 // (binary32) with 256-bit loads, and a 1 x ob outer block is ob / 16
 // adjacent lanes, reduced with xor-shuffles.  No shared-memory tile, no
@@ -272,6 +273,7 @@ bool row_supports(const QuantJob& j) {
   if (!aligned32(j.x) || (j.residual && !aligned32(j.residual)) || (j.qdq_orient == 1 && !aligned32(j.y)))
     return false;
   if (j.s_src == S_IN_TILE && !(j.ob == 16 || j.ob == 32 || j.ob == 64)) return false;
+  if (j.rsl.mma) return false;  // the tensor-core scale layout is written by the tile kernels
   return true;
 }
 

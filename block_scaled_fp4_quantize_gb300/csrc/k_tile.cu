@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(NTHR) quant_tile_kernel(const QuantJob j) {
       else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, n0, deq);
       if (valid) {
         if (j.row_codes) *reinterpret_cast<uint2*>(j.row_codes + n0 / 2) = make_uint2(o.codes_lo, o.codes_hi);
-        if (j.row_scales) j.row_scales[n0 / 16] = (uint8_t)o.sc;
+        if (j.row_scales) j.row_scales[sf_offset(j.rsl, g, m, kb / 16)] = (uint8_t)o.sc;
         if (j.residual) {
           float rr[16];
 #pragma unroll
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(NTHR) quant_tile_kernel(const QuantJob j) {
       else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, n0, deq);
       if (valid) {
         if (j.col_codes) *reinterpret_cast<uint2*>(j.col_codes + n0 / 2) = make_uint2(o.codes_lo, o.codes_hi);
-        if (j.col_scales) j.col_scales[n0 / 16] = (uint8_t)o.sc;
+        if (j.col_scales) j.col_scales[sf_offset(j.csl, g, k, mb / 16)] = (uint8_t)o.sc;
       }
       if (qdq_col) {
         // transpose the dequantized segment back to x's layout through smem

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define FP4Q_ABI_VERSION 1
+#define FP4Q_ABI_VERSION 2
 
 /* ---- status codes ------------------------------------------------------ */
 #define FP4Q_OK 0
@@ -74,6 +74,9 @@ extern "C" {
 
 #define FP4Q_OUT_ROW 1u /* rowwise buffers (blocks along K)                       */
 #define FP4Q_OUT_COL 2u /* columnwise buffers (blocks along M, stored as x^T)     */
+/* inner-scale buffer layouts (p->scale_layout) */
+#define FP4Q_SCALE_LAYOUT_LINEAR 0 /* [G, R, C/16] row-major                     */
+#define FP4Q_SCALE_LAYOUT_MMA 1    /* 128 x 4 tiles read by block-scaled MMA    */
 
 /* ---- parameters ----------------------------------------------------------
  * Rules checked by every entry point (FP4Q_ERR_SHAPE / _MODE / _DTYPE):
@@ -107,7 +110,23 @@ typedef struct fp4q_params {
                                     instead of computing them ("NVFP4 / AMD-FP4
                                     outer-block scaling", "Implementation":
                                     precomputed_outer_scale)                        */
+  int32_t scale_layout; /* FP4Q_SCALE_LAYOUT_LINEAR | FP4Q_SCALE_LAYOUT_MMA (below) */
 } fp4q_params_t;
+
+/* Inner-scale layouts.  An orientation's scales form, per matrix g, an
+ * R x C16 byte matrix (rowwise: R = M, C16 = K/16; columnwise: R = K,
+ * C16 = M/16).
+ *   LINEAR: byte (g, r, c) at (g R + r) C16 + c.
+ *   MMA: the layout NVFP4 tensor cores read the scales of a K-major operand
+ *     in ("fp4-train" README, "Method": codes and scales in the layout
+ *     Blackwell FP4 tensor cores consume; the tiling itself is NVIDIA's
+ *     published block-scaling-factor layout of the cuBLAS documentation,
+ *     "1D Block Scaling Factors Layout").  R is padded to a multiple of 128
+ *     and C16 to a multiple of 4 (padding bytes are zero); the matrix is cut
+ *     into 128 x 4 tiles stored one after another, tile (R / 128 index,
+ *     C16 / 4 index) row-major, 512 bytes each; inside a tile, byte (r, c) is
+ *     at (r mod 32) * 16 + (r / 32) * 4 + c.  Matrices follow one another,
+ *     each padded.  fp4q_query_sizes reports the padded sizes. */
 
 /* Output buffers of fp4_quantize (device pointers; NULL when unused).
  *   row_codes   uint8 [G, M, K/2]     row_scales  uint8 [G, M, K/16]
@@ -139,7 +158,7 @@ typedef struct fp4q_sizes {
 } fp4q_sizes_t;
 
 /* Fill *p with defaults: struct_size set, G = 1, bf16 in and out, mode none,
- * E4M3, RNE, rowwise output, everything else 0. */
+ * E4M3, RNE, rowwise output, linear scale layout, everything else 0. */
 void fp4q_params_init(fp4q_params_t *p);
 
 /* Validate *p and report the buffer sizes fp4_quantize needs for p->out_mask

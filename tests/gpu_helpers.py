@@ -77,3 +77,16 @@ def snr_db(x: np.ndarray, y: np.ndarray) -> float:
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def to_mma_layout(lin: np.ndarray) -> np.ndarray:
+    """[G, R, C16] linear inner scales -> the flat 128 x 4 tiled layout that
+    block-scaled tensor-core MMAs read (rows padded to 128, columns to 4,
+    padding zero; tiles row-major; inside a tile byte (r, c) at
+    (r mod 32) * 16 + (r // 32) * 4 + c), written from its definition."""
+    G, R, C = lin.shape
+    Rp, Cp = -(-R // 128) * 128, -(-C // 4) * 4
+    pad = np.zeros((G, Rp, Cp), np.uint8)
+    pad[:, :R, :C] = lin
+    t = pad.reshape(G, Rp // 128, 4, 32, Cp // 4, 4)          # g, tile row, r // 32, r % 32, tile col, c
+    return np.ascontiguousarray(t.transpose(0, 1, 4, 3, 2, 5)).reshape(-1)

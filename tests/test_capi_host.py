@@ -36,7 +36,7 @@ def test_header_declares_the_bound_functions():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.fp4q_abi_version() == 1
+    assert lib.fp4q_abi_version() == 2
     out = os.popen("nm -D --defined-only %s" % _capi._build.lib_path()).read()
     for name in declared_functions():
         assert re.search(r"\sT\s%s$" % name, out, re.M), name
@@ -45,8 +45,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_params_struct_layout_matches(lib):
     p = _capi.Params()
     lib.fp4q_params_init(ctypes.byref(p))
-    assert p.struct_size == ctypes.sizeof(_capi.Params) == 88
-    assert (p.G, p.in_dtype, p.out_dtype, p.mode, p.out_mask) == (1, _capi.BF16, _capi.BF16, 0, 1)
+    assert p.struct_size == ctypes.sizeof(_capi.Params) == 96
+    assert (p.G, p.in_dtype, p.out_dtype, p.mode, p.out_mask, p.scale_layout) == (1, _capi.BF16, _capi.BF16, 0, 1, 0)
     assert ctypes.sizeof(_capi.Outputs) == 7 * 8 and ctypes.sizeof(_capi.Sizes) == 8 * 8
 
 
@@ -165,3 +165,23 @@ def test_empty_inputs_enqueue_nothing(lib):
 def test_status_strings(lib):
     for code, name in _capi.STATUS.items():
         assert lib.fp4q_status_string(code).decode().startswith(name)
+
+
+def test_mma_scale_layout_sizes_and_validation(lib):
+    """Tensor-core scale layout: rows padded to 128 and scales per row to 4,
+    512-byte tiles per matrix; other layout codes are rejected."""
+    for G, M, K in ((1, 208, 336), (3, 128, 256), (2, 16, 64), (1, 4096, 7168)):
+        p = mk(lib, G=G, M=M, K=K, out_mask=3, scale_layout=1)
+        s = _capi.Sizes()
+        assert lib.fp4q_query_sizes(ctypes.byref(p), ctypes.byref(s)) == 0
+        cdiv = lambda a, b: -(-a // b)
+        assert s.row_scales == G * cdiv(M, 128) * cdiv(K // 16, 4) * 512
+        assert s.col_scales == G * cdiv(K, 128) * cdiv(M // 16, 4) * 512
+        assert s.row_codes == G * M * K // 2
+        p.scale_layout = 0
+        assert lib.fp4q_query_sizes(ctypes.byref(p), ctypes.byref(s)) == 0
+        assert s.row_scales == G * M * K // 16 and s.col_scales == G * K * M // 16
+    p = mk(lib, scale_layout=2)
+    assert lib.fp4q_query_sizes(ctypes.byref(p), ctypes.byref(_capi.Sizes())) == -4  # FP4Q_ERR_MODE
+    p = mk(lib, scale_layout=1)
+    assert lib.mxfp4_fake_quantize(ctypes.byref(p), None, None, None) == -4  # FP4Q_ERR_MODE
