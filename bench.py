@@ -252,6 +252,27 @@ def _extra_workloads():
             return "%d x bf16[5760,2880] 2-D 64x64 outer %s rowwise+columnwise" % (G, fmt), nb, ms, 1
         return run
 
+    def moe_grouped_tokens(iters, warmup, opts):
+        # 65536 tokens routed to 32 experts with lognormal popularity (seed 0),
+        # each expert's count rounded down to a multiple of 64 (the outer block)
+        Ge, T, Kt = 32, 65536, 2880
+        gen = torch.Generator("cpu").manual_seed(0)
+        w = torch.exp(torch.randn(Ge, generator=gen))
+        cnt = (w / w.sum() * T).floor().long() // 64 * 64
+        cnt[-1] += T - int(cnt.sum())
+        off = torch.zeros(Ge + 1, dtype=torch.int64)
+        off[1:] = torch.cumsum(cnt, 0)
+        xt = (torch.randn(T, Kt, generator=torch.Generator(dev).manual_seed(1), device=dev)).to(torch.bfloat16)
+        offd = off.to(dev)
+        kw = dict(mode="outer_block", outer_block_size=64, rowwise=True, columnwise=True)
+        q = fq.quantize_grouped(xt, offd, **kw)
+        ws = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+        ms = _events_time(lambda i: fq.quantize_grouped(xt, offd, out=q, workspace=ws, **kw), iters, warmup)
+        n = T * Kt
+        nb = n * 2 + 2 * (n // 2) + 2 * (n // 16) + 2 * (n // 64) * 4
+        return ("%d tokens x bf16[%d] in %d ragged expert groups (%d..%d rows), 1x64 outer, rowwise+columnwise" % (
+            T, Kt, Ge, int(cnt.min()), int(cnt.max())), nb, ms, 2)
+
     def sr_ef_weight_qdq(iters, warmup, opts):
         g = torch.Generator(dev).manual_seed(0)
         Wt = torch.randn(8192, 8192, generator=g, device=dev) * 0.02
@@ -277,6 +298,7 @@ def _extra_workloads():
         "dequantize_activations": (dequantize_activations, 50, 5),
         "moe_experts_e4m3": (_moe("e4m3"), 20, 3),
         "moe_experts_ue5m3": (_moe("ue5m3"), 20, 3),
+        "moe_grouped_tokens": (moe_grouped_tokens, 30, 3),
         "sr_ef_weight_qdq": (sr_ef_weight_qdq, 20, 3),
     }
 

@@ -23,7 +23,7 @@ import torch
 from . import _capi
 from ._capi import FP4QError
 
-__all__ = ["QuantizedFP4", "quantize", "dequantize", "qdq", "mxfp4_fake_quantize", "mxfp4_fake_quantize_host",
+__all__ = ["QuantizedFP4", "quantize", "quantize_grouped", "dequantize", "qdq", "mxfp4_fake_quantize", "mxfp4_fake_quantize_host",
            "tensor_amax", "build", "FP4QError", "query_sizes", "host_workspace_bytes"]
 
 _MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
@@ -115,6 +115,8 @@ class QuantizedFP4:
     col_outer: Optional[torch.Tensor] = None   # float32 [G, K, M/ob]
     tile_outer: Optional[torch.Tensor] = None  # float32 [G, M/ob, K/ob] or [1]
     scale_layout: str = "linear"               # inner-scale layout: "linear" or "mma" (128 x 4 tiles)
+    group_offsets: Optional[torch.Tensor] = None  # quantize_grouped: int64 [groups + 1]
+    group_error: Optional[torch.Tensor] = None    # quantize_grouped: nonzero if the offsets were invalid
 
 
 def _outer_shapes(G, M, K, mode, ob, outer_2d, row, col):
@@ -177,6 +179,61 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
     st = _lib().fp4_quantize(ctypes.byref(p), _ptr(x3), ctypes.byref(o), _ptr(residual), _ptr(ws),
                              int(s.workspace), _stream(dev))
     _capi.check(st, "fp4_quantize")
+    return q
+
+
+def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0,
+                     outer_2d: bool = False, scale_format: str = "e4m3", stochastic: bool = False, seed: int = 0,
+                     step: int = 0, rowwise: bool = True, columnwise: bool = False,
+                     precomputed_outer: Optional[QuantizedFP4] = None, out: Optional[QuantizedFP4] = None,
+                     workspace: Optional[torch.Tensor] = None) -> QuantizedFP4:
+    """Ragged grouped NVFP4 / AMD-FP4 quantize: rows offsets[e] ..
+    offsets[e + 1] of the bf16 [M, K] CUDA tensor x form group e (e.g. the
+    tokens routed to expert e), each quantized as a matrix of its own.
+    ``offsets`` is a CUDA int64 tensor [groups + 1] (read on the device).
+    Columnwise buffers hold each group's transpose back to back (see
+    include/fp4q.h); tensorwise mode gives one scale per group in
+    ``tile_outer``.  Invalid offsets write nothing and set ``q.group_error``
+    (a CUDA int32 tensor) nonzero."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    if not (offsets.is_cuda and offsets.dtype == torch.int64 and offsets.dim() == 1 and offsets.is_contiguous()):
+        raise ValueError("offsets must be a contiguous CUDA int64 vector [groups + 1]")
+    x3, G, M, K, ld = _view3d(x)
+    ngroups = offsets.numel() - 1
+    mask = (_capi.OUT_ROW if rowwise else 0) | (_capi.OUT_COL if columnwise else 0)
+    p = _params(G, M, K, ld, x.dtype, mode=mode, outer_block_size=outer_block_size, outer_2d=outer_2d,
+                scale_format=scale_format, stochastic=stochastic, seed=seed, step=step, out_mask=mask,
+                use_precomputed_outer=precomputed_outer is not None)
+    s = _capi.Sizes()
+    _capi.check(_lib().fp4q_query_sizes_grouped(ctypes.byref(p), ngroups, ctypes.byref(s)), "fp4q_query_sizes_grouped")
+    dev = x.device
+    if out is None:
+        u8 = dict(dtype=torch.uint8, device=dev)
+        q = QuantizedFP4((1, M, K), mode, outer_block_size, outer_2d, False, scale_format)
+        if rowwise:
+            q.row_codes = torch.empty(1, M, K // 2, **u8)
+            q.row_scales = torch.empty(1, M, K // 16, **u8)
+        if columnwise:
+            q.col_codes = torch.empty(K * M // 2, **u8)      # group transposes back to back
+            q.col_scales = torch.empty(K * M // 16, **u8)
+        for name, nbytes in (("row_outer", s.row_outer), ("col_outer", s.col_outer), ("tile_outer", s.tile_outer)):
+            if nbytes:
+                src = getattr(precomputed_outer, name, None) if precomputed_outer is not None else None
+                setattr(q, name, src if src is not None else torch.empty(int(nbytes) // 4, dtype=torch.float32,
+                                                                          device=dev))
+    else:
+        q = out
+    q.group_offsets = offsets
+    if workspace is None or workspace.numel() < s.workspace:
+        workspace = torch.empty(int(s.workspace), dtype=torch.uint8, device=dev)
+    q.group_error = workspace[:4].view(torch.int32)
+    o = _capi.Outputs(*[_ptr(getattr(q, n)) for n in
+                        ("row_codes", "row_scales", "row_outer", "col_codes", "col_scales", "col_outer",
+                         "tile_outer")])
+    st = _lib().fp4_quantize_grouped(ctypes.byref(p), _ptr(x3), _ptr(offsets), ngroups, ctypes.byref(o),
+                                     _ptr(workspace), int(workspace.numel()), _stream(dev))
+    _capi.check(st, "fp4_quantize_grouped")
     return q
 
 

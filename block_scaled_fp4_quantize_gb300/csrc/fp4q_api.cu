@@ -240,6 +240,79 @@ int fp4_quantize(const fp4q_params_t* p, const void* x, const fp4q_outputs_t* ou
   return launch_quantizer(j, vec_ok(p, x, residual, nullptr), st);
 }
 
+int fp4q_query_sizes_grouped(const fp4q_params_t* p, int64_t ngroups, fp4q_sizes_t* sizes) {
+  if (!p || !sizes) return FP4Q_ERR_NULL;
+  const int rc = check_nvfp4(p, p->out_mask);
+  if (rc) return rc;
+  if (p->G != 1 || ngroups < 1 || ngroups > 65535) return FP4Q_ERR_SHAPE;
+  sizes_for(p, p->out_mask, sizes);
+  if (p->mode == FP4Q_MODE_TENSORWISE) sizes->tile_outer = (size_t)ngroups * sizeof(float);
+  sizes->workspace = group_ws_bytes(ngroups);
+  return FP4Q_OK;
+}
+
+int fp4_quantize_grouped(const fp4q_params_t* p, const void* x, const int64_t* offsets, int64_t ngroups,
+                         const fp4q_outputs_t* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p || !out) return FP4Q_ERR_NULL;
+  fp4q_sizes_t s;
+  int rc = fp4q_query_sizes_grouped(p, ngroups, &s);
+  if (rc) return rc;
+  const uint32_t mask = p->out_mask;
+  const bool row = mask & FP4Q_OUT_ROW, col = mask & FP4Q_OUT_COL;
+  const bool small_ob = p->outer_block_size == 16 || p->outer_block_size == 32 || p->outer_block_size == 64;
+  if (p->in_dtype != FP4Q_BF16 || p->inner_2d || p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR ||
+      (p->use_precomputed_outer && p->mode != FP4Q_MODE_OUTER_BLOCK) ||
+      (p->mode == FP4Q_MODE_OUTER_BLOCK && col && !p->outer_2d && !small_ob && !p->use_precomputed_outer))
+    return FP4Q_ERR_UNSUPPORTED;
+  if (!offsets || !workspace) return FP4Q_ERR_NULL;
+  if (workspace_bytes < s.workspace) return FP4Q_ERR_WORKSPACE;
+  if (!aligned(workspace, 16) || !aligned(offsets, 8)) return FP4Q_ERR_ALIGN;
+  if (p->M == 0 || p->K == 0) return FP4Q_OK;
+  if (!x) return FP4Q_ERR_NULL;
+  if (row && (!out->row_codes || !out->row_scales)) return FP4Q_ERR_NULL;
+  if (col && (!out->col_codes || !out->col_scales)) return FP4Q_ERR_NULL;
+  if ((s.row_outer && !out->row_outer) || (s.col_outer && !out->col_outer) || (s.tile_outer && !out->tile_outer))
+    return FP4Q_ERR_NULL;
+  if (!vec_aligned(x, p->ld * 2)) return FP4Q_ERR_ALIGN;
+  if ((row && !aligned(out->row_codes, 8)) || (col && !aligned(out->col_codes, 8))) return FP4Q_ERR_ALIGN;
+  if (!aligned(out->row_outer, 4) || !aligned(out->col_outer, 4) || !aligned(out->tile_outer, 4)) return FP4Q_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  QuantJob j = base_job(p, x, nullptr);
+  j.do_row = row;
+  j.do_col = col;
+  j.row_codes = row ? out->row_codes : nullptr;
+  j.row_scales = row ? out->row_scales : nullptr;
+  j.col_codes = col ? out->col_codes : nullptr;
+  j.col_scales = col ? out->col_scales : nullptr;
+  j.row_outer = s.row_outer ? out->row_outer : nullptr;
+  j.col_outer = s.col_outer ? out->col_outer : nullptr;
+  j.tile_outer = s.tile_outer ? out->tile_outer : nullptr;
+  j.ngroups = ngroups;
+  j.goff = offsets;
+  j.gws = static_cast<GroupWs*>(workspace);
+  // every group a whole number of the blocks that span rows
+  int align = 1;
+  if (col) align = 16;
+  if (p->mode == FP4Q_MODE_OUTER_BLOCK && (p->outer_2d || col)) align = p->outer_block_size;
+  const bool tw = p->mode == FP4Q_MODE_TENSORWISE;
+  if (launch_group_prep(j, align, tw, st) != cudaSuccess) return FP4Q_ERR_CUDA;
+  if (p->mode == FP4Q_MODE_NONE) {
+    j.s_src = S_ONE;
+  } else if (tw) {
+    j.s_src = S_TENSORWISE_WS;  // per-group amax from the workspace
+  } else if (p->use_precomputed_outer) {
+    j.s_src = S_FROM_BUFFER;
+  } else if (p->outer_block_size == 16 || p->outer_block_size == 32 || p->outer_block_size == 64) {
+    j.s_src = S_IN_TILE;
+  } else {
+    j.s_src = S_FROM_BUFFER;  // group boundaries are whole outer blocks: the pre-pass of the whole tensor holds
+    if (launch_outer_prepass(j, st) != cudaSuccess) return FP4Q_ERR_CUDA;
+  }
+  cudaError_t e = cudaSuccess;
+  if (!launch_ctb(j, st, &e)) return FP4Q_ERR_CUDA;
+  return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
 int fp4_qdq(const fp4q_params_t* p, int orient, const void* x, void* y, float* residual, float* outer, void* workspace,
             size_t workspace_bytes, void* stream) {
   if (!p) return FP4Q_ERR_NULL;

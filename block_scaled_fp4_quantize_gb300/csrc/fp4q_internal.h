@@ -46,6 +46,26 @@ inline int64_t sf_bytes(const ScaleLayout& L, int64_t G) {
   return L.mma ? G * L.nrb * L.ncb * 512 : G * L.R * L.C16;
 }
 
+// Device workspace of a grouped quantize: a validity flag and the tile count
+// (set by the preparation kernel), the per-group prefix of 128-row tiles
+// (tprefix[e] = tiles of the groups before e) and the per-group amax.
+struct GroupWs {
+  uint32_t bad;     // nonzero: offsets invalid, nothing is written
+  uint32_t mtiles;  // total 128-row tiles over all groups
+  uint32_t pad[2];
+  // followed by uint32_t tprefix[ngroups + 1], then uint32_t amax[ngroups]
+};
+
+inline size_t group_ws_bytes(int64_t ngroups) {
+  return (size_t)(16 + 4 * (ngroups + 1) + 4 * ngroups + 255) / 256 * 256;
+}
+__host__ __device__ __forceinline__ uint32_t* group_tprefix(GroupWs* w) {
+  return reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(w) + 16);
+}
+__host__ __device__ __forceinline__ uint32_t* group_amax(GroupWs* w, int64_t ngroups) {
+  return group_tprefix(w) + ngroups + 1;
+}
+
 // One quantize / qdq job.  Rowwise quantities are indexed [G, M, K], the
 // columnwise ones [G, K, M].
 struct QuantJob {
@@ -71,6 +91,11 @@ struct QuantJob {
   int out_bf16;
   int qdq_orient;   // 0: quantize; 1: qdq along K; 2: qdq along M
   ScaleLayout rsl, csl;  // rowwise / columnwise inner-scale layouts
+  // ragged groups (0 = none): rows [goff[e], goff[e + 1]) of the [M, K]
+  // input form group e, quantized as a matrix of its own
+  int64_t ngroups;
+  const int64_t* goff;  // device [ngroups + 1]
+  GroupWs* gws;         // device workspace of the grouped path
 };
 
 struct DequantJob {
@@ -104,11 +129,14 @@ bool ct_supports(const QuantJob& j);
 bool row_supports(const QuantJob& j);
 bool ctb_supports(const QuantJob& j);
 bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err);
+bool launch_ctb_grouped(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 cudaError_t launch_row(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_ct(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st);
 cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st);
 cudaError_t launch_mxfp4(const MxJob& j, cudaStream_t st);
+// grouped path: offsets check + tile prefix (+ per-group amax for tensorwise)
+cudaError_t launch_group_prep(const QuantJob& j, int align, bool amax, cudaStream_t st);
 
 }  // namespace fp4q

@@ -23,9 +23,13 @@ struct TileIter {
   int tiles_k, tiles_m, ntiles, idx, tk, tm, g, dk, dm, dg;
   template <int TM>
   __device__ __forceinline__ void init(const QuantJob& j) {
-    tiles_k = (int)((j.K + 63) / 64);
-    tiles_m = (int)((j.M + TM - 1) / TM);
-    ntiles = (int)(j.G * tiles_m * tiles_k);
+    init_n((int)((j.K + 63) / 64), (int)((j.M + TM - 1) / TM), (int)j.G);
+  }
+  // a walk over G x tiles_m x tiles_k tiles (tk fastest)
+  __device__ __forceinline__ void init_n(int tiles_k_, int tiles_m_, int g_count) {
+    tiles_k = tiles_k_ > 0 ? tiles_k_ : 1;
+    tiles_m = tiles_m_ > 0 ? tiles_m_ : 1;
+    ntiles = (tiles_k_ > 0 && tiles_m_ > 0) ? g_count * tiles_m * tiles_k : 0;
     idx = (int)blockIdx.x;
     tk = idx % tiles_k;
     tm = (idx / tiles_k) % tiles_m;

@@ -131,6 +131,70 @@ __global__ void __launch_bounds__(256) tensor_amax_flat_kernel(const QuantJob j,
   if (threadIdx.x == 0) atomicMax(amax, v);
 }
 
+// Grouped path, one CTA: checks the offsets (0 = goff[0] <= ... <=
+// goff[n] = M, every group a multiple of `align` rows), writes the prefix of
+// 128-row tiles per group and the total, and clears the per-group amax.
+__global__ void __launch_bounds__(1024) group_prep_kernel(const QuantJob j, int align) {
+  __shared__ uint32_t part[1024];
+  GroupWs* w = j.gws;
+  const int64_t n = j.ngroups;
+  uint32_t* tp = group_tprefix(w);
+  uint32_t* am = group_amax(w, n);
+  const int t = threadIdx.x;
+  if (t == 0) w->bad = 0u;
+  __syncthreads();
+  const int64_t chunk = (n + 1023) / 1024;
+  const int64_t e0 = t * chunk, e1 = e0 + chunk < n ? e0 + chunk : n;
+  uint32_t bad = 0, sum = 0;
+  if (t == 0 && (j.goff[0] != 0 || j.goff[n] != j.M)) bad = 1;
+  for (int64_t e = e0; e < e1; ++e) {
+    const int64_t a = j.goff[e], b = j.goff[e + 1];
+    if (b < a || (b - a) % align) bad = 1;
+    else sum += (uint32_t)((b - a + 127) / 128);
+    am[e] = 0u;
+    if (j.mode == 1 && j.tile_outer && b == a) j.tile_outer[e] = 0.0f;  // an empty group's tensorwise scale
+  }
+  if (bad) atomicOr(&w->bad, 1u);
+  part[t] = sum;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {  // inclusive scan of the chunk sums
+    const uint32_t v = t >= o ? part[t - o] : 0u;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  uint32_t run = t ? part[t - 1] : 0u;
+  for (int64_t e = e0; e < e1; ++e) {
+    tp[e] = run;
+    const int64_t a = j.goff[e], b = j.goff[e + 1];
+    if (b >= a) run += (uint32_t)((b - a + 127) / 128);
+  }
+  if (t == 1023) {
+    tp[n] = part[1023];
+    w->mtiles = part[1023];
+  }
+}
+
+// Per-group tensorwise amax of a bf16 [M, K] input (row stride ld, 16-byte
+// aligned rows): blockIdx.y = group, CTAs along x stride over its rows.
+__global__ void __launch_bounds__(256) group_amax_kernel(const QuantJob j) {
+  __shared__ uint32_t sh[8];
+  GroupWs* w = j.gws;
+  if (w->bad) return;
+  const int64_t e = blockIdx.y;
+  const int64_t r0 = j.goff[e], r1 = j.goff[e + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t units = j.K / 8;
+  uint32_t acc = 0;
+  for (int64_t r = r0 + (int64_t)blockIdx.x * 8 + warp; r < r1; r += (int64_t)gridDim.x * 8) {
+    const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(j.x) + r * j.ld);
+    for (int64_t u = lane; u < units; u += 32) amax_unit<true, false>(__ldcs(row + u), nullptr, acc);
+  }
+  uint32_t v = umax(fix_abs(acc & 0x7FFFu, 0x7F80u, 0x7F7Fu), fix_abs((acc >> 16) & 0x7FFFu, 0x7F80u, 0x7F7Fu)) << 16;
+  v = block_max(v, sh);
+  if (threadIdx.x == 0 && v) atomicMax(&group_amax(w, j.ngroups)[e], v);
+}
+
 // 1-D rowwise outer scales (ob along K): one warp per outer block.
 __global__ void __launch_bounds__(256) outer_row_kernel(const QuantJob j) {
   const ScaleFmt f = scale_fmt(j.ue5m3);
@@ -266,6 +330,19 @@ cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_
   }
   tensor_amax_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(j, amax_ws);
   return cudaGetLastError();
+}
+
+cudaError_t launch_group_prep(const QuantJob& j, int align, bool amax, cudaStream_t st) {
+  group_prep_kernel<<<1, 1024, 0, st>>>(j, align);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (amax) {
+    const int64_t per = (int64_t)num_sms() * 8 / (j.ngroups > 0 ? j.ngroups : 1);
+    const dim3 grid((unsigned)(per < 1 ? 1 : (per > 64 ? 64 : per)), (unsigned)j.ngroups);
+    group_amax_kernel<<<grid, 256, 0, st>>>(j);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st) {

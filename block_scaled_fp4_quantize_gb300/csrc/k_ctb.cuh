@@ -1,0 +1,560 @@
+// k_ctb.cuh -- the bf16 cast-transpose kernel body, instantiated without
+// groups in k_ctb.cu and with ragged groups in k_ctb_grouped.cu (two
+// translation units, compiled in parallel).  Design notes: k_ctb.cu.
+#pragma once
+
+#include "fp4q_block.cuh"
+#include "fp4q_device.cuh"
+#include "fp4q_internal.h"
+#include "fp4q_tma.cuh"
+
+namespace fp4q {
+namespace {
+
+constexpr int BT = 256;             // threads per CTA
+constexpr int BM = 128, BK = 64;    // tile
+constexpr int BNS = 3;              // tiles in flight
+constexpr int BRAW = BM * BK * 2;   // bytes of one raw tile
+constexpr int CST = 72;             // bytes per staged column of codes (64 + 8 against bank conflicts)
+
+// Shared memory (offsets from the 1024-byte aligned base)
+struct BL {
+  __host__ __device__ static constexpr int raw(int s) { return s * BRAW; }
+  static constexpr int tab = BNS * BRAW;               // 256 x (s, zh, zl, -)
+  static constexpr int codes = tab + 256 * 16;         // 64 columns x CST
+  static constexpr int scales = codes + 64 * CST;      // 64 columns x 8
+  static constexpr int red2d = scales + 64 * 8;        // 32 x u32: 2-D sub-tile maxima
+  static constexpr int redc = red2d + 32 * 4;          // 64 x 4 u32: column 1-D outer maxima
+  static constexpr int sr2d = redc + 256 * 4;          // 32 x (S, 1 / S)
+  static constexpr int bars = sr2d + 32 * 8;           // BNS mbarriers
+  static constexpr int total = bars + 8 * BNS + 1024;  // + alignment slack
+};
+
+// Outer-scale source of a launch
+enum BOuter : int { BO_NONE = 0, BO_UNIFORM, BO_T1D, BO_T2D, BO_B1D, BO_B2D };
+
+__device__ unsigned int g_ctb_timeout = 0;
+
+__device__ __forceinline__ void issue_bf16_tile(const CUtensorMap* map, const TilePos& p, unsigned char* raw,
+                                                uint64_t* bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)BRAW);
+  tma_load3(raw, map, (int)p.k0, (int)p.m0, (int)p.g, bar);
+}
+
+// Sanitized copy of a bf16 pair (NaN -> +0, +-inf -> +-largest finite).
+__device__ __forceinline__ uint32_t sanitize_bf16x2(uint32_t w) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v = (w >> (16 * h)) & 0xFFFFu;
+    const uint32_t a = v & 0x7FFFu;
+    if (a > 0x7F80u) v = 0u;
+    else if (a == 0x7F80u) v = (v & 0x8000u) | 0x7F7Fu;
+    r |= v << (16 * h);
+  }
+  return r;
+}
+
+// max |.| of the two halves of a packed bf16 maximum, as binary32.
+__device__ __forceinline__ float bf16x2_hmax(uint32_t m) {
+  m &= 0x7FFF7FFFu;
+  const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+  return bitsf((hi > lo ? hi : lo) << 16);
+}
+
+// Per-block steps shared by both passes: inner scale, x' = u / S, codes.
+// With an outer scale (NEG) the block arrives negated, v = -u.
+template <bool SR, bool UE5M3, bool NEG>
+__device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (&v)[16], float am, float S, float r,
+                                                bool none, const QuantJob& j, uint32_t orient, uint64_t n0,
+                                                uint32_t& w0, uint32_t& w1) {
+  Norm n;
+  n.none = none;
+  n.S = S;
+  n.r = r;
+  n.pos = none || positive(S);
+  n.fast = !none && positive_normal(S) && positive_normal(r);
+  struct {
+    const float4* tab;
+  } tv{tab};
+  float4 T;
+  const uint32_t sc = block_scale<UE5M3>(tv, am, n, T);
+  float x[16], dq[16];
+  if (NEG) normalize16_neg(v, x, n);
+  else normalize16(v, x, n);
+  encode16<SR, false>(x, T, n, j.seed, j.step, orient, n0, w0, w1, dq);
+  return sc;
+}
+
+// Position in the grouped walk: group e owns the 128-row tiles
+// tprefix[e] .. tprefix[e + 1] - 1 of the walk; a cursor only moves forward
+// (a CTA's tile indices grow), so finding the group of a tile is amortized.
+struct GroupCursor {
+  int64_t e = -1;
+  uint32_t lo = 0, hi = 0;
+  __device__ __forceinline__ void seek(const uint32_t* tp, uint32_t q) {
+    while (hi <= q) {
+      ++e;
+      lo = hi;
+      hi = tp[e + 1];
+    }
+  }
+};
+
+template <bool SR, bool UE5M3, int BO, bool GR>
+__global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
+  extern __shared__ __align__(16) unsigned char smem_dyn[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float4* tab = reinterpret_cast<float4*>(smem + BL::tab);
+  unsigned char* cst = smem + BL::codes;
+  unsigned char* sst = smem + BL::scales;
+  uint32_t* red2d = reinterpret_cast<uint32_t*>(smem + BL::red2d);
+  uint32_t* redc = reinterpret_cast<uint32_t*>(smem + BL::redc);
+  float2* sr2d = reinterpret_cast<float2*>(smem + BL::sr2d);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BL::bars);
+
+  // grouped inputs: rows [goff[e], goff[e + 1]) form group e, quantized as
+  // a matrix of its own; the walk covers each group's 128-row tiles
+  constexpr bool gr = GR;
+  const uint32_t* gtp = gr ? group_tprefix(j.gws) : nullptr;
+  if (gr && j.gws->bad) return;  // invalid offsets: write nothing
+  TileIter cur;
+  if (gr) cur.init_n((int)((j.K + 63) / 64), (int)j.gws->mtiles, 1);
+  else cur.init<BM>(j);
+  GroupCursor gc, pc;  // processing cursor (all threads), prefetch cursor (thread 0)
+  auto tile_at = [&](int i) -> TilePos {
+    if (!gr) return cur.pos_of<BM>(i);
+    const uint32_t q = (uint32_t)(i / cur.tiles_k);
+    pc.seek(gtp, q);
+    return TilePos{0, j.goff[pc.e] + 128 * (int64_t)(q - pc.lo), (int64_t)(i - (int)q * cur.tiles_k) * 64};
+  };
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < BNS; ++s) mbar_init(&bars[s]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < BNS - 1; ++s) {
+      const int i = cur.idx + s * (int)gridDim.x;
+      if (i < cur.ntiles) issue_bf16_tile(&tmap, tile_at(i), smem + BL::raw(s), &bars[s]);
+    }
+  }
+  build_scale_table<UE5M3>(tab, t, BT);
+  if (t < 32) red2d[t] = 0u;
+  redc[t] = 0u;
+
+  const bool none = BO == BO_NONE;
+  const int ob = j.ob;
+  const int lob = ob > 0 ? 31 - __clz(ob) : 0;
+  const bool ob_pow2 = ob > 0 && (ob & (ob - 1)) == 0;
+  const int64_t mob = ob > 0 ? j.M / ob : 0, kob = ob > 0 ? j.K / ob : 0;
+  float S_u = 1.0f, r_u = 1.0f;
+  int64_t s_group = -1;  // group whose tensorwise scale S_u holds (grouped path)
+  if (BO == BO_UNIFORM && gr) {
+  } else if (BO == BO_UNIFORM) {
+    if (j.s_src == S_TENSORWISE_WS) {
+      S_u = ieee_div(bitsf(*j.tw_amax), UE5M3 ? 688128.0f : 2688.0f);
+      if (blockIdx.x == 0 && t == 0 && j.tile_outer) j.tile_outer[0] = S_u;
+    } else {
+      S_u = j.tile_outer[0];
+    }
+    r_u = ieee_rcp(S_u);
+  }
+  const int64_t M = j.M, K = j.K;
+  const bool row_wide = (K % 32) == 0 && ((reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0);
+
+  // rowwise ownership
+  const int rr = t >> 1, rh = t & 1;
+  // columnwise ownership: rows 16 warp .., columns 2 lane, 2 lane + 1; the
+  // swizzled byte offset of this lane's pair in row 16 warp + i is
+  // rowbase + (cunit ^ (i mod 8)) * 16 + cbyte
+  const int cunit = lane >> 2, cbyte = (lane & 3) * 4;
+  __syncthreads();
+
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int it = 0; cur.valid(); ++it) {
+    const unsigned char* raw = smem + BL::raw(slot);
+    TilePos p = cur.pos<BM>();
+    // the tile's group: rows [goff, gend), columnwise index of (k, m) =
+    // cbase + k * cstride + m (the group's own [K, rows] transpose)
+    int64_t gend = M, goff = 0, cbase = p.g * K * M, cstride = M;
+    if (gr) {
+      gc.seek(gtp, (uint32_t)cur.tm);
+      goff = j.goff[gc.e];
+      gend = j.goff[gc.e + 1];
+      p = TilePos{0, goff + 128 * (int64_t)((uint32_t)cur.tm - gc.lo), p.k0};
+      cbase = K * goff - goff;
+      cstride = gend - goff;
+      if (BO == BO_UNIFORM && gc.e != s_group) {  // the group's tensorwise scale
+        s_group = gc.e;
+        S_u = ieee_div(bitsf(group_amax(j.gws, j.ngroups)[gc.e]), UE5M3 ? 688128.0f : 2688.0f);
+        r_u = ieee_rcp(S_u);
+      }
+      if (BO == BO_UNIFORM && t == 0 && p.m0 == goff && p.k0 == 0 && j.tile_outer) j.tile_outer[gc.e] = S_u;
+    }
+    if (t == 0) {
+      const int i = cur.idx + (BNS - 1) * (int)gridDim.x;
+      const int s = slot == 0 ? BNS - 1 : slot - 1;
+      if (i < cur.ntiles) issue_bf16_tile(&tmap, tile_at(i), smem + BL::raw(s), &bars[s]);
+    }
+    cur.next();
+    const bool arrived = mbar_wait(&bars[slot], phase, 1u << 22);
+    if (!__syncthreads_and(arrived)) {
+      if (t == 0) {
+        atomicExch(&g_ctb_timeout, 1u);
+        for (int d = 1; d < BNS; ++d) {
+          const int i = it + d;
+          if (cur.idx + (d - 1) * (int)gridDim.x < cur.ntiles)
+            mbar_wait(&bars[i % BNS], (uint32_t)(i / BNS) & 1u, 1u << 22);
+        }
+      }
+      return;
+    }
+    if (++slot == BNS) {
+      slot = 0;
+      phase ^= 1u;
+    }
+
+    // ------------------------------------------------------------ rowwise
+    const int64_t m = p.m0 + rr;
+    const bool rvalid = m < gend;
+    const int64_t rel = (p.g * M + m) * K + p.k0 + 32 * rh;  // flat index of this thread's first element
+    uint4 a[4] = {};
+    float am[2] = {0.0f, 0.0f};
+    if (j.do_row || BO == BO_T2D) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      a[q] = *reinterpret_cast<const uint4*>(raw + (rr * 8 + ((4 * rh + q) ^ (rr & 7))) * 16);
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+      am[b] = bf16x2_hmax(bf16x2_amax(bf16x2_amax(bf16x2_amax(a[2 * b].x, a[2 * b].y), bf16x2_amax(a[2 * b].z, a[2 * b].w)),
+                                      bf16x2_amax(bf16x2_amax(a[2 * b + 1].x, a[2 * b + 1].y),
+                                                  bf16x2_amax(a[2 * b + 1].z, a[2 * b + 1].w))));
+    if (fbits(am[0]) >= 0x7F800000u || fbits(am[1]) >= 0x7F800000u) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a[q].x = sanitize_bf16x2(a[q].x); a[q].y = sanitize_bf16x2(a[q].y);
+        a[q].z = sanitize_bf16x2(a[q].z); a[q].w = sanitize_bf16x2(a[q].w);
+      }
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        am[b] = bf16x2_hmax(bf16x2_amax(bf16x2_amax(bf16x2_amax(a[2 * b].x, a[2 * b].y), bf16x2_amax(a[2 * b].z, a[2 * b].w)),
+                                        bf16x2_amax(bf16x2_amax(a[2 * b + 1].x, a[2 * b + 1].y),
+                                                    bf16x2_amax(a[2 * b + 1].z, a[2 * b + 1].w))));
+    }
+    }
+
+    // 2-D outer scales of the tile's ob x ob sub-blocks
+    if (BO == BO_T2D) {
+      uint32_t v = umax(fbits(am[0]), fbits(am[1]));
+      uint32_t v0 = fbits(am[0]), v1 = fbits(am[1]);
+      if (ob >= 32) v0 = v1 = v;
+      if (ob == 64) { v0 = umax(v0, __shfl_xor_sync(0xFFFFFFFFu, v0, 1)); v1 = v0; }
+      // rows of this warp: lanes 2 apart
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) {
+        v0 = umax(v0, __shfl_xor_sync(0xFFFFFFFFu, v0, o));
+        v1 = umax(v1, __shfl_xor_sync(0xFFFFFFFFu, v1, o));
+      }
+      const int nbk = 64 >> lob;
+      if (lane < 2) {
+        // sub-block column of this thread's blocks: (32 rh + 16 b) >> lob
+        const int sb0 = (32 * rh) >> lob, sb1 = (32 * rh + 16) >> lob;
+        const int srow = (16 * warp) >> lob;
+        if (ob == 16) {
+          red2d[srow * nbk + sb0] = v0;
+          red2d[srow * nbk + sb1] = v1;
+        } else {
+          atomicMax(&red2d[srow * nbk + sb0], v0);
+          if (sb1 != sb0) atomicMax(&red2d[srow * nbk + sb1], v1);
+        }
+      }
+      __syncthreads();
+      const int nsub = (BM >> lob) * nbk;
+      if (t < nsub) {
+        const float A = bitsf(red2d[t]);
+        red2d[t] = 0u;
+        const float S = outer_scale<UE5M3>(A);
+        sr2d[t] = make_float2(S, ieee_rcp(S));
+        const int64_t mi = p.m0 + (int64_t)(t / nbk) * ob, kj = p.k0 + (int64_t)(t % nbk) * ob;
+        if (j.tile_outer && mi < gend && kj < K) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = S;
+      }
+      __syncthreads();
+    }
+
+    if (j.do_row) {
+      float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
+      if (BO == BO_UNIFORM) {
+        S[0] = S[1] = S_u;
+        R[0] = R[1] = r_u;
+      } else if (BO == BO_T1D) {
+        uint32_t g0 = fbits(am[0]), g1 = fbits(am[1]);
+        if (ob >= 32) g0 = g1 = umax(g0, g1);
+        if (ob == 64) { g0 = umax(g0, __shfl_xor_sync(0xFFFFFFFFu, g0, 1)); g1 = g0; }
+        S[0] = outer_scale<UE5M3>(bitsf(g0));
+        R[0] = ieee_rcp(S[0]);
+        if (ob == 16) {
+          S[1] = outer_scale<UE5M3>(bitsf(g1));
+          R[1] = ieee_rcp(S[1]);
+        } else {
+          S[1] = S[0];
+          R[1] = R[0];
+        }
+        if (j.row_outer && rvalid) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int64_t e = rel + 16 * b;
+            if (p.k0 + 32 * rh + 16 * b < K && (e & (ob - 1)) == 0) j.row_outer[e >> lob] = S[b];
+          }
+        }
+      } else if (BO == BO_T2D) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const float2 sr = sr2d[((16 * warp + (lane >> 1)) >> lob) * (64 >> lob) + ((32 * rh + 16 * b) >> lob)];
+          S[b] = sr.x;
+          R[b] = sr.y;
+        }
+      } else if (BO == BO_B1D || BO == BO_B2D) {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const int64_t kb = p.k0 + 32 * rh + 16 * b;
+          if (rvalid && kb < K) {
+            if (BO == BO_B1D) S[b] = j.row_outer[ob_pow2 ? ((rel + 16 * b) >> lob) : (rel + 16 * b) / ob];
+            else S[b] = j.tile_outer[(p.g * mob + m / ob) * kob + kb / ob];
+          }
+          R[b] = ieee_rcp(S[b]);
+        }
+      }
+      uint32_t cw[4], scw = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        float u[16];  // u, or -u with an outer scale
+        const uint32_t wd[8] = {a[2 * b].x, a[2 * b].y, a[2 * b].z, a[2 * b].w,
+                                a[2 * b + 1].x, a[2 * b + 1].y, a[2 * b + 1].z, a[2 * b + 1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          u[2 * i] = BO == BO_NONE ? bf16lo(wd[i]) : nbf16lo(wd[i]);
+          u[2 * i + 1] = BO == BO_NONE ? bf16hi(wd[i]) : nbf16hi(wd[i]);
+        }
+        const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, am[b], S[b], R[b], none, j, 0u,
+                                                                  (uint64_t)(rel + 16 * b), cw[2 * b], cw[2 * b + 1]);
+        scw |= sc << (8 * b);
+      }
+      if (rvalid) {
+        const int nb = (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
+        // scale byte offset: linear rel / 16; tensor-core tiles: the tile of
+        // (m0 / 128, k0 / 64), row rr of it, columns 2 rh and 2 rh + 1
+        const int64_t so = j.rsl.mma ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
+                                           ((rr & 31) << 4) + ((rr >> 5) << 2) + 2 * rh
+                                     : rel / 16;
+        if (nb == 2 && row_wide) {
+          *reinterpret_cast<uint4*>(j.row_codes + rel / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          *reinterpret_cast<uint16_t*>(j.row_scales + so) = (uint16_t)scw;
+        } else {
+          if (nb >= 1) {
+            *reinterpret_cast<uint2*>(j.row_codes + rel / 2) = make_uint2(cw[0], cw[1]);
+            j.row_scales[so] = (uint8_t)scw;
+          }
+          if (nb >= 2) {
+            *reinterpret_cast<uint2*>(j.row_codes + rel / 2 + 8) = make_uint2(cw[2], cw[3]);
+            j.row_scales[so + 1] = (uint8_t)(scw >> 8);
+          }
+        }
+      }
+    }
+
+    // --------------------------------------------------------- columnwise
+    if (!j.do_col) {  // rowwise-only call (tensor-core scale layout)
+      __syncthreads();
+      continue;
+    }
+    uint32_t wv[16];
+    {
+      const unsigned char* rb = raw + warp * 16 * 128 + cbyte;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(rb + i * 128 + ((cunit ^ (i & 7)) << 4));
+    }
+    uint32_t mx = bf16x2_amax(wv[0], wv[1]);
+#pragma unroll
+    for (int i = 2; i < 16; i += 2) mx = bf16x2_amax(mx, bf16x2_amax(wv[i], wv[i + 1]));
+    mx &= 0x7FFF7FFFu;
+    if ((mx & 0xFFFFu) >= 0x7F80u || (mx >> 16) >= 0x7F80u) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) wv[i] = sanitize_bf16x2(wv[i]);
+      mx = bf16x2_amax(wv[0], wv[1]);
+#pragma unroll
+      for (int i = 2; i < 16; i += 2) mx = bf16x2_amax(mx, bf16x2_amax(wv[i], wv[i + 1]));
+      mx &= 0x7FFF7FFFu;
+    }
+    const float cam[2] = {bitsf(mx << 16), bitsf(mx & 0xFFFF0000u)};
+    const int64_t mb = p.m0 + 16 * warp;  // first row of this lane's blocks
+    const bool mvalid = mb < gend;
+    float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
+    if (BO == BO_UNIFORM) {
+      S[0] = S[1] = S_u;
+      R[0] = R[1] = r_u;
+    } else if (BO == BO_T1D) {
+      uint32_t g[2] = {fbits(cam[0]), fbits(cam[1])};
+      if (ob > 16) {  // the outer block spans ob / 16 warps
+        const int grp = (16 * warp) >> lob;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) atomicMax(&redc[(2 * lane + c) * 4 + grp], g[c]);
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) g[c] = redc[(2 * lane + c) * 4 + grp];
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        S[c] = outer_scale<UE5M3>(bitsf(g[c]));
+        R[c] = ieee_rcp(S[c]);
+        const int64_t k = p.k0 + 2 * lane + c;
+        if (j.col_outer && k < K && mvalid && ((16 * warp) & (ob - 1)) == 0)
+          j.col_outer[(cbase + k * cstride + mb) >> lob] = S[c];
+      }
+    } else if (BO == BO_T2D) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float2 sr = sr2d[((16 * warp) >> lob) * (64 >> lob) + ((2 * lane + c) >> lob)];
+        S[c] = sr.x;
+        R[c] = sr.y;
+      }
+    } else if (BO == BO_B1D || BO == BO_B2D) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int64_t k = p.k0 + 2 * lane + c;
+        if (k < K && mvalid) {
+          if (BO == BO_B1D) S[c] = j.col_outer[ob_pow2 ? ((cbase + k * cstride + mb) >> lob) : (cbase + k * cstride + mb) / ob];
+          else S[c] = j.tile_outer[(p.g * mob + (ob_pow2 ? (mb >> lob) : mb / ob)) * kob + (ob_pow2 ? (k >> lob) : k / ob)];
+        }
+        R[c] = ieee_rcp(S[c]);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float u[16];  // u, or -u with an outer scale
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        u[i] = BO == BO_NONE ? (c ? bf16hi(wv[i]) : bf16lo(wv[i])) : (c ? nbf16hi(wv[i]) : nbf16lo(wv[i]));
+      const int64_t k = p.k0 + 2 * lane + c;
+      uint32_t w0, w1;
+      const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, cam[c], S[c], R[c], none, j, 1u,
+                                                                (uint64_t)(cbase + k * cstride + mb), w0, w1);
+      *reinterpret_cast<uint2*>(cst + (2 * lane + c) * CST + 8 * warp) = make_uint2(w0, w1);
+      sst[(2 * lane + c) * 8 + warp] = (uint8_t)sc;
+    }
+    __syncthreads();
+    if (BO == BO_T1D && ob > 16 && ((16 * warp) & (ob - 1)) == 0) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) redc[(2 * lane + c) * 4 + ((16 * warp) >> lob)] = 0u;
+    }
+    // copy-out: thread t stores rows 32 (t mod 4) .. + 31 of column t / 4
+    {
+      const int col = t >> 2, ch = t & 3;
+      const int64_t k = p.k0 + col;
+      const int64_t m1 = p.m0 + 32 * ch;
+      if (k < K && m1 < gend) {
+        const int nb = (int)min((int64_t)2, (gend - m1) / 16);
+        const uint2 c0 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch);
+        const uint2 c1 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch + 8);
+        uint8_t* d = j.col_codes + (cbase + k * cstride + m1) / 2;
+        if (nb == 2 && (reinterpret_cast<uintptr_t>(d) & 15u) == 0) {
+          *reinterpret_cast<uint4*>(d) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+        } else {
+          *reinterpret_cast<uint2*>(d) = c0;
+          if (nb == 2) *reinterpret_cast<uint2*>(d + 8) = c1;
+        }
+      }
+      if (t < 64) {
+        const int64_t kk = p.k0 + t;
+        if (kk < K) {
+          const int nbm = (int)min((int64_t)8, (gend - p.m0) / 16);
+          const uint2 v = *reinterpret_cast<const uint2*>(sst + t * 8);
+          if (j.csl.mma) {
+            // scale columns m0 / 16 + 4 h .. + 3 of row kk: 4 bytes of tile
+            // (kk / 128, m0 / 64 + h)
+            uint8_t* d = j.col_scales + ((p.g * j.csl.nrb + (kk >> 7)) * j.csl.ncb + (p.m0 >> 6)) * 512 +
+                         ((kk & 31) << 4) + (((kk >> 5) & 3) << 2);
+            if (nbm == 8) {
+              *reinterpret_cast<uint32_t*>(d) = v.x;
+              *reinterpret_cast<uint32_t*>(d + 512) = v.y;
+            } else {
+              for (int q = 0; q < nbm; ++q) d[(q >> 2) * 512 + (q & 3)] = (uint8_t)((q < 4 ? v.x : v.y) >> (8 * (q & 3)));
+            }
+          } else {
+            uint8_t* d = j.col_scales + (cbase + kk * cstride + p.m0) / 16;
+            if (nbm == 8 && (reinterpret_cast<uintptr_t>(d) & 7u) == 0) {
+              *reinterpret_cast<uint2*>(d) = v;
+            } else {
+              for (int q = 0; q < nbm; ++q) d[q] = (uint8_t)((q < 4 ? v.x : v.y) >> (8 * (q & 3)));
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+bool make_bf16_map(const QuantJob& j, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)j.K, (cuuint64_t)j.M, (cuuint64_t)j.G};
+  const cuuint64_t strides[2] = {(cuuint64_t)j.ld * 2, (cuuint64_t)j.M * (cuuint64_t)j.ld * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(j.x), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SR, bool UE5M3, int BO, bool GR>
+cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
+  auto kern = ctb_kernel<SR, UE5M3, BO, GR>;
+  static int per_sm_cache[128] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128) dev = 0;
+  int& per_sm = per_sm_cache[dev];
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BL::total);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, BT, BL::total);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+  }
+  // grouped: the tile count lives on the device; an upper bound is
+  // ceil(M / 128) + groups 128-row tiles per 64-column strip
+  const int64_t tiles = j.ngroups > 0 ? ((j.M + BM - 1) / BM + j.ngroups) * ((j.K + BK - 1) / BK)
+                                      : j.G * ((j.M + BM - 1) / BM) * ((j.K + BK - 1) / BK);
+  const int64_t cap = (int64_t)num_sms() * per_sm;
+  kern<<<(int)(tiles < cap ? tiles : cap), BT, BL::total, st>>>(j, map);
+  return cudaGetLastError();
+}
+
+template <bool SR, bool UE5M3, bool GR>
+cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
+  if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR>(j, map, st);
+  if (j.s_src == S_TENSORWISE_WS || j.mode == 1) return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR>(j, map, st);
+  if (j.s_src == S_IN_TILE)
+    return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR>(j, map, st) : launch_ctb_t<SR, UE5M3, BO_T1D, GR>(j, map, st);
+  return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_B2D, GR>(j, map, st) : launch_ctb_t<SR, UE5M3, BO_B1D, GR>(j, map, st);
+}
+
+// All variants of one grouping mode: false if the tensor map cannot be built.
+template <bool GR>
+bool launch_ctb_all(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
+  CUtensorMap map;
+  if (!make_bf16_map(j, &map)) return false;
+  if (j.sr) *err = j.ue5m3 ? launch_ctb_o<true, true, GR>(j, map, st) : launch_ctb_o<true, false, GR>(j, map, st);
+  else *err = j.ue5m3 ? launch_ctb_o<false, true, GR>(j, map, st) : launch_ctb_o<false, false, GR>(j, map, st);
+  return true;
+}
+
+}  // namespace
+}  // namespace fp4q

@@ -1,0 +1,12 @@
+// k_ctb_grouped.cu -- the bf16 cast-transpose kernel over ragged groups of
+// rows (fp4_quantize_grouped): each group's 128-row tiles, its own
+// columnwise transpose and tensorwise scale.  Kernel body: k_ctb.cuh.
+#include "k_ctb.cuh"
+
+namespace fp4q {
+
+bool launch_ctb_grouped(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
+  return launch_ctb_all<true>(j, st, err);
+}
+
+}  // namespace fp4q

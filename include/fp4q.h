@@ -188,6 +188,37 @@ int fp4q_query_sizes(const fp4q_params_t *p, fp4q_sizes_t *sizes);
 int fp4_quantize(const fp4q_params_t *p, const void *x, const fp4q_outputs_t *out, float *residual,
                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* Ragged grouped quantize (mixture-of-experts token groups): x is [M, K]
+ * (p->G must be 1) and rows [offsets[e], offsets[e + 1]) form group e,
+ * e < ngroups; each group is quantized as a matrix of its own ("NVFP4 /
+ * AMD-FP4 outer-block (two-level) scaling for FP4 training", "Technical
+ * design": per-operand scales; the MoE expert weights and tokens it targets).
+ *   offsets: DEVICE int64 [ngroups + 1], 0 = offsets[0] <= ... <=
+ *     offsets[ngroups] = M, every group a multiple of 16 rows with the
+ *     columnwise mask, of ob rows with 2-D outer blocks or columnwise 1-D
+ *     outer blocks.  They are read on the device (no host synchronization);
+ *     if they break a rule, nothing is written and the first 32-bit word of
+ *     the workspace is nonzero after the call.
+ *   Outputs: rowwise buffers, row_outer and 2-D tile_outer exactly as for
+ *     the whole [M, K] tensor (group boundaries fall on block boundaries).
+ *     Group e's columnwise codes are its own [K, m_e / 2] transpose at byte
+ *     K * offsets[e] / 2 of col_codes (scales [K, m_e / 16] at
+ *     K * offsets[e] / 16; 1-D col_outer [K, m_e / ob] at K * offsets[e] / ob
+ *     floats).  Tensorwise mode: one scale per group, tile_outer [ngroups].
+ *   Stochastic rounding draws from each code's flat index in its output
+ *   buffer (rowwise [M, K], columnwise the concatenated group transposes).
+ *   workspace: >= sizes.workspace bytes from fp4q_query_sizes_grouped,
+ *     16-byte aligned.
+ *   bf16 input, 1 x 16 inner blocks, linear scale layout; FP4Q_ERR_UNSUPPORTED
+ *   otherwise, and for columnwise 1-D outer blocks other than 16, 32, 64
+ *   without precomputed scales. */
+int fp4_quantize_grouped(const fp4q_params_t *p, const void *x, const int64_t *offsets, int64_t ngroups,
+                         const fp4q_outputs_t *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Buffer sizes of fp4_quantize_grouped (FP4Q_ERR_SHAPE unless p->G == 1 and
+ * 1 <= ngroups <= 65535). */
+int fp4q_query_sizes_grouped(const fp4q_params_t *p, int64_t ngroups, fp4q_sizes_t *sizes);
+
 /* Dequantize one orientation's buffers to y ([G, R, C] contiguous, R x C =
  * M x K for orient FP4Q_OUT_ROW, K x M for FP4Q_OUT_COL) in p->out_dtype:
  *   y = OUT((e2m1(q) * s) * S)   (binary32 products, RNE to bf16 or exact fp32)
