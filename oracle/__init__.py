@@ -104,6 +104,12 @@ def _lib():
         L.orc_qdq.argtypes = [ctypes.POINTER(Cfg), ctypes.c_int, P, P, P, P, P, P]
         L.orc_mxfp4_fake_quantize.restype = ctypes.c_int
         L.orc_mxfp4_fake_quantize.argtypes = [ctypes.POINTER(Cfg), P, P]
+        L.orc_mxfp8_exponent.restype = ctypes.c_int
+        L.orc_mxfp8_exponent.argtypes = [ctypes.c_double]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_encode.argtypes = [ctypes.c_double]
+        L.orc_mxfp4_project_mxfp8.restype = ctypes.c_int
+        L.orc_mxfp4_project_mxfp8.argtypes = [ctypes.POINTER(Cfg), P, P, P, P, P, P]
         L.orc_subnormals_ok.restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -243,6 +249,37 @@ def mxfp4_fake_quantize(x, K=None, *, out_dtype=None):
     rc = _lib().orc_mxfp4_fake_quantize(ctypes.byref(cfg), _ptr(x), _ptr(y))
     assert rc == 0
     return y
+
+
+def mxfp4_project_mxfp8(x, K=None, *, out_dtype=None, out_mask=ROW | COL, with_y=True):
+    """MXFP4 projection and its MXFP8 encodings (OCP MX reading, see the C
+    source): returns dict y [G,M,K] (or None), row_codes [G,M,K] u8 (E4M3),
+    row_scales [G,M,K/32] u8 (UE8M0), col_codes [G,K,M], col_scales
+    [G,K,M/32] for the orientations in out_mask."""
+    x = _as3d(x)
+    cfg = make_cfg(x, K, out_dtype=out_dtype)
+    G, M, Kk = cfg.G, cfg.M, cfg.K
+    out = {"y": np.zeros((G, M, Kk), _out_np(cfg.out_dtype)) if with_y else None,
+           "row_codes": None, "row_scales": None, "col_codes": None, "col_scales": None}
+    if out_mask & ROW:
+        out["row_codes"] = np.zeros((G, M, Kk), np.uint8)
+        out["row_scales"] = np.zeros((G, M, Kk // 32), np.uint8)
+    if out_mask & COL:
+        assert M % 32 == 0
+        out["col_codes"] = np.zeros((G, Kk, M), np.uint8)
+        out["col_scales"] = np.zeros((G, Kk, M // 32), np.uint8)
+    rc = _lib().orc_mxfp4_project_mxfp8(ctypes.byref(cfg), _ptr(x), _ptr(out["y"]), _ptr(out["row_codes"]),
+                                       _ptr(out["row_scales"]), _ptr(out["col_codes"]), _ptr(out["col_scales"]))
+    assert rc == 0
+    return out
+
+
+def mxfp8_exponent(A: float) -> int:
+    return _lib().orc_mxfp8_exponent(float(A))
+
+
+def e4m3_encode(v: float) -> int:
+    return _lib().orc_e4m3_encode(float(v))
 
 
 # ---- scalar helpers (for pins) ------------------------------------------

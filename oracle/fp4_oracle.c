@@ -508,6 +508,103 @@ int orc_mxfp4_fake_quantize(const orc_cfg *cf, const void *x, void *y) {
   return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* MXFP4 projection re-encoded as MXFP8 ([TEQAT] "Design": the projected    */
+/* weight goes to the host's MXFP8 quantizer, losslessly rowwise and with   */
+/* bounded re-quantization columnwise (32 x 1 blocks); "Known limitations":  */
+/* a fused projection + quantize kernel is future work).                     */
+/*                                                                            */
+/* Reading -- the pages do not define MXFP8, so this follows the OCP         */
+/* Microscaling (MX) format specification v1.0: per block of 32 values a    */
+/* shared scale 2^X, X = floor(log2(max |v|)) - 8 (8 = the largest exponent  */
+/* of an E4M3 element), clamped to the UE8M0 range [-127, 127] and stored as */
+/* the byte X + 127; each element is E4M3(v / 2^X), round to nearest even,   */
+/* saturating at 448, sign kept (so -0 is 0x80).  A block of zeros takes     */
+/* X = -127.  A block holding a NaN -- a poisoned MXFP4 block -- is all NaN: */
+/* scale byte 0xFF and element bytes 0x7F.                                   */
+/* ------------------------------------------------------------------------ */
+
+int orc_mxfp8_exponent(double A) {
+  if (A == 0.0) return -127;
+  int e;
+  frexp(A, &e);          /* A = f 2^e, 1/2 <= f < 1: floor(log2 A) = e - 1 */
+  int X = (e - 1) - 8;
+  if (X < -127) X = -127;
+  if (X > 127) X = 127;
+  return X;
+}
+
+uint8_t orc_e4m3_encode(double v) {
+  uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  return (uint8_t)(sign | orc_scale_encode(ORC_FMT_E4M3, (float)fabs(v)));
+}
+
+/* One MXFP8 block of 32 values v[0], v[s], ..., v[31 s]. */
+static void mxfp8_block(const double *v, int64_t s, uint8_t *codes, int64_t cs, uint8_t *scale) {
+  double A = 0.0;
+  int nan = 0;
+  for (int i = 0; i < 32; i++) {
+    if (isnan(v[i * s])) nan = 1;
+    else if (fabs(v[i * s]) > A) A = fabs(v[i * s]);
+  }
+  if (nan) {
+    *scale = 0xFF;
+    for (int i = 0; i < 32; i++) codes[i * cs] = 0x7F;
+    return;
+  }
+  int X = orc_mxfp8_exponent(A);
+  *scale = (uint8_t)(X + 127);
+  for (int i = 0; i < 32; i++) codes[i * cs] = orc_e4m3_encode(ldexp(v[i * s], -X));
+}
+
+/* y (optional): the MXFP4 projection, as orc_mxfp4_fake_quantize.  Rowwise
+ * MXFP8 (1 x 32 blocks along K): codes [G, M, K], scales [G, M, K/32].
+ * Columnwise (32 x 1 blocks along M, x transposed): codes [G, K, M], scales
+ * [G, K, M/32]; needs M % 32 == 0. */
+int orc_mxfp4_project_mxfp8(const orc_cfg *cf, const void *x, void *y, uint8_t *row_codes, uint8_t *row_scales,
+                            uint8_t *col_codes, uint8_t *col_scales) {
+  int64_t G = cf->G, M = cf->M, K = cf->K;
+  double *P = (double *)malloc(sizeof(double) * (size_t)(G * M * K));
+  if (!P) return -1;
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t i = 0; i < M; i++)
+      for (int64_t j0 = 0; j0 < K; j0 += 32) {
+        double A = 0.0;
+        int poisoned = 0;
+        for (int64_t j = j0; j < j0 + 32; j++) {
+          double v = (double)load_in(x, cf->in_dtype, (g * M + i) * cf->ld + j);
+          if (!isfinite(v)) poisoned = 1;
+          else if (fabs(v) > A) A = fabs(v);
+        }
+        int E = orc_mxfp4_exponent(A);
+        for (int64_t j = j0; j < j0 + 32; j++) {
+          int64_t n = (g * M + i) * K + j;
+          double v = (double)load_in(x, cf->in_dtype, (g * M + i) * cf->ld + j);
+          P[n] = poisoned ? NAN : ldexp(orc_e2m1_decode(orc_e2m1_rne(ldexp(v, -E))), E);
+          if (y) {
+            if (poisoned) {
+              if (cf->out_dtype == ORC_BF16) ((uint16_t *)y)[n] = 0x7FC0;
+              else ((uint32_t *)y)[n] = 0x7FC00000u;
+            } else {
+              store_out(y, cf->out_dtype, n, (float)P[n]);
+            }
+          }
+        }
+      }
+  if (row_codes)
+    for (int64_t r = 0; r < G * M; r++)
+      for (int64_t j0 = 0; j0 < K; j0 += 32)
+        mxfp8_block(P + r * K + j0, 1, row_codes + r * K + j0, 1, row_scales + r * (K / 32) + j0 / 32);
+  if (col_codes)
+    for (int64_t g = 0; g < G; g++)
+      for (int64_t j = 0; j < K; j++)
+        for (int64_t i0 = 0; i0 < M; i0 += 32)
+          mxfp8_block(P + (g * M + i0) * K + j, K, col_codes + (g * K + j) * M + i0, 1,
+                      col_scales + (g * K + j) * (M / 32) + i0 / 32);
+  free(P);
+  return 0;
+}
+
 /* Startup check used by the tests: subnormals survive a multiply (no
  * flush-to-zero in this process). */
 int orc_subnormals_ok(void) {

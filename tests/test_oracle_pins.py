@@ -612,3 +612,92 @@ def test_mxfp4_fp32_input_bruteforce(orc):
             want = _mx_reference_block_f32(x[r, 32 * b:32 * b + 32])
             got = y[r, 32 * b:32 * b + 32]
             np.testing.assert_array_equal(got.view(np.uint32), np.array(want, np.float32).view(np.uint32))
+
+
+# ----------------------------------------------------------------------------
+# MXFP4 projection re-encoded as MXFP8 ([TEQAT] "Design"; MXFP8 per the OCP
+# MX v1.0 reading stated in the oracle)
+# ----------------------------------------------------------------------------
+
+def _e4m3_decode_torch(codes: np.ndarray) -> np.ndarray:
+    """E4M3 bytes -> float64 with torch's float8_e4m3fn (an independent decoder)."""
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _mxfp8_decode(codes, scales, axis_len):
+    v = _e4m3_decode_torch(codes)
+    X = scales.astype(np.int64) - 127
+    return v * np.exp2(np.repeat(X, 32, axis=-1)).reshape(v.shape)
+
+
+def _wide_range_bf16(shape, seed):
+    g = torch.Generator("cpu").manual_seed(seed)
+    x = torch.randn(*shape, generator=g) * torch.exp2(torch.randint(-120, 120, (shape[0], 1), generator=g).float())
+    return x.to(torch.bfloat16)
+
+
+def test_mxfp8_rowwise_encoding_of_the_projection_is_lossless(orc):
+    """[TEQAT] "Design": the MXFP8 rowwise encoding of the projected weight is
+    bitwise lossless -- decoding codes and scales gives the projection back
+    exactly (all bf16 patterns and a wide-range tensor; poisoned blocks aside)."""
+    for x in (W.all_bf16_patterns(), _wide_range_bf16((64, 256), 21)):
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        out = orc.mxfp4_project_mxfp8(xb, out_dtype="fp32", out_mask=1)
+        y = orc.mxfp4_fake_quantize(xb, out_dtype="fp32")[0]     # the separately pinned projection
+        assert (out["y"][0].view(np.uint32) == y.view(np.uint32)).all()
+        dec = _mxfp8_decode(out["row_codes"][0], out["row_scales"][0], 32)
+        ok = np.isfinite(y)
+        assert (dec[ok] == y[ok].astype(np.float64)).all()
+        blocks = ~np.isfinite(y).reshape(y.shape[0], -1, 32).all(axis=2)
+        assert (out["row_scales"][0][blocks] == 0xFF).all()
+        assert (out["row_codes"][0].reshape(y.shape[0], -1, 32)[blocks] == 0x7F).all()
+
+
+def test_mxfp8_exponent_rule(orc):
+    """X = floor(log2 A) - 8, clamped to [-127, 127]; A = 0 gives -127."""
+    rng = np.random.default_rng(5)
+    vals = list(np.exp2(rng.uniform(-140, 130, 2000))) + [2.0 ** k for k in range(-140, 128)] + \
+        [2.0 ** k * (2 - 2 ** -20) for k in range(-130, 127)]
+    for A in vals:
+        X = orc.mxfp8_exponent(float(A))
+        f = Fraction(A)  # exact floor(log2 A) from the rational value
+        fl = f.numerator.bit_length() - f.denominator.bit_length()
+        if Fraction(2) ** fl > f:
+            fl -= 1
+        assert X == min(max(fl - 8, -127), 127), (A, X, fl)
+    assert orc.mxfp8_exponent(0.0) == -127
+
+
+def test_mxfp8_columnwise_elements_match_torch_float8(orc):
+    """Columnwise blocks mix rows with different MXFP4 exponents: the element
+    bytes are torch's float8_e4m3fn rounding of v / 2^X (never above 448 for
+    projected values), and the re-quantization error is within half an E4M3
+    step."""
+    x = _wide_range_bf16((64, 128), 22)
+    x[5, 7] = float("nan")
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    out = orc.mxfp4_project_mxfp8(xb, out_dtype="fp32", out_mask=2)
+    y = out["y"][0].astype(np.float64)                     # [M, K]
+    codes, scales = out["col_codes"][0], out["col_scales"][0]  # [K, M], [K, M/32]
+    for k in range(128):
+        for b in range(2):
+            v = y[32 * b:32 * b + 32, k]
+            if not np.isfinite(v).all():
+                assert scales[k, b] == 0xFF and (codes[k, 32 * b:32 * b + 32] == 0x7F).all()
+                continue
+            X = int(scales[k, b]) - 127
+            t = v * 2.0 ** -X
+            assert np.abs(t).max() <= 448
+            ref = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert (codes[k, 32 * b:32 * b + 32] == ref).all(), (k, b)
+            dec = _e4m3_decode_torch(codes[k, 32 * b:32 * b + 32]) * 2.0 ** X
+            assert (np.abs(dec - v) <= np.maximum(np.abs(v) * 2.0 ** -4, 2.0 ** (X - 10))).all()
+
+
+def test_mxfp8_zero_and_signed_zero_blocks(orc):
+    x = np.zeros((32, 64), np.uint16)
+    x[:, 32:] = 0x8000                                       # -0 in the second block
+    out = orc.mxfp4_project_mxfp8(x, out_dtype="bf16")
+    assert (out["row_scales"][0] == 0).all()                # X = -127 for all-zero blocks
+    assert (out["row_codes"][0][:, :32] == 0x00).all() and (out["row_codes"][0][:, 32:] == 0x80).all()
+    assert (out["col_codes"][0][:32] == 0x00).all() and (out["col_codes"][0][32:] == 0x80).all()
