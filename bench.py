@@ -252,6 +252,16 @@ def _extra_workloads():
             return "%d x bf16[5760,2880] 2-D 64x64 outer %s rowwise+columnwise" % (G, fmt), nb, ms, 1
         return run
 
+    def mxfp4_project_mxfp8(iters, warmup, opts):
+        # the headline weight: projection + MXFP8 rowwise and columnwise in one pass
+        xh, _ = W.mxfp4_weight()
+        xs = [xh.to(dev) for _ in range(2)]
+        outs = [fq.mxfp4_project_mxfp8(xx) for xx in xs]
+        ms = _events_time(lambda i: fq.mxfp4_project_mxfp8(xs[i & 1], out=outs[i & 1]), iters, warmup)
+        n = xh.numel()
+        return ("bf16[8192,8192] -> MXFP4 projection -> MXFP8 rowwise + columnwise (E4M3 + UE8M0)",
+                2 * n + 2 * n + 2 * (n // 32), ms, 1)
+
     def moe_grouped_tokens(iters, warmup, opts):
         # 65536 tokens routed to 32 experts with lognormal popularity (seed 0),
         # each expert's count rounded down to a multiple of 64 (the outer block)
@@ -299,6 +309,7 @@ def _extra_workloads():
         "moe_experts_e4m3": (_moe("e4m3"), 20, 3),
         "moe_experts_ue5m3": (_moe("ue5m3"), 20, 3),
         "moe_grouped_tokens": (moe_grouped_tokens, 30, 3),
+        "mxfp4_project_mxfp8": (mxfp4_project_mxfp8, 50, 5),
         "sr_ef_weight_qdq": (sr_ef_weight_qdq, 20, 3),
     }
 

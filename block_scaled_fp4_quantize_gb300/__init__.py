@@ -23,7 +23,7 @@ import torch
 from . import _capi
 from ._capi import FP4QError
 
-__all__ = ["QuantizedFP4", "quantize", "quantize_grouped", "dequantize", "qdq", "mxfp4_fake_quantize", "mxfp4_fake_quantize_host",
+__all__ = ["QuantizedFP4", "MXFP8Pair", "quantize", "quantize_grouped", "dequantize", "mxfp4_project_mxfp8", "qdq", "mxfp4_fake_quantize", "mxfp4_fake_quantize_host",
            "tensor_amax", "build", "FP4QError", "query_sizes", "host_workspace_bytes"]
 
 _MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
@@ -300,6 +300,41 @@ def mxfp4_fake_quantize(x: torch.Tensor, out_dtype: Optional[torch.dtype] = None
     st = _lib().mxfp4_fake_quantize(ctypes.byref(p), _ptr(x3), _ptr(y), _stream(x.device))
     _capi.check(st, "mxfp4_fake_quantize")
     return y if (x.dim() == 3 or out is not None) else y[0]
+
+
+@dataclass
+class MXFP8Pair:
+    """Outputs of mxfp4_project_mxfp8; absent parts are None."""
+    y: Optional[torch.Tensor] = None           # the MXFP4 projection [G, M, K]
+    row_codes: Optional[torch.Tensor] = None   # E4M3 bytes [G, M, K]
+    row_scales: Optional[torch.Tensor] = None  # UE8M0 bytes [G, M, K/32]
+    col_codes: Optional[torch.Tensor] = None   # E4M3 bytes [G, K, M]
+    col_scales: Optional[torch.Tensor] = None  # UE8M0 bytes [G, K, M/32]
+
+
+def mxfp4_project_mxfp8(x: torch.Tensor, *, rowwise: bool = True, columnwise: bool = True, with_y: bool = False,
+                        out_dtype: Optional[torch.dtype] = None, out: Optional[MXFP8Pair] = None) -> MXFP8Pair:
+    """Fused MXFP4 projection of x and its MXFP8 encodings (rowwise 1 x 32,
+    columnwise 32 x 1), reading x once; ``with_y`` also returns the
+    projection itself.  See include/fp4q.h for the MXFP8 rule."""
+    x3, G, M, K, ld = _view3d(x)
+    out_dtype = out_dtype or x.dtype
+    mask = (_capi.OUT_ROW if rowwise else 0) | (_capi.OUT_COL if columnwise else 0)
+    p = _params(G, M, K, ld, x.dtype, out_dtype, out_mask=mask)
+    dev = x.device
+    if out is None:
+        u8 = dict(dtype=torch.uint8, device=dev)
+        out = MXFP8Pair()
+        if with_y:
+            out.y = torch.empty(G, M, K, dtype=out_dtype, device=dev)
+        if rowwise:
+            out.row_codes, out.row_scales = torch.empty(G, M, K, **u8), torch.empty(G, M, K // 32, **u8)
+        if columnwise:
+            out.col_codes, out.col_scales = torch.empty(G, K, M, **u8), torch.empty(G, K, M // 32, **u8)
+    st = _lib().mxfp4_project_mxfp8(ctypes.byref(p), _ptr(x3), _ptr(out.y), _ptr(out.row_codes), _ptr(out.row_scales),
+                                    _ptr(out.col_codes), _ptr(out.col_scales), _stream(dev))
+    _capi.check(st, "mxfp4_project_mxfp8")
+    return out
 
 
 HOST_CHUNK_BYTES = 16 << 20

@@ -22,7 +22,7 @@ OUT_ROW, OUT_COL = 1, 2
 
 # every symbol include/fp4q.h declares
 EXPORTS = ("fp4q_params_init", "fp4q_query_sizes", "fp4_quantize", "fp4_dequantize", "fp4_qdq",
-           "mxfp4_fake_quantize", "mxfp4_fake_quantize_host", "fp4_tensor_amax", "fp4_quantize_grouped",
+           "mxfp4_fake_quantize", "mxfp4_fake_quantize_host", "mxfp4_project_mxfp8", "fp4_tensor_amax", "fp4_quantize_grouped",
            "fp4q_query_sizes_grouped", "fp4q_status_string",
            "fp4q_abi_version", "fp4_quantize_noalloc")
 
@@ -86,6 +86,8 @@ def load(fast_math: bool = False, path: str | None = None):
     L.mxfp4_fake_quantize.argtypes = [PP, P, P, P]
     L.mxfp4_fake_quantize_host.restype = I
     L.mxfp4_fake_quantize_host.argtypes = [PP, P, P, P, ctypes.c_size_t, P]
+    L.mxfp4_project_mxfp8.restype = I
+    L.mxfp4_project_mxfp8.argtypes = [PP, P, P, P, P, P, P, P]
     L.fp4_quantize_grouped.restype = I
     L.fp4_quantize_grouped.argtypes = [PP, P, P, ctypes.c_int64, ctypes.POINTER(Outputs), P, ctypes.c_size_t, P]
     L.fp4q_query_sizes_grouped.restype = I

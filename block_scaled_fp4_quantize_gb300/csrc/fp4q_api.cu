@@ -428,6 +428,45 @@ int fp4_tensor_amax(const fp4q_params_t* p, const void* x, const float* residual
   return launch_tensor_amax(j, reinterpret_cast<uint32_t*>(amax), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }
 
+int mxfp4_project_mxfp8(const fp4q_params_t* p, const void* x, void* y, uint8_t* row_codes, uint8_t* row_scales,
+                        uint8_t* col_codes, uint8_t* col_scales, void* stream) {
+  if (!p) return FP4Q_ERR_NULL;
+  if (p->struct_size != sizeof(fp4q_params_t)) return FP4Q_ERR_ABI;
+  int rc = check_dtype(p->in_dtype);
+  if (rc) return rc;
+  rc = check_dtype(p->out_dtype);
+  if (rc) return rc;
+  if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
+      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0)
+    return FP4Q_ERR_MODE;
+  if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
+  const uint32_t mask = p->out_mask;
+  if (mask & ~3u) return FP4Q_ERR_MODE;
+  const bool row = mask & FP4Q_OUT_ROW, col = mask & FP4Q_OUT_COL;
+  if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K || p->K % 32) return FP4Q_ERR_SHAPE;
+  if (col && p->M % 32) return FP4Q_ERR_SHAPE;
+  if (p->G == 0 || p->M == 0 || p->K == 0) return FP4Q_OK;
+  if (!x) return FP4Q_ERR_NULL;
+  if ((row && (!row_codes || !row_scales)) || (col && (!col_codes || !col_scales))) return FP4Q_ERR_NULL;
+  if (!vec_aligned(x, p->ld * esize(p->in_dtype)) || (y && !aligned(y, 16)) || (row && !aligned(row_codes, 16)) ||
+      (col && !aligned(col_codes, 16)))
+    return FP4Q_ERR_ALIGN;
+  QuantJob j{};
+  j.x = x;
+  j.ld = p->ld;
+  j.in_bf16 = p->in_dtype == FP4Q_BF16;
+  j.out_bf16 = p->out_dtype == FP4Q_BF16;
+  j.G = p->G;
+  j.M = p->M;
+  j.K = p->K;
+  j.y = y;
+  j.row_codes = row ? row_codes : nullptr;
+  j.row_scales = row ? row_scales : nullptr;
+  j.col_codes = col ? col_codes : nullptr;
+  j.col_scales = col ? col_scales : nullptr;
+  return launch_mxfp8(j, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
 const char* fp4q_status_string(int status) {
   switch (status) {
     case FP4Q_OK: return "FP4Q_OK";

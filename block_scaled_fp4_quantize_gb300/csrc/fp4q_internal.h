@@ -136,6 +136,9 @@ cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_
 cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st);
 cudaError_t launch_mxfp4(const MxJob& j, cudaStream_t st);
+// fused MXFP4 projection + MXFP8 re-encode: x, ld, G, M, K, in_bf16, out_bf16,
+// y (optional), row_codes / row_scales, col_codes / col_scales
+cudaError_t launch_mxfp8(const QuantJob& j, cudaStream_t st);
 // grouped path: offsets check + tile prefix (+ per-group amax for tensorwise)
 cudaError_t launch_group_prep(const QuantJob& j, int align, bool amax, cudaStream_t st);
 

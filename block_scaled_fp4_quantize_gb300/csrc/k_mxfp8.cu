@@ -1,0 +1,221 @@
+// k_mxfp8.cu -- fused MXFP4 projection + MXFP8 re-encode ("MXFP4 weight QAT
+// recipes on MXFP8 and FP8 block-scaling hosts", "Design": the projected
+// weight goes to the host's MXFP8 quantizer, rowwise losslessly and
+// columnwise (32 x 1) with bounded re-quantization; "Known limitations": a
+// fused projection + quantize kernel is named as future work).
+//
+// MXFP8 follows the OCP Microscaling v1.0 rule: per block of 32 values a
+// scale 2^X, X = floor(log2 amax) - 8 clamped to [-127, 127] (byte X + 127),
+// elements E4M3(v / 2^X) with RNE and saturation; a block of zeros takes
+// X = -127, a block holding a NaN (a poisoned MXFP4 block) is scale 0xFF
+// with elements 0x7F.
+//
+// One CTA of 256 threads per 128 x 64 tile of x, read once:
+//   rowwise: thread t owns the 1 x 32 block (row t / 2, columns 32 (t mod 2)
+//     ..): MXFP4 projection (exponent from the integer bits of the block
+//     maximum), the optional projected output, and the rowwise MXFP8 block.
+//     Its scale needs no search: the projected maximum is
+//     e2m1(q_max) 2^E, so X = E + floor(log2 e2m1(q_max)) - 8, and every
+//     element y / 2^X = e2m1(q) 2^(E - X) is exact in E4M3.
+//   the projected values are staged in shared memory as bf16 (exact: two
+//     significant bits, exponents within bf16's range);
+//   columnwise: thread t owns column t mod 64 of rows 32 (t / 64) .. + 31,
+//     one 32 x 1 MXFP8 block, read from the staged tile.
+#include "fp4q_device.cuh"
+#include "fp4q_internal.h"
+
+namespace fp4q {
+namespace {
+
+constexpr int XT = 256;
+constexpr int XM = 128, XK = 64;
+constexpr int YS = XK * 2 + 16;  // staged row stride in bytes (padding against bank conflicts)
+
+// MXFP4 block exponent (see k_mxfp4.cu): least E with 6 * 2^E >= max(A, 6 * 2^-126), capped at 125.
+__device__ __forceinline__ int mx_exp(uint32_t amax_bits) {
+  const uint32_t ac = amax_bits > 0x01C00000u ? amax_bits : 0x01C00000u;
+  const int k = (int)(ac >> 23) - 127;
+  const int e = (ac & 0x7FFFFFu) <= 0x400000u ? k - 2 : k - 1;
+  return e < 125 ? e : 125;
+}
+
+// Two E4M3 bytes (RNE, satfinite): `lo` in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float pow2f(int e) { return bitsf((uint32_t)(e + 127) << 23); }  // -126 <= e <= 127
+
+template <bool IN_BF16>
+__device__ __forceinline__ void load_block32(const void* x, int64_t idx, float (&v)[32], uint32_t& amax) {
+  // 32 elements from element index idx (16-byte aligned)
+  if (IN_BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + idx);
+    uint32_t m = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldcs(p + q);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * q + 2 * i] = bf16lo(ww[i]);
+        v[8 * q + 2 * i + 1] = bf16hi(ww[i]);
+        m = q == 0 && i == 0 ? ww[i] : bf16x2_amax(m, ww[i]);
+      }
+    }
+    m &= 0x7FFF7FFFu;
+    const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+    amax = (hi > lo ? hi : lo) << 16;
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx);
+    float m = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 w = __ldcs(p + q);
+      v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+      m = f32_amax(f32_amax(m, w.x), f32_amax(f32_amax(w.y, w.z), w.w));
+    }
+    amax = fbits(m) & 0x7FFFFFFFu;
+  }
+}
+
+template <bool IN_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(XT) mxfp8_kernel(const QuantJob j, int64_t tiles_m, int64_t tiles_k) {
+  __shared__ __align__(16) unsigned char ys[XM * YS];  // projected tile, bf16
+  const int t = threadIdx.x;
+  const int64_t tile = blockIdx.x;
+  const int64_t tk = tile % tiles_k, tm = (tile / tiles_k) % tiles_m, g = tile / (tiles_k * tiles_m);
+  const int64_t m0 = tm * XM, k0 = tk * XK;
+  const int64_t M = j.M, K = j.K;
+
+  // ---- rowwise: one 1 x 32 block per thread
+  {
+    const int rr = t >> 1, rh = t & 1;
+    const int64_t m = m0 + rr, k = k0 + 32 * rh;
+    if (m < M && k < K) {
+      float v[32];
+      uint32_t amax;
+      load_block32<IN_BF16>(j.x, (g * M + m) * j.ld + k, v, amax);
+      const bool poison = amax >= 0x7F800000u;
+      const int E = mx_exp(amax);
+      const float inv = pow2f(-E), sc = E >= -126 ? pow2f(E) : 0.0f;
+      uint32_t qb[16];  // E2M1 code bytes
+      uint32_t qmax = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        qb[i] = e2m1x2_rne(ieee_mul(v[2 * i], inv), ieee_mul(v[2 * i + 1], inv));
+        qmax = umax(qmax, umax(qb[i] & 7u, (qb[i] >> 4) & 7u));
+      }
+      // projected values y = e2m1(q) 2^E (exact)
+      float y[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float g0, g1;
+        e2m1x2_decode(qb[i], g0, g1);
+        y[2 * i] = ieee_mul(g0, sc);
+        y[2 * i + 1] = ieee_mul(g1, sc);
+      }
+      const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
+      if (j.y) {
+        if (OUT_BF16) {
+          uint4* d = reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(y[8 * q + 2 * i], y[8 * q + 2 * i + 1]);
+            d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* d = reinterpret_cast<float4*>(static_cast<float*>(j.y) + n);
+          const float qn = bitsf(0x7FC00000u);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d[q] = poison ? make_float4(qn, qn, qn, qn) : make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+        }
+      }
+      if (j.row_codes) {
+        // X = E + floor(log2 e2m1(qmax)) - 8 (qmax: 0 -> zeros; 1 -> 0.5; 2,3 -> 1, 1.5; 4,5 -> 2, 3; 6,7 -> 4, 6)
+        const int fl = qmax <= 1u ? -1 : (int)(qmax >> 1) - 1;
+        int X = qmax == 0u ? -127 : E + fl - 8;
+        X = X < -127 ? -127 : X;
+        const float s2 = pow2f(E - X);  // 2^(E - X) in [2^1, 2^9]
+        uint32_t cw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float g[4];
+          e2m1x2_decode(qb[2 * i], g[0], g[1]);
+          e2m1x2_decode(qb[2 * i + 1], g[2], g[3]);
+          cw[i] = e4m3x2(ieee_mul(g[0], s2), ieee_mul(g[1], s2)) | (e4m3x2(ieee_mul(g[2], s2), ieee_mul(g[3], s2)) << 16);
+          if (poison) cw[i] = 0x7F7F7F7Fu;
+        }
+        uint4* d = reinterpret_cast<uint4*>(j.row_codes + n);
+        d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        j.row_scales[n / 32] = poison ? (uint8_t)0xFF : (uint8_t)(X + 127);
+      }
+      if (j.col_codes) {  // stage the projection (bf16, exact; NaN for a poisoned block)
+        uint4* d = reinterpret_cast<uint4*>(ys + rr * YS + rh * 64);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(y[8 * q + 2 * i], y[8 * q + 2 * i + 1]);
+          d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+  if (!j.col_codes) return;
+  __syncthreads();
+
+  // ---- columnwise: one 32 x 1 block per thread (M % 32 == 0)
+  const int c = t & 63, rb = t >> 6;
+  const int64_t k = k0 + c, mb = m0 + 32 * rb;
+  if (k >= K || mb >= M) return;
+  float v[32];
+  uint32_t amax = 0, nan = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t b = *reinterpret_cast<const uint16_t*>(ys + (32 * rb + i) * YS + 2 * c);
+    v[i] = bitsf(b << 16);
+    const uint32_t a = b & 0x7FFFu;
+    nan |= a > 0x7F80u ? 1u : 0u;
+    amax = umax(amax, a);
+  }
+  // X = floor(log2 amax) - 8 from the exponent bits (subnormal / zero amax: -127)
+  const int ex = (int)(amax >> 7);
+  int X = ex == 0 ? -127 : ex - 127 - 8;
+  X = X < -127 ? -127 : X;
+  const float inv = pow2f(-X);
+  uint32_t cw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cw[i] = e4m3x2(ieee_mul(v[4 * i], inv), ieee_mul(v[4 * i + 1], inv)) |
+            (e4m3x2(ieee_mul(v[4 * i + 2], inv), ieee_mul(v[4 * i + 3], inv)) << 16);
+    if (nan) cw[i] = 0x7F7F7F7Fu;
+  }
+  const int64_t n = (g * K + k) * M + mb;  // element index in the [G, K, M] columnwise outputs
+  uint4* d = reinterpret_cast<uint4*>(j.col_codes + n);
+  d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  j.col_scales[n / 32] = nan ? (uint8_t)0xFF : (uint8_t)(X + 127);
+}
+
+template <bool IN_BF16, bool OUT_BF16>
+cudaError_t launch_t(const QuantJob& j, cudaStream_t st) {
+  const int64_t tiles_m = (j.M + XM - 1) / XM, tiles_k = (j.K + XK - 1) / XK;
+  mxfp8_kernel<IN_BF16, OUT_BF16><<<(unsigned)(j.G * tiles_m * tiles_k), XT, 0, st>>>(j, tiles_m, tiles_k);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8(const QuantJob& j, cudaStream_t st) {
+  if (j.in_bf16) return j.out_bf16 ? launch_t<true, true>(j, st) : launch_t<true, false>(j, st);
+  return j.out_bf16 ? launch_t<false, true>(j, st) : launch_t<false, false>(j, st);
+}
+
+}  // namespace fp4q

@@ -266,6 +266,27 @@ int mxfp4_fake_quantize(const fp4q_params_t *p, const void *x, void *y, void *st
  * to 0 on the stream, then combined with atomic maxima). */
 int fp4_tensor_amax(const fp4q_params_t *p, const void *x, const float *residual, float *amax, void *stream);
 
+/* MXFP4 projection re-encoded as MXFP8, fused ("MXFP4 weight QAT recipes on
+ * MXFP8 and FP8 block-scaling hosts", "Design": the projected weight handed
+ * to the host's MXFP8 quantizer -- rowwise losslessly, columnwise 32 x 1 with
+ * bounded re-quantization; "Known limitations": the fused projection +
+ * quantize kernel).  x is read once; outputs:
+ *   y (optional, NULL to skip): the projection, as mxfp4_fake_quantize;
+ *   rowwise (p->out_mask & FP4Q_OUT_ROW): row_codes [G, M, K] E4M3 bytes,
+ *     row_scales [G, M, K/32] UE8M0 bytes (1 x 32 blocks along K);
+ *   columnwise (FP4Q_OUT_COL): col_codes [G, K, M], col_scales [G, K, M/32]
+ *     (32 x 1 blocks along M, stored as x transposed); needs M % 32 == 0.
+ * MXFP8 (the pages do not define it; the OCP Microscaling v1.0 rule): per
+ * block the scale byte is X + 127 with X = floor(log2 max|v|) - 8 clamped to
+ * [-127, 127] (all-zero blocks: X = -127); elements are E4M3(v / 2^X), round
+ * to nearest even, saturating at 448, sign kept.  A block holding a NaN (a
+ * poisoned MXFP4 block) has scale 0xFF and element bytes 0x7F.  The rowwise
+ * encoding of a projected block is exact: decoding it gives y.
+ * Requires K % 32 == 0, 16-byte aligned x rows, y and code buffers; the knobs
+ * as for mxfp4_fake_quantize. */
+int mxfp4_project_mxfp8(const fp4q_params_t *p, const void *x, void *y, uint8_t *row_codes, uint8_t *row_scales,
+                        uint8_t *col_codes, uint8_t *col_scales, void *stream);
+
 /* Input bytes of one chunk of mxfp4_fake_quantize_host (a whole number of
  * rows; at least one row). */
 #define FP4Q_HOST_CHUNK_BYTES (16u << 20)
