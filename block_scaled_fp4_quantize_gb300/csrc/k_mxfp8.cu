@@ -82,7 +82,7 @@ __device__ __forceinline__ void load_block32(const void* x, int64_t idx, float (
 }
 
 template <bool IN_BF16, bool OUT_BF16>
-__global__ void __launch_bounds__(XT) mxfp8_kernel(const QuantJob j, int64_t tiles_m, int64_t tiles_k) {
+__global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t tiles_m, int64_t tiles_k) {
   __shared__ __align__(16) unsigned char ys[XM * YS];  // projected tile, bf16
   const int t = threadIdx.x;
   const int64_t tile = blockIdx.x;
@@ -108,32 +108,34 @@ __global__ void __launch_bounds__(XT) mxfp8_kernel(const QuantJob j, int64_t til
         qb[i] = e2m1x2_rne(ieee_mul(v[2 * i], inv), ieee_mul(v[2 * i + 1], inv));
         qmax = umax(qmax, umax(qb[i] & 7u, (qb[i] >> 4) & 7u));
       }
-      // projected values y = e2m1(q) 2^E (exact)
-      float y[32];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float g0, g1;
-        e2m1x2_decode(qb[i], g0, g1);
-        y[2 * i] = ieee_mul(g0, sc);
-        y[2 * i + 1] = ieee_mul(g1, sc);
-      }
+      // projected values y = e2m1(q) 2^E (exact), recomputed from the codes
+      // for each output so that no 32-value array stays live
       const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
-      if (j.y) {
-        if (OUT_BF16) {
-          uint4* d = reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n);
+      if (j.y || j.col_codes) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(y[8 * q + 2 * i], y[8 * q + 2 * i + 1]);
-            d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int i = 0; i < 4; ++i) {
+            float g0, g1;
+            e2m1x2_decode(qb[4 * q + i], g0, g1);
+            w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(ieee_mul(g0, sc), ieee_mul(g1, sc));
           }
-        } else {
+          if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
+            *reinterpret_cast<uint4*>(ys + rr * YS + rh * 64 + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (j.y && OUT_BF16) reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (j.y && !OUT_BF16) {
           float4* d = reinterpret_cast<float4*>(static_cast<float*>(j.y) + n);
           const float qn = bitsf(0x7FC00000u);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            d[q] = poison ? make_float4(qn, qn, qn, qn) : make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+          for (int q = 0; q < 8; ++q) {
+            float g[4];
+            e2m1x2_decode(qb[2 * q], g[0], g[1]);
+            e2m1x2_decode(qb[2 * q + 1], g[2], g[3]);
+            d[q] = poison ? make_float4(qn, qn, qn, qn)
+                          : make_float4(ieee_mul(g[0], sc), ieee_mul(g[1], sc), ieee_mul(g[2], sc), ieee_mul(g[3], sc));
+          }
         }
       }
       if (j.row_codes) {
@@ -155,16 +157,6 @@ __global__ void __launch_bounds__(XT) mxfp8_kernel(const QuantJob j, int64_t til
         d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
         d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
         j.row_scales[n / 32] = poison ? (uint8_t)0xFF : (uint8_t)(X + 127);
-      }
-      if (j.col_codes) {  // stage the projection (bf16, exact; NaN for a poisoned block)
-        uint4* d = reinterpret_cast<uint4*>(ys + rr * YS + rh * 64);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(y[8 * q + 2 * i], y[8 * q + 2 * i + 1]);
-          d[q] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
       }
     }
   }
