@@ -64,6 +64,7 @@ class Cfg(ctypes.Structure):
         ("fmt", ctypes.c_int32), ("rounding", ctypes.c_int32), ("seed", ctypes.c_uint64),
         ("step", ctypes.c_uint32), ("out_mask", ctypes.c_uint32), ("use_precomputed", ctypes.c_int32),
         ("sr_index_base", ctypes.c_int64),
+        ("col_hadamard", ctypes.c_int32), ("hadamard_signs", ctypes.c_uint32),
     ]
 
 
@@ -110,6 +111,8 @@ def _lib():
         L.orc_e4m3_encode.argtypes = [ctypes.c_double]
         L.orc_mxfp4_project_mxfp8.restype = ctypes.c_int
         L.orc_mxfp4_project_mxfp8.argtypes = [ctypes.POINTER(Cfg), P, P, P, P, P, P]
+        L.orc_rht16.restype = None
+        L.orc_rht16.argtypes = [P, ctypes.c_uint32, ctypes.c_int32]
         L.orc_subnormals_ok.restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -141,7 +144,7 @@ def _as3d(x):
 
 def make_cfg(x, K=None, *, mode="none", ob=0, outer_2d=False, inner_2d=False, fmt="e4m3",
              rounding="rne", seed=0, step=0, out_mask=ROW, use_precomputed=False, out_dtype=None,
-             sr_index_base=0):
+             sr_index_base=0, col_hadamard=False, hadamard_signs=0):
     G, M, ld = x.shape
     K = ld if K is None else K
     in_code = _dtype_code(x)
@@ -149,7 +152,8 @@ def make_cfg(x, K=None, *, mode="none", ob=0, outer_2d=False, inner_2d=False, fm
     return Cfg(G, M, K, ld, in_code, out_code, _MODES[mode] if isinstance(mode, str) else mode, ob,
                int(outer_2d), int(inner_2d), _FMTS[fmt] if isinstance(fmt, str) else fmt,
                {"rne": RNE, "sr": SR}[rounding] if isinstance(rounding, str) else rounding,
-               seed, step, out_mask, int(use_precomputed), int(sr_index_base))
+               seed, step, out_mask, int(use_precomputed), int(sr_index_base), int(bool(col_hadamard)),
+               int(hadamard_signs) & 0xFFFFFFFF)
 
 
 def outer_shapes(cfg):
@@ -272,6 +276,14 @@ def mxfp4_project_mxfp8(x, K=None, *, out_dtype=None, out_mask=ROW | COL, with_y
                                        _ptr(out["row_scales"]), _ptr(out["col_codes"]), _ptr(out["col_scales"]))
     assert rc == 0
     return out
+
+
+def rht16(v, signs: int, in_dtype: str = "fp32"):
+    """The oracle's 16-point random Hadamard transform of one block (float32)."""
+    a = np.ascontiguousarray(np.asarray(v, np.float32).copy())
+    assert a.shape == (16,)
+    _lib().orc_rht16(_ptr(a), int(signs) & 0xFFFFFFFF, BF16 if in_dtype == "bf16" else FP32)
+    return a
 
 
 def mxfp8_exponent(A: float) -> int:

@@ -66,6 +66,9 @@ typedef struct {
                                 stochastic-rounding counter, so a slice of
                                 rows can be checked with the indices it has
                                 in the whole tensor (0 for whole tensors)   */
+  int32_t col_hadamard;      /* 1: Hadamard transform along M before the
+                                columnwise quantization (orc_rht16)        */
+  uint32_t hadamard_signs;   /* bit i set: element i of each 16-block negated */
 } orc_cfg;
 
 /* ------------------------------------------------------------------------ */
@@ -382,6 +385,46 @@ static float *build_u(const orc_cfg *cf, const void *x, const float *residual) {
   return u;
 }
 
+/* Random Hadamard transform of one block of 16 values ([ALTO] "Op-level test
+ * coverage": outer-block scaling combined with an M-axis Hadamard transform;
+ * the page does not define it, so this is the reading): negate element i
+ * where bit i of `signs` is set, apply the 16 x 16 Sylvester Hadamard matrix
+ * (entry (i, k) = (-1)^popcount(i & k)) and scale by 1/4 (= 1/sqrt 16, so
+ * the transform is orthonormal).  The product is computed by the fast
+ * Walsh-Hadamard butterfly -- for h = 1, 2, 4, 8 and each i with (i & h) == 0,
+ * (v_i, v_{i+h}) <- (v_i + v_{i+h}, v_i - v_{i+h}) -- every sum one binary32
+ * operation in this order, then each value times 0.25.  Values that leave
+ * the binary32 range are sanitized again like the input (NaN -> +0,
+ * +-inf -> +-the largest finite value of the input dtype). */
+void orc_rht16(float *v, uint32_t signs, int32_t in_dtype) {
+  for (int i = 0; i < 16; i++)
+    if ((signs >> i) & 1u) v[i] = -v[i];
+  for (int h = 1; h < 16; h <<= 1)
+    for (int i = 0; i < 16; i++)
+      if (!(i & h)) {
+        float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+  for (int i = 0; i < 16; i++) v[i] = sanitize(v[i] * 0.25f, in_dtype);
+}
+
+/* u with every 16-row block of every column transformed by orc_rht16 (the
+ * input of the columnwise orientation when col_hadamard is set). */
+static float *build_z(const orc_cfg *cf, const float *u) {
+  int64_t G = cf->G, M = cf->M, K = cf->K;
+  float *z = (float *)malloc(sizeof(float) * (size_t)(G * M * K));
+  float blk[16];
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t j = 0; j < K; j++)
+      for (int64_t i0 = 0; i0 < M; i0 += 16) {
+        for (int r = 0; r < 16; r++) blk[r] = u[(g * M + i0 + r) * K + j];
+        orc_rht16(blk, cf->hadamard_signs, cf->in_dtype);
+        for (int r = 0; r < 16; r++) z[(g * M + i0 + r) * K + j] = blk[r];
+      }
+  return z;
+}
+
 /* Quantize x into the requested orientations.  Outer-scale buffers:
  * S_row [G,M,K/ob] (1-D rowwise), S_col [G,K,M/ob] (1-D columnwise),
  * S_tile [G,M/ob,K/ob] (2-D, shared) or [1] (tensorwise).  With
@@ -392,7 +435,24 @@ int orc_quantize(const orc_cfg *cf, const void *x, float *residual,
                  uint8_t *col_codes, uint8_t *col_scales, float *S_col, float *S_tile) {
   int64_t n_el = cf->G * cf->M * cf->K;
   float *u = build_u(cf, x, residual);
-  if (!cf->use_precomputed) compute_outer(cf, u, S_row, S_col, S_tile);
+  float *z = NULL;
+  if (cf->col_hadamard && (cf->out_mask & ORC_COL)) {
+    /* the transform feeds the columnwise side only: its outer scales come
+       from z, so tensorwise / 2-D scales (shared by both sides) do not apply */
+    if (cf->mode == ORC_MODE_TENSORWISE || (cf->mode == ORC_MODE_OUTER && cf->outer_2d) || cf->inner_2d ||
+        cf->use_precomputed || cf->M % 16) {
+      free(u);
+      return -2;
+    }
+    z = build_z(cf, u);
+    orc_cfg rc = *cf, cc = *cf;
+    rc.out_mask = cf->out_mask & ORC_ROW;
+    cc.out_mask = ORC_COL;
+    compute_outer(&rc, u, S_row, S_col, S_tile);
+    compute_outer(&cc, z, S_row, S_col, S_tile);
+  } else if (!cf->use_precomputed) {
+    compute_outer(cf, u, S_row, S_col, S_tile);
+  }
   if (cf->out_mask & ORC_ROW) {
     float *deq = residual ? (float *)malloc(sizeof(float) * (size_t)n_el) : NULL;
     quantize_orientation(cf, ORC_ROW, u, S_row, S_col, S_tile, row_codes, row_scales, deq);
@@ -403,7 +463,8 @@ int orc_quantize(const orc_cfg *cf, const void *x, float *residual,
     }
   }
   if (cf->out_mask & ORC_COL)
-    quantize_orientation(cf, ORC_COL, u, S_row, S_col, S_tile, col_codes, col_scales, NULL);
+    quantize_orientation(cf, ORC_COL, z ? z : u, S_row, S_col, S_tile, col_codes, col_scales, NULL);
+  free(z);
   free(u);
   return 0;
 }

@@ -701,3 +701,75 @@ def test_mxfp8_zero_and_signed_zero_blocks(orc):
     assert (out["row_scales"][0] == 0).all()                # X = -127 for all-zero blocks
     assert (out["row_codes"][0][:, :32] == 0x00).all() and (out["row_codes"][0][:, 32:] == 0x80).all()
     assert (out["col_codes"][0][:32] == 0x00).all() and (out["col_codes"][0][32:] == 0x80).all()
+
+
+# ----------------------------------------------------------------------------
+# Random Hadamard transform along M before the columnwise quantization
+# ([ALTO] "Op-level test coverage": outer-block x M-axis Hadamard; the
+# transform itself is this build's reading, stated in the oracle)
+# ----------------------------------------------------------------------------
+
+def _sylvester16():
+    H = np.ones((16, 16), dtype=object)
+    for i in range(16):
+        for k in range(16):
+            H[i, k] = -1 if bin(i & k).count("1") % 2 else 1
+    return H
+
+
+def test_rht16_is_the_scaled_sylvester_product(orc):
+    """Integer inputs: every butterfly sum is exact, so the oracle must give
+    (1/4) H16 (s .* v) exactly (rational arithmetic)."""
+    H = _sylvester16()
+    rng = np.random.default_rng(31)
+    for _ in range(200):
+        v = rng.integers(-4096, 4096, 16)
+        s = int(rng.integers(0, 1 << 16))
+        sv = [Fraction(int(v[i]) * (-1 if (s >> i) & 1 else 1)) for i in range(16)]
+        want = [sum(H[i, k] * sv[k] for k in range(16)) / 4 for i in range(16)]
+        got = orc.rht16(v.astype(np.float32), s)
+        assert [Fraction(float(g)) for g in got] == want
+
+
+def test_rht16_is_orthonormal_and_its_own_inverse(orc):
+    rng = np.random.default_rng(32)
+    for _ in range(100):
+        v = rng.integers(-1000, 1000, 16).astype(np.float32)
+        s = int(rng.integers(0, 1 << 16))
+        back = orc.rht16(orc.rht16(v, s), 0)              # (H/4)(H/4) = I, then undo the signs
+        flip = np.array([-1 if (s >> i) & 1 else 1 for i in range(16)], np.float32)
+        assert (back * flip == v).all()
+        w = rng.standard_normal(16).astype(np.float32) * np.float32(10.0 ** rng.uniform(-20, 20))
+        z = orc.rht16(w, s).astype(np.float64)
+        nw = np.linalg.norm(w.astype(np.float64))
+        assert abs(np.linalg.norm(z) - nw) <= 1e-6 * nw
+
+
+def test_rht16_overflow_is_sanitized(orc):
+    big = np.full(16, np.float32(3.3895314e38))            # largest finite bf16
+    z = orc.rht16(big, 0, in_dtype="bf16")
+    assert np.isfinite(z).all()
+    assert z[0] == np.float32(3.3895314e38) and (z[1:] == 0).all()
+
+
+def test_col_hadamard_quantize_is_quantize_of_the_transform(orc):
+    """With col_hadamard, the columnwise codes and scales are those of the
+    ordinary columnwise quantization of the transformed tensor; the rowwise
+    side is untouched."""
+    x = W.lognormal((1, 64, 64), 34, sigma=2.0)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    xf = x.float().numpy()[0]
+    s = 0xA5C3
+    z = np.empty_like(xf)
+    for j in range(64):
+        for i0 in range(0, 64, 16):
+            z[i0:i0 + 16, j] = orc.rht16(xf[i0:i0 + 16, j], s, in_dtype="bf16")
+    for kw in (dict(mode="none"), dict(mode="outer_block", ob=16), dict(mode="outer_block", ob=32),
+               dict(mode="none", rounding="sr", seed=4, step=1)):
+        got = orc.quantize(xb, out_mask=3, col_hadamard=True, hadamard_signs=s, **kw)
+        ref_row = orc.quantize(xb, out_mask=1, **kw)
+        ref_col = orc.quantize(z[None].astype(np.float32), out_mask=2, **kw)
+        assert (got["row_codes"] == ref_row["row_codes"]).all() and (got["row_scales"] == ref_row["row_scales"]).all()
+        assert (got["col_codes"] == ref_col["col_codes"]).all() and (got["col_scales"] == ref_col["col_scales"]).all()
+        if kw["mode"] == "outer_block":
+            assert (got["col_outer"].view(np.uint32) == ref_col["col_outer"].view(np.uint32)).all()
