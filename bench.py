@@ -300,6 +300,10 @@ def _extra_workloads():
         "activations_tensorwise": (_activations(dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4, 3),
                                    50, 5),
         "activations_none": (_activations(dict(mode="none"), 2 * codes + 2 * (M * K // 16), 1), 50, 5),
+        "activations_hadamard_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64,
+                                                               col_hadamard=True, hadamard_signs=0xA5C3),
+                                                          2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1),
+                                             50, 5),
         "activations_rowwise_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64),
                                                          codes + M * K // 16 + (M * K // 64) * 4, 1,
                                                          columnwise=False), 50, 5),

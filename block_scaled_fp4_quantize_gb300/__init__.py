@@ -73,7 +73,7 @@ def _view3d(x: torch.Tensor):
 
 def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_size=0, outer_2d=False,
             inner_2d=False, scale_format="e4m3", stochastic=False, seed=0, step=0, out_mask=_capi.OUT_ROW,
-            use_precomputed_outer=False, scale_layout="linear"):
+            use_precomputed_outer=False, scale_layout="linear", col_hadamard=False, hadamard_signs=0):
     p = _capi.new_params(_lib())
     p.G, p.M, p.K, p.ld = G, M, K, ld
     p.in_dtype = _DT.get(in_dtype, -1)
@@ -89,6 +89,8 @@ def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_s
     p.out_mask = int(out_mask)
     p.use_precomputed_outer = int(bool(use_precomputed_outer))
     p.scale_layout = _LAYOUTS[scale_layout]
+    p.col_hadamard = int(bool(col_hadamard))
+    p.hadamard_signs = int(hadamard_signs) & 0xFFFF
     return p
 
 
@@ -138,7 +140,8 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
              inner_2d: bool = False, scale_format: str = "e4m3", stochastic: bool = False, seed: int = 0,
              step: int = 0, rowwise: bool = True, columnwise: bool = False,
              residual: Optional[torch.Tensor] = None, precomputed_outer: Optional[QuantizedFP4] = None,
-             out: Optional[QuantizedFP4] = None, scale_layout: str = "linear") -> QuantizedFP4:
+             out: Optional[QuantizedFP4] = None, scale_layout: str = "linear", col_hadamard: bool = False,
+             hadamard_signs: int = 0) -> QuantizedFP4:
     """NVFP4 / AMD-FP4 quantize of a CUDA bf16 or fp32 tensor ([M, K] or [G, M, K]).
 
     ``residual`` (fp32, [G, M, K] contiguous) enables error feedback and is
@@ -147,12 +150,15 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
     preallocated output buffers.  ``scale_layout="mma"`` writes the inner
     scales in the 128 x 4 tiled layout block-scaled tensor-core MMAs read
     (see include/fp4q.h); the scale tensors are then flat padded byte
-    buffers."""
+    buffers.  ``col_hadamard`` applies the random Hadamard transform along M
+    (16-row blocks, sign mask ``hadamard_signs``) before the columnwise
+    quantization."""
     x3, G, M, K, ld = _view3d(x)
     mask = (_capi.OUT_ROW if rowwise else 0) | (_capi.OUT_COL if columnwise else 0)
     p = _params(G, M, K, ld, x.dtype, mode=mode, outer_block_size=outer_block_size, outer_2d=outer_2d,
                 inner_2d=inner_2d, scale_format=scale_format, stochastic=stochastic, seed=seed, step=step,
-                out_mask=mask, use_precomputed_outer=precomputed_outer is not None, scale_layout=scale_layout)
+                out_mask=mask, use_precomputed_outer=precomputed_outer is not None, scale_layout=scale_layout,
+                col_hadamard=col_hadamard, hadamard_signs=hadamard_signs)
     s = query_sizes(p)
     dev = x.device
     if out is None:

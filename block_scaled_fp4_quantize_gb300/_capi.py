@@ -16,7 +16,7 @@ BF16, FP32, FP16 = 1, 2, 3
 MODE_NONE, MODE_TENSORWISE, MODE_OUTER_BLOCK = 0, 1, 2
 SCALE_E4M3, SCALE_UE5M3 = 0, 1
 SCALE_LAYOUT_LINEAR, SCALE_LAYOUT_MMA = 0, 1
-ABI_VERSION = 2  # FP4Q_ABI_VERSION of include/fp4q.h
+ABI_VERSION = 3  # FP4Q_ABI_VERSION of include/fp4q.h
 RNE, STOCHASTIC = 0, 1
 OUT_ROW, OUT_COL = 1, 2
 
@@ -35,7 +35,7 @@ class Params(ctypes.Structure):
         ("outer_block_size", ctypes.c_int32), ("outer_2d", ctypes.c_int32), ("inner_2d", ctypes.c_int32),
         ("scale_format", ctypes.c_int32), ("rounding", ctypes.c_int32),
         ("seed", ctypes.c_uint64), ("step", ctypes.c_uint32), ("use_precomputed_outer", ctypes.c_int32),
-        ("scale_layout", ctypes.c_int32),
+        ("scale_layout", ctypes.c_int32), ("col_hadamard", ctypes.c_int32), ("hadamard_signs", ctypes.c_uint32),
     ]
 
 

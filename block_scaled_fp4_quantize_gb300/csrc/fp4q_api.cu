@@ -59,6 +59,7 @@ int check_nvfp4(const fp4q_params_t* p, uint32_t mask) {
   if (p->rounding != FP4Q_RNE && p->rounding != FP4Q_STOCHASTIC) return FP4Q_ERR_MODE;
   if ((p->outer_2d & ~1) || (p->inner_2d & ~1) || (p->use_precomputed_outer & ~1)) return FP4Q_ERR_MODE;
   if (p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR && p->scale_layout != FP4Q_SCALE_LAYOUT_MMA) return FP4Q_ERR_MODE;
+  if (p->col_hadamard & ~1) return FP4Q_ERR_MODE;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K) return FP4Q_ERR_SHAPE;
   if (p->K % 16) return FP4Q_ERR_SHAPE;
   const bool col = (mask & FP4Q_OUT_COL) != 0u;
@@ -148,8 +149,12 @@ int prepare_outer(const fp4q_params_t* p, QuantJob& j, void* ws, cudaStream_t st
 // FP4Q_NO_CTB_KERNEL=1 skip the flat and the bf16 cast-transpose kernels
 // (for parity testing of each path).
 int launch_quantizer(const QuantJob& j, bool vec, cudaStream_t st) {
-  const bool fast = vec && ct_supports(j) && !getenv_flag("FP4Q_GENERAL_KERNEL");
   cudaError_t e;
+  if (j.col_rht) {  // only the bf16 cast-transpose kernel has the transform
+    if (!launch_ctb(j, st, &e)) return FP4Q_ERR_CUDA;
+    return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+  }
+  const bool fast = vec && ct_supports(j) && !getenv_flag("FP4Q_GENERAL_KERNEL");
   if (fast && row_supports(j) && !getenv_flag("FP4Q_NO_ROW_KERNEL")) e = launch_row(j, st);
   else if (fast && ctb_supports(j) && !getenv_flag("FP4Q_NO_CTB_KERNEL") && launch_ctb(j, st, &e)) {}
   else if (fast) e = launch_ct(j, st);
@@ -217,7 +222,17 @@ int fp4_quantize(const fp4q_params_t* p, const void* x, const fp4q_outputs_t* ou
       return cudaMemsetAsync(out->tile_outer, 0, sizeof(float), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
     return FP4Q_OK;
   }
+  if (p->col_hadamard) {
+    const int ob = p->outer_block_size;
+    if (!col) return FP4Q_ERR_MODE;
+    if (p->in_dtype != FP4Q_BF16 || p->inner_2d || p->mode == FP4Q_MODE_TENSORWISE || p->use_precomputed_outer ||
+        (p->mode == FP4Q_MODE_OUTER_BLOCK && (p->outer_2d || !(ob == 16 || ob == 32 || ob == 64))) ||
+        !vec_ok(p, x, residual, nullptr))
+      return FP4Q_ERR_UNSUPPORTED;
+  }
   QuantJob j = base_job(p, x, residual);
+  j.col_rht = p->col_hadamard;
+  j.rht_signs = p->hadamard_signs & 0xFFFFu;
   j.do_row = row;
   j.do_col = col;
   j.row_codes = row ? out->row_codes : nullptr;
@@ -260,7 +275,7 @@ int fp4_quantize_grouped(const fp4q_params_t* p, const void* x, const int64_t* o
   const uint32_t mask = p->out_mask;
   const bool row = mask & FP4Q_OUT_ROW, col = mask & FP4Q_OUT_COL;
   const bool small_ob = p->outer_block_size == 16 || p->outer_block_size == 32 || p->outer_block_size == 64;
-  if (p->in_dtype != FP4Q_BF16 || p->inner_2d || p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR ||
+  if (p->in_dtype != FP4Q_BF16 || p->inner_2d || p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR || p->col_hadamard ||
       (p->use_precomputed_outer && p->mode != FP4Q_MODE_OUTER_BLOCK) ||
       (p->mode == FP4Q_MODE_OUTER_BLOCK && col && !p->outer_2d && !small_ob && !p->use_precomputed_outer))
     return FP4Q_ERR_UNSUPPORTED;
@@ -322,6 +337,7 @@ int fp4_qdq(const fp4q_params_t* p, int orient, const void* x, void* y, float* r
   rc = check_dtype(p->out_dtype);
   if (rc) return rc;
   if (residual && orient == (int)FP4Q_OUT_COL) return FP4Q_ERR_UNSUPPORTED;
+  if (p->col_hadamard) return FP4Q_ERR_UNSUPPORTED;
   fp4q_sizes_t s;
   sizes_for(p, (uint32_t)orient, &s);
   const bool needs_outer = p->mode != FP4Q_MODE_NONE;
@@ -392,7 +408,8 @@ int mxfp4_fake_quantize(const fp4q_params_t* p, const void* x, void* y, void* st
   rc = check_dtype(p->out_dtype);
   if (rc) return rc;
   if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
-      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0)
+      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0 ||
+      p->col_hadamard != 0)
     return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K || p->K % 32) return FP4Q_ERR_SHAPE;
@@ -437,7 +454,8 @@ int mxfp4_project_mxfp8(const fp4q_params_t* p, const void* x, void* y, uint8_t*
   rc = check_dtype(p->out_dtype);
   if (rc) return rc;
   if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
-      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0)
+      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0 ||
+      p->col_hadamard != 0)
     return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
   const uint32_t mask = p->out_mask;

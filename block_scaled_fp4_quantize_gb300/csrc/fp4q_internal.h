@@ -96,6 +96,8 @@ struct QuantJob {
   int64_t ngroups;
   const int64_t* goff;  // device [ngroups + 1]
   GroupWs* gws;         // device workspace of the grouped path
+  int col_rht;          // 1: Hadamard transform along M before the columnwise side
+  uint32_t rht_signs;   // its sign mask (bit i: element i of each 16-block negated)
 };
 
 struct DequantJob {
@@ -130,6 +132,7 @@ bool row_supports(const QuantJob& j);
 bool ctb_supports(const QuantJob& j);
 bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 bool launch_ctb_grouped(const QuantJob& j, cudaStream_t st, cudaError_t* err);
+bool launch_ctb_rht(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 cudaError_t launch_row(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_ct(const QuantJob& j, cudaStream_t st);
 cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_t st);

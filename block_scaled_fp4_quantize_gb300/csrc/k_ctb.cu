@@ -36,7 +36,8 @@ bool ctb_supports(const QuantJob& j) {
 // false: the tensor map could not be built (the caller takes another kernel)
 bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   if (j.ngroups > 0) return launch_ctb_grouped(j, st, err);
-  return launch_ctb_all<false>(j, st, err);
+  if (j.col_rht) return launch_ctb_rht(j, st, err);
+  return launch_ctb_all<false, false>(j, st, err);
 }
 
 }  // namespace fp4q

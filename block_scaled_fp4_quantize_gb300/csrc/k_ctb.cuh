@@ -63,6 +63,43 @@ __device__ __forceinline__ float bf16x2_hmax(uint32_t m) {
   return bitsf((hi > lo ? hi : lo) << 16);
 }
 
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Random Hadamard transform of a lane's two column blocks (16 rows each, the
+// pair (column 2 l, column 2 l + 1) packed per row): signs, the fast
+// Walsh-Hadamard butterfly h = 1, 2, 4, 8 in binary32, times 1/4 -- the
+// same operations in the same order as the definition.
+__device__ __forceinline__ void rht16x2(const uint32_t (&wv)[16], uint32_t signs, float (&z0)[16], float (&z1)[16]) {
+  uint64_t p[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t neg = ((signs >> i) & 1u) ? 0x8000000080000000ull : 0ull;
+    p[i] = pk2(bf16lo(wv[i]), bf16hi(wv[i])) ^ neg;
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      const uint64_t a = p[i], b = p[i + h];
+      p[i] = add2(a, b);
+      p[i + h] = sub2(a, b);
+    }
+  }
+  const uint64_t q = pk2(0.25f, 0.25f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) upk2(mul2(p[i], q), z0[i], z1[i]);
+}
+
 // Per-block steps shared by both passes: inner scale, x' = u / S, codes.
 // With an outer scale (NEG) the block arrives negated, v = -u.
 template <bool SR, bool UE5M3, bool NEG>
@@ -102,7 +139,7 @@ struct GroupCursor {
   }
 };
 
-template <bool SR, bool UE5M3, int BO, bool GR>
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
 __global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -392,7 +429,23 @@ __global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __gr
       for (int i = 2; i < 16; i += 2) mx = bf16x2_amax(mx, bf16x2_amax(wv[i], wv[i + 1]));
       mx &= 0x7FFF7FFFu;
     }
-    const float cam[2] = {bitsf(mx << 16), bitsf(mx & 0xFFFF0000u)};
+    float cam[2] = {bitsf(mx << 16), bitsf(mx & 0xFFFF0000u)};
+    // columnwise Hadamard transform along M (the rowwise side is untouched)
+    float z0[16], z1[16];
+    if (RHT) {
+      rht16x2(wv, j.rht_signs, z0, z1);
+      cam[0] = amax16(z0);
+      cam[1] = amax16(z1);
+      if (fbits(cam[0]) >= 0x7F800000u || fbits(cam[1]) >= 0x7F800000u) {  // the sums left the range
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          z0[i] = sanitize(z0[i], 0x7F7F0000u);
+          z1[i] = sanitize(z1[i], 0x7F7F0000u);
+        }
+        cam[0] = amax16(z0);
+        cam[1] = amax16(z1);
+      }
+    }
     const int64_t mb = p.m0 + 16 * warp;  // first row of this lane's blocks
     const bool mvalid = mb < gend;
     float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
@@ -437,14 +490,15 @@ __global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __gr
     }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      float u[16];  // u, or -u with an outer scale
+      float u[16];  // u, or -u with an outer scale (the transformed z with RHT)
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        u[i] = BO == BO_NONE ? (c ? bf16hi(wv[i]) : bf16lo(wv[i])) : (c ? nbf16hi(wv[i]) : nbf16lo(wv[i]));
+        u[i] = RHT ? (c ? z1[i] : z0[i])
+                   : (BO == BO_NONE ? (c ? bf16hi(wv[i]) : bf16lo(wv[i])) : (c ? nbf16hi(wv[i]) : nbf16lo(wv[i])));
       const int64_t k = p.k0 + 2 * lane + c;
       uint32_t w0, w1;
-      const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, cam[c], S[c], R[c], none, j, 1u,
-                                                                (uint64_t)(cbase + k * cstride + mb), w0, w1);
+      const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE && !RHT>(tab, u, cam[c], S[c], R[c], none, j, 1u,
+                                                                         (uint64_t)(cbase + k * cstride + mb), w0, w1);
       *reinterpret_cast<uint2*>(cst + (2 * lane + c) * CST + 8 * warp) = make_uint2(w0, w1);
       sst[(2 * lane + c) * 8 + warp] = (uint8_t)sc;
     }
@@ -513,9 +567,9 @@ bool make_bf16_map(const QuantJob& j, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool SR, bool UE5M3, int BO, bool GR>
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
 cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
-  auto kern = ctb_kernel<SR, UE5M3, BO, GR>;
+  auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT>;
   static int per_sm_cache[128] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -537,22 +591,32 @@ cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, cudaStream_t
   return cudaGetLastError();
 }
 
-template <bool SR, bool UE5M3, bool GR>
+template <bool SR, bool UE5M3, bool GR, bool RHT>
 cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
-  if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR>(j, map, st);
-  if (j.s_src == S_TENSORWISE_WS || j.mode == 1) return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR>(j, map, st);
-  if (j.s_src == S_IN_TILE)
-    return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR>(j, map, st) : launch_ctb_t<SR, UE5M3, BO_T1D, GR>(j, map, st);
-  return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_B2D, GR>(j, map, st) : launch_ctb_t<SR, UE5M3, BO_B1D, GR>(j, map, st);
+  if constexpr (RHT) {  // the transform is defined with no outer scale or 1-D outer blocks
+    if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true>(j, map, st);
+    return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, st);
+  } else {
+    if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false>(j, map, st);
+    if (j.s_src == S_TENSORWISE_WS || j.mode == 1) return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false>(j, map, st);
+    if (j.s_src == S_IN_TILE)
+      return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false>(j, map, st)
+                        : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false>(j, map, st);
+    return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_B2D, GR, false>(j, map, st)
+                      : launch_ctb_t<SR, UE5M3, BO_B1D, GR, false>(j, map, st);
+  }
 }
 
-// All variants of one grouping mode: false if the tensor map cannot be built.
-template <bool GR>
+// All variants of one grouping / transform mode: false if the tensor map
+// cannot be built.
+template <bool GR, bool RHT>
 bool launch_ctb_all(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   CUtensorMap map;
   if (!make_bf16_map(j, &map)) return false;
-  if (j.sr) *err = j.ue5m3 ? launch_ctb_o<true, true, GR>(j, map, st) : launch_ctb_o<true, false, GR>(j, map, st);
-  else *err = j.ue5m3 ? launch_ctb_o<false, true, GR>(j, map, st) : launch_ctb_o<false, false, GR>(j, map, st);
+  if (j.sr)
+    *err = j.ue5m3 ? launch_ctb_o<true, true, GR, RHT>(j, map, st) : launch_ctb_o<true, false, GR, RHT>(j, map, st);
+  else
+    *err = j.ue5m3 ? launch_ctb_o<false, true, GR, RHT>(j, map, st) : launch_ctb_o<false, false, GR, RHT>(j, map, st);
   return true;
 }
 

@@ -6,7 +6,7 @@
 namespace fp4q {
 
 bool launch_ctb_grouped(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
-  return launch_ctb_all<true>(j, st, err);
+  return launch_ctb_all<true, false>(j, st, err);
 }
 
 }  // namespace fp4q

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define FP4Q_ABI_VERSION 2
+#define FP4Q_ABI_VERSION 3
 
 /* ---- status codes ------------------------------------------------------ */
 #define FP4Q_OK 0
@@ -111,6 +111,9 @@ typedef struct fp4q_params {
                                     outer-block scaling", "Implementation":
                                     precomputed_outer_scale)                        */
   int32_t scale_layout; /* FP4Q_SCALE_LAYOUT_LINEAR | FP4Q_SCALE_LAYOUT_MMA (below) */
+  int32_t col_hadamard; /* 1: random Hadamard transform along M before the
+                           columnwise quantization (fp4_quantize, below)    */
+  uint32_t hadamard_signs; /* bits 0-15: sign mask of that transform         */
 } fp4q_params_t;
 
 /* Inner-scale layouts.  An orientation's scales form, per matrix g, an
@@ -187,6 +190,21 @@ int fp4q_query_sizes(const fp4q_params_t *p, fp4q_sizes_t *sizes);
  *   Returns FP4Q_ERR_WORKSPACE if missing or too small. */
 int fp4_quantize(const fp4q_params_t *p, const void *x, const fp4q_outputs_t *out, float *residual,
                  void *workspace, size_t workspace_bytes, void *stream);
+/* With p->col_hadamard = 1 the columnwise side quantizes z instead of u:
+ * every 16-row block of every column is multiplied by (1/4) H16 D, with D
+ * = diag(+-1) from p->hadamard_signs (bit i set: row i of the block
+ * negated) and H16 the Sylvester Hadamard matrix, entry (i, k) =
+ * (-1)^popcount(i & k) ("NVFP4 / AMD-FP4 outer-block (two-level) scaling
+ * for FP4 training", "Op-level test coverage": outer-block x M-axis
+ * Hadamard).  z is computed by the fast Walsh-Hadamard butterfly (stages
+ * h = 1, 2, 4, 8, each sum one binary32 operation), times 1/4, then
+ * sanitized like the input; the columnwise outer scales are taken from z.
+ * The rowwise side is unchanged.  The product of two operands transformed
+ * with the same D over their shared M axis equals the untransformed product
+ * (H16 D / 4 is orthonormal).  Needs the columnwise mask, bf16 input, mode
+ * none or 1-D outer blocks of 16, 32 or 64 (computed, not precomputed),
+ * 1 x 16 inner blocks and 16-byte aligned rows (FP4Q_ERR_UNSUPPORTED
+ * otherwise). */
 
 /* Ragged grouped quantize (mixture-of-experts token groups): x is [M, K]
  * (p->G must be 1) and rows [offsets[e], offsets[e + 1]) form group e,

@@ -36,7 +36,7 @@ def test_header_declares_the_bound_functions():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.fp4q_abi_version() == 2
+    assert lib.fp4q_abi_version() == 3
     out = os.popen("nm -D --defined-only %s" % _capi._build.lib_path()).read()
     for name in declared_functions():
         assert re.search(r"\sT\s%s$" % name, out, re.M), name
@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_params_struct_layout_matches(lib):
     p = _capi.Params()
     lib.fp4q_params_init(ctypes.byref(p))
-    assert p.struct_size == ctypes.sizeof(_capi.Params) == 96
+    assert p.struct_size == ctypes.sizeof(_capi.Params) == 104
     assert (p.G, p.in_dtype, p.out_dtype, p.mode, p.out_mask, p.scale_layout) == (1, _capi.BF16, _capi.BF16, 0, 1, 0)
     assert ctypes.sizeof(_capi.Outputs) == 7 * 8 and ctypes.sizeof(_capi.Sizes) == 8 * 8
 
