@@ -13,7 +13,7 @@ namespace {
 
 constexpr int BT = 256;             // threads per CTA
 constexpr int BM = 128, BK = 64;    // tile
-constexpr int BNS = 3;              // tiles in flight
+constexpr int BNS = 2;              // tiles in flight (2 stages x 4 resident CTAs per SM)
 constexpr int BRAW = BM * BK * 2;   // bytes of one raw tile
 constexpr int CST = 72;             // bytes per staged column of codes (64 + 8 against bank conflicts)
 
@@ -140,7 +140,7 @@ struct GroupCursor {
 };
 
 template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
-__global__ void __launch_bounds__(BT, 3) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
