@@ -78,9 +78,12 @@ extern "C" int mxfp4_fake_quantize_host(const fp4q_params_t* p, const void* x, v
   // staging: 2 slots x (input rows + output rows), each buffer 256-byte aligned
   const int64_t in_row = p->K * ein, out_row = p->K * eout;
   auto round256 = [](int64_t v) { return (v + 255) & ~int64_t(255); };
-  int64_t chunk = (int64_t)(FP4Q_HOST_CHUNK_BYTES / in_row);
+  // the largest chunk (whole rows) whose two input and two output buffers fit
+  int64_t chunk = (int64_t)ws_bytes / (2 * (in_row + out_row));
+  while (chunk > 1 && 2 * (round256(chunk * in_row) + round256(chunk * out_row)) > (int64_t)ws_bytes) --chunk;
+  const int64_t cap = (int64_t)(FP4Q_HOST_CHUNK_BYTES / in_row);
+  if (chunk > cap) chunk = cap;
   if (chunk < 1) chunk = 1;
-  while (chunk > 1 && 2 * (round256(chunk * in_row) + round256(chunk * out_row)) > (int64_t)ws_bytes) chunk /= 2;
   if (2 * (round256(chunk * in_row) + round256(chunk * out_row)) > (int64_t)ws_bytes) return FP4Q_ERR_WORKSPACE;
   unsigned char* base = static_cast<unsigned char*>(ws);
   unsigned char* in_buf[2] = {base, base + round256(chunk * in_row)};

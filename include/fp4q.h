@@ -305,24 +305,26 @@ int fp4_tensor_amax(const fp4q_params_t *p, const void *x, const float *residual
 int mxfp4_project_mxfp8(const fp4q_params_t *p, const void *x, void *y, uint8_t *row_codes, uint8_t *row_scales,
                         uint8_t *col_codes, uint8_t *col_scales, void *stream);
 
-/* Input bytes of one chunk of mxfp4_fake_quantize_host (a whole number of
- * rows; at least one row). */
-#define FP4Q_HOST_CHUNK_BYTES (16u << 20)
+/* Largest input chunk of mxfp4_fake_quantize_host (a whole number of rows;
+ * at least one row). */
+#define FP4Q_HOST_CHUNK_BYTES (64u << 20)
 
 /* MXFP4 fake-quantize (as mxfp4_fake_quantize) of a tensor in HOST memory:
  * x is [G, M, K] host memory (row stride p->ld elements, matrices back to
  * back), y is [G, M, K] contiguous host memory in p->out_dtype.  The rows are
- * moved in chunks of about FP4Q_HOST_CHUNK_BYTES through `ws`, a caller-owned
- * DEVICE staging area (256-byte aligned) that holds two chunks of input and
- * two of output.  The host-to-device copy of one chunk, the kernel of the
- * previous one and the device-to-host copy of the one before overlap (two
- * copy streams that the library creates once per device, events, and the
- * kernel on `stream`).  The call returns once the work is enqueued; it is
- * complete when `stream` reaches the point of the call (later work on
- * `stream` sees y written).  Host buffers should be page-locked
- * (cudaHostAlloc / cudaHostRegister) for the copies to run asynchronously.
- * Calls on one device are serialized by a lock while they enqueue; `ws` must
- * not be shared with work that may run at the same time.
+ * moved in chunks through `ws`, a caller-owned DEVICE staging area
+ * (256-byte aligned) that holds two chunks of input and two of output; a
+ * chunk is the largest whole number of rows that lets the four fit in
+ * ws_bytes, at most FP4Q_HOST_CHUNK_BYTES of input (16 MiB chunks measured
+ * best for 134 MB transfers).  The host-to-device copy of one chunk, the
+ * kernel of the previous one and the device-to-host copy of the one before
+ * overlap (two copy streams that the library creates once per device,
+ * events, and the kernel on `stream`).  The call returns once the work is
+ * enqueued; it is complete when `stream` reaches the point of the call
+ * (later work on `stream` sees y written).  Host buffers should be
+ * page-locked (cudaHostAlloc / cudaHostRegister) for the copies to run
+ * asynchronously.  Calls on one device are serialized by a lock while they
+ * enqueue; `ws` must not be shared with work that may run at the same time.
  * Returns FP4Q_ERR_WORKSPACE if ws_bytes cannot hold two chunks of one row;
  * otherwise the errors of mxfp4_fake_quantize.  The pages' MXFP4 kernel reads
  * device memory; this entry point adds the host transfers around it. */
