@@ -242,6 +242,62 @@ __global__ void __launch_bounds__(256) outer_2d_kernel(const QuantJob j) {
   }
 }
 
+// Dequantize, linear scales without 2-D outer blocks: every index is a
+// function of the flat block index b (codes at 8 b, scale at b, a 1 x ob
+// outer scale at 16 b / ob), so there is no division.  One thread per
+// microblock, two in flight per thread; OUTER: 0 none, 1 one scale, 2 1-D.
+template <bool OUT_BF16, int OUTER>
+__global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
+  const ScaleFmt f = scale_fmt(j.ue5m3);
+  const int64_t nmb = j.G * j.R * (j.C / 16);
+  const int lob = j.ob > 0 ? 31 - __clz(j.ob) : 0;
+  const bool pow2 = j.ob > 0 && (j.ob & (j.ob - 1)) == 0;
+  const float S1 = OUTER == 1 ? j.outer[0] : 1.0f;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b0 < nmb; b0 += 2 * stride) {
+    uint2 cw[2];
+    uint32_t sb[2];
+    float S[2] = {S1, S1};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int64_t b = b0 + q * stride;
+      if (b < nmb) {
+        cw[q] = __ldcs(reinterpret_cast<const uint2*>(j.codes) + b);
+        sb[q] = j.scales[b];
+        if (OUTER == 2) S[q] = j.outer[pow2 ? (b * 16) >> lob : (b * 16) / j.ob];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int64_t b = b0 + q * stride;
+      if (b >= nmb) continue;
+      const float s = dec_scale(sb[q], f);
+      uint32_t w[8];
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = ((i < 4 ? cw[q].x : cw[q].y) >> (8 * (i & 3))) & 0xFFu;
+        float g0, g1;
+        e2m1x2_decode(byte, g0, g1);
+        float d0 = ieee_mul(g0, s), d1 = ieee_mul(g1, s);
+        if (OUTER) { d0 = ieee_mul(d0, S[q]); d1 = ieee_mul(d1, S[q]); }
+        v[2 * i] = d0;
+        v[2 * i + 1] = d1;
+        w[i] = pack_bf16x2(d0, d1);
+      }
+      if (OUT_BF16) {
+        uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + b * 16);
+        __stcs(p, make_uint4(w[0], w[1], w[2], w[3]));
+        __stcs(p + 1, make_uint4(w[4], w[5], w[6], w[7]));
+      } else {
+        float4* p = reinterpret_cast<float4*>(static_cast<float*>(j.y) + b * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) __stcs(p + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+      }
+    }
+  }
+}
+
 // Dequantize: one thread per 1 x 16 microblock.
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(256) dequant_kernel(const DequantJob j, int vec_out) {
@@ -368,6 +424,19 @@ cudaError_t launch_outer_prepass(const QuantJob& j, cudaStream_t st) {
 cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st) {
   const int64_t nmb = j.G * j.R * (j.C / 16);
   const int vec = vec_aligned(j.y, 16);
+  if (vec && !j.sl.mma && !(j.mode == 2 && j.outer_2d) && (reinterpret_cast<uintptr_t>(j.codes) & 7u) == 0) {
+    const int grid = grid_for((nmb + 1) / 2, 256, 8);
+    if (j.out_bf16) {
+      if (j.mode == 0) dequant_flat_kernel<true, 0><<<grid, 256, 0, st>>>(j);
+      else if (j.mode == 1) dequant_flat_kernel<true, 1><<<grid, 256, 0, st>>>(j);
+      else dequant_flat_kernel<true, 2><<<grid, 256, 0, st>>>(j);
+    } else {
+      if (j.mode == 0) dequant_flat_kernel<false, 0><<<grid, 256, 0, st>>>(j);
+      else if (j.mode == 1) dequant_flat_kernel<false, 1><<<grid, 256, 0, st>>>(j);
+      else dequant_flat_kernel<false, 2><<<grid, 256, 0, st>>>(j);
+    }
+    return cudaGetLastError();
+  }
   const int grid = grid_for(nmb, 256, 8);
   if (j.out_bf16) dequant_kernel<true><<<grid, 256, 0, st>>>(j, vec);
   else dequant_kernel<false><<<grid, 256, 0, st>>>(j, vec);
