@@ -19,8 +19,9 @@
 //     element y / 2^X = e2m1(q) 2^(E - X) is exact in E4M3.
 //   the projected values are staged in shared memory as bf16 (exact: two
 //     significant bits, exponents within bf16's range);
-//   columnwise: thread t owns column t mod 64 of rows 32 (t / 64) .. + 31,
-//     one 32 x 1 MXFP8 block, read from the staged tile.
+//   columnwise: a lane owns half (16 rows) of two 32 x 1 MXFP8 blocks of
+//     adjacent columns, read from the staged tile as bf16 pairs; the block
+//     maxima meet with one shuffle.
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
 
@@ -29,7 +30,7 @@ namespace {
 
 constexpr int XT = 256;
 constexpr int XM = 128, XK = 64;
-constexpr int YS = XK * 2 + 16;  // staged row stride in bytes (padding against bank conflicts)
+constexpr int YS = XK * 2;  // staged row stride in bytes; 16-byte units XOR-swizzled by bit 4 of the row
 
 // MXFP4 block exponent (see k_mxfp4.cu): least E with 6 * 2^E >= max(A, 6 * 2^-126), capped at 125.
 __device__ __forceinline__ int mx_exp(uint32_t amax_bits) {
@@ -122,7 +123,8 @@ __global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t 
             w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(ieee_mul(g0, sc), ieee_mul(g1, sc));
           }
           if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
-            *reinterpret_cast<uint4*>(ys + rr * YS + rh * 64 + 16 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ (((rr >> 4) & 1) << 2)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           if (j.y && OUT_BF16) reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n)[q] = make_uint4(w[0], w[1], w[2], w[3]);
         }
         if (j.y && !OUT_BF16) {
@@ -163,37 +165,50 @@ __global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t 
   if (!j.col_codes) return;
   __syncthreads();
 
-  // ---- columnwise: one 32 x 1 block per thread (M % 32 == 0)
-  const int c = t & 63, rb = t >> 6;
-  const int64_t k = k0 + c, mb = m0 + 32 * rb;
-  if (k >= K || mb >= M) return;
-  float v[32];
-  uint32_t amax = 0, nan = 0;
+  // ---- columnwise (M % 32 == 0): warp w takes the 32-row block w / 2 and
+  // column half w mod 2; lane l the column pair 16 (w mod 2) + (l mod 16)
+  // and rows 16 (l / 16) .. + 15 of the block, read as bf16 pairs (the two
+  // row halves of a 64-byte run sit 64 bytes apart through the swizzle, so
+  // a warp's loads do not conflict); the partner lane l ^ 16 holds the other
+  // half of both blocks.
+  const int lane = t & 31, warp = t >> 5;
+  const int rb = warp >> 1, half = lane >> 4;
+  const int col0 = 2 * (16 * (warp & 1) + (lane & 15));
+  const int64_t k = k0 + col0, mb = m0 + 32 * rb;
+  const bool valid = k < K && mb < M;  // K % 32 == 0: both columns or neither
+  uint32_t wv[16];
+  {
+    const unsigned char* base = ys + (32 * rb + 16 * half) * YS + (((col0 >> 3) ^ (half << 2)) << 4) + (col0 & 7) * 2;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t b = *reinterpret_cast<const uint16_t*>(ys + (32 * rb + i) * YS + 2 * c);
-    v[i] = bitsf(b << 16);
-    const uint32_t a = b & 0x7FFFu;
-    nan |= a > 0x7F80u ? 1u : 0u;
-    amax = umax(amax, a);
+    for (int i = 0; i < 16; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(base + i * YS);
   }
-  // X = floor(log2 amax) - 8 from the exponent bits (subnormal / zero amax: -127)
-  const int ex = (int)(amax >> 7);
-  int X = ex == 0 ? -127 : ex - 127 - 8;
-  X = X < -127 ? -127 : X;
-  const float inv = pow2f(-X);
-  uint32_t cw[8];
+  uint32_t mx = bf16x2_amax(wv[0], wv[1]);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    cw[i] = e4m3x2(ieee_mul(v[4 * i], inv), ieee_mul(v[4 * i + 1], inv)) |
-            (e4m3x2(ieee_mul(v[4 * i + 2], inv), ieee_mul(v[4 * i + 3], inv)) << 16);
-    if (nan) cw[i] = 0x7F7F7F7Fu;
+  for (int i = 2; i < 16; i += 2) mx = bf16x2_amax(mx, bf16x2_amax(wv[i], wv[i + 1]));
+  mx = bf16x2_amax(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+  if (!valid) return;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t a = (mx >> (16 * c)) & 0x7FFFu;  // |max| of the column's 32 values (NaN propagates)
+    const bool nan = a > 0x7F80u;
+    // X = floor(log2 amax) - 8 from the exponent bits (subnormal / zero amax: -127)
+    const int ex = (int)(a >> 7);
+    int X = ex == 0 ? -127 : ex - 127 - 8;
+    X = X < -127 ? -127 : X;
+    const float inv = pow2f(-X);
+    uint32_t cw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = c ? bf16hi(wv[4 * i + e]) : bf16lo(wv[4 * i + e]);
+      cw[i] = e4m3x2(ieee_mul(v[0], inv), ieee_mul(v[1], inv)) | (e4m3x2(ieee_mul(v[2], inv), ieee_mul(v[3], inv)) << 16);
+      if (nan) cw[i] = 0x7F7F7F7Fu;
+    }
+    const int64_t n = (g * K + k + c) * M + mb;  // block start in the [G, K, M] columnwise outputs
+    *reinterpret_cast<uint4*>(j.col_codes + n + 16 * half) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    if (half == 0) j.col_scales[n / 32] = nan ? (uint8_t)0xFF : (uint8_t)(X + 127);
   }
-  const int64_t n = (g * K + k) * M + mb;  // element index in the [G, K, M] columnwise outputs
-  uint4* d = reinterpret_cast<uint4*>(j.col_codes + n);
-  d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-  d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-  j.col_scales[n / 32] = nan ? (uint8_t)0xFF : (uint8_t)(X + 127);
 }
 
 template <bool IN_BF16, bool OUT_BF16>
