@@ -82,89 +82,81 @@ __device__ __forceinline__ void load_block32(const void* x, int64_t idx, float (
   }
 }
 
-template <bool IN_BF16, bool OUT_BF16>
-__global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t tiles_m, int64_t tiles_k) {
-  __shared__ __align__(16) unsigned char ys[XM * YS];  // projected tile, bf16
-  const int t = threadIdx.x;
-  const int64_t tile = blockIdx.x;
-  const int64_t tk = tile % tiles_k, tm = (tile / tiles_k) % tiles_m, g = tile / (tiles_k * tiles_m);
-  const int64_t m0 = tm * XM, k0 = tk * XK;
+// Rowwise part of one 1 x 32 block (row m, columns k ..): projection, the
+// optional projected output, the rowwise MXFP8 block and the bf16 staging of
+// the projection for the columnwise part.  v: the block's values, amax:
+// max |v| bits (inf / NaN: a poisoned block).
+template <bool OUT_BF16>
+__device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32], uint32_t amax, int64_t g, int64_t m,
+                                         int64_t k, int rr, int rh, unsigned char* ys) {
   const int64_t M = j.M, K = j.K;
-
-  // ---- rowwise: one 1 x 32 block per thread
-  {
-    const int rr = t >> 1, rh = t & 1;
-    const int64_t m = m0 + rr, k = k0 + 32 * rh;
-    if (m < M && k < K) {
-      float v[32];
-      uint32_t amax;
-      load_block32<IN_BF16>(j.x, (g * M + m) * j.ld + k, v, amax);
-      const bool poison = amax >= 0x7F800000u;
-      const int E = mx_exp(amax);
-      const float inv = pow2f(-E), sc = E >= -126 ? pow2f(E) : 0.0f;
-      uint32_t qb[16];  // E2M1 code bytes
-      uint32_t qmax = 0;
+  const bool poison = amax >= 0x7F800000u;
+  const int E = mx_exp(amax);
+  const float inv = pow2f(-E), sc = E >= -126 ? pow2f(E) : 0.0f;
+  uint32_t qb[16];  // E2M1 code bytes
+  uint32_t qmax = 0;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        qb[i] = e2m1x2_rne(ieee_mul(v[2 * i], inv), ieee_mul(v[2 * i + 1], inv));
-        qmax = umax(qmax, umax(qb[i] & 7u, (qb[i] >> 4) & 7u));
+  for (int i = 0; i < 16; ++i) {
+    qb[i] = e2m1x2_rne(ieee_mul(v[2 * i], inv), ieee_mul(v[2 * i + 1], inv));
+    qmax = umax(qmax, umax(qb[i] & 7u, (qb[i] >> 4) & 7u));
+  }
+  // projected values y = e2m1(q) 2^E (exact), recomputed from the codes
+  // for each output so that no 32-value array stays live
+  const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
+  if (j.y || j.col_codes) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float g0, g1;
+        e2m1x2_decode(qb[4 * q + i], g0, g1);
+        w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(ieee_mul(g0, sc), ieee_mul(g1, sc));
       }
-      // projected values y = e2m1(q) 2^E (exact), recomputed from the codes
-      // for each output so that no 32-value array stays live
-      const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
-      if (j.y || j.col_codes) {
+      if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
+        *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ (((rr >> 4) & 1) << 2)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      if (j.y && OUT_BF16) reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (j.y && !OUT_BF16) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(j.y) + n);
+      const float qn = bitsf(0x7FC00000u);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float g0, g1;
-            e2m1x2_decode(qb[4 * q + i], g0, g1);
-            w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(ieee_mul(g0, sc), ieee_mul(g1, sc));
-          }
-          if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
-            *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ (((rr >> 4) & 1) << 2)) << 4)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          if (j.y && OUT_BF16) reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n)[q] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        if (j.y && !OUT_BF16) {
-          float4* d = reinterpret_cast<float4*>(static_cast<float*>(j.y) + n);
-          const float qn = bitsf(0x7FC00000u);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float g[4];
-            e2m1x2_decode(qb[2 * q], g[0], g[1]);
-            e2m1x2_decode(qb[2 * q + 1], g[2], g[3]);
-            d[q] = poison ? make_float4(qn, qn, qn, qn)
-                          : make_float4(ieee_mul(g[0], sc), ieee_mul(g[1], sc), ieee_mul(g[2], sc), ieee_mul(g[3], sc));
-          }
-        }
-      }
-      if (j.row_codes) {
-        // X = E + floor(log2 e2m1(qmax)) - 8 (qmax: 0 -> zeros; 1 -> 0.5; 2,3 -> 1, 1.5; 4,5 -> 2, 3; 6,7 -> 4, 6)
-        const int fl = qmax <= 1u ? -1 : (int)(qmax >> 1) - 1;
-        int X = qmax == 0u ? -127 : E + fl - 8;
-        X = X < -127 ? -127 : X;
-        const float s2 = pow2f(E - X);  // 2^(E - X) in [2^1, 2^9]
-        uint32_t cw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float g[4];
-          e2m1x2_decode(qb[2 * i], g[0], g[1]);
-          e2m1x2_decode(qb[2 * i + 1], g[2], g[3]);
-          cw[i] = e4m3x2(ieee_mul(g[0], s2), ieee_mul(g[1], s2)) | (e4m3x2(ieee_mul(g[2], s2), ieee_mul(g[3], s2)) << 16);
-          if (poison) cw[i] = 0x7F7F7F7Fu;
-        }
-        uint4* d = reinterpret_cast<uint4*>(j.row_codes + n);
-        d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        j.row_scales[n / 32] = poison ? (uint8_t)0xFF : (uint8_t)(X + 127);
+      for (int q = 0; q < 8; ++q) {
+        float g[4];
+        e2m1x2_decode(qb[2 * q], g[0], g[1]);
+        e2m1x2_decode(qb[2 * q + 1], g[2], g[3]);
+        d[q] = poison ? make_float4(qn, qn, qn, qn)
+                      : make_float4(ieee_mul(g[0], sc), ieee_mul(g[1], sc), ieee_mul(g[2], sc), ieee_mul(g[3], sc));
       }
     }
   }
-  if (!j.col_codes) return;
-  __syncthreads();
+  if (j.row_codes) {
+    // X = E + floor(log2 e2m1(qmax)) - 8 (qmax: 0 -> zeros; 1 -> 0.5; 2,3 -> 1, 1.5; 4,5 -> 2, 3; 6,7 -> 4, 6)
+    const int fl = qmax <= 1u ? -1 : (int)(qmax >> 1) - 1;
+    int X = qmax == 0u ? -127 : E + fl - 8;
+    X = X < -127 ? -127 : X;
+    const float s2 = pow2f(E - X);  // 2^(E - X) in [2^1, 2^9]
+    uint32_t cw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float g[4];
+      e2m1x2_decode(qb[2 * i], g[0], g[1]);
+      e2m1x2_decode(qb[2 * i + 1], g[2], g[3]);
+      cw[i] = e4m3x2(ieee_mul(g[0], s2), ieee_mul(g[1], s2)) | (e4m3x2(ieee_mul(g[2], s2), ieee_mul(g[3], s2)) << 16);
+      if (poison) cw[i] = 0x7F7F7F7Fu;
+    }
+    uint4* d = reinterpret_cast<uint4*>(j.row_codes + n);
+    d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    j.row_scales[n / 32] = poison ? (uint8_t)0xFF : (uint8_t)(X + 127);
+  }
+}
 
+// Columnwise part of a 128 x 64 tile from the staged projection.
+__device__ __forceinline__ void col_work(const QuantJob& j, const unsigned char* ys, int64_t g, int64_t m0, int64_t k0,
+                                         int t) {
+  const int64_t M = j.M, K = j.K;
   // ---- columnwise (M % 32 == 0): warp w takes the 32-row block w / 2 and
   // column half w mod 2; lane l the column pair 16 (w mod 2) + (l mod 16)
   // and rows 16 (l / 16) .. + 15 of the block, read as bf16 pairs (the two
@@ -209,6 +201,28 @@ __global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t 
     *reinterpret_cast<uint4*>(j.col_codes + n + 16 * half) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     if (half == 0) j.col_scales[n / 32] = nan ? (uint8_t)0xFF : (uint8_t)(X + 127);
   }
+}
+
+template <bool IN_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t tiles_m, int64_t tiles_k) {
+  __shared__ __align__(16) unsigned char ys[XM * YS];  // projected tile, bf16
+  const int t = threadIdx.x;
+  const int64_t tile = blockIdx.x;
+  const int64_t tk = tile % tiles_k, tm = (tile / tiles_k) % tiles_m, g = tile / (tiles_k * tiles_m);
+  const int64_t m0 = tm * XM, k0 = tk * XK;
+  {
+    const int rr = t >> 1, rh = t & 1;
+    const int64_t m = m0 + rr, k = k0 + 32 * rh;
+    if (m < j.M && k < j.K) {
+      float v[32];
+      uint32_t amax;
+      load_block32<IN_BF16>(j.x, (g * j.M + m) * j.ld + k, v, amax);
+      row_work<OUT_BF16>(j, v, amax, g, m, k, rr, rh, ys);
+    }
+  }
+  if (!j.col_codes) return;
+  __syncthreads();
+  col_work(j, ys, g, m0, k0, t);
 }
 
 template <bool IN_BF16, bool OUT_BF16>
