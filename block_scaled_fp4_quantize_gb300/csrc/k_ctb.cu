@@ -5,7 +5,8 @@
 // training", "Technical design", outer and inner scales).
 //
 // A CTA of 256 threads walks 128 (M) x 64 (K) tiles of x; each tile arrives
-// by a 3-D tensor copy with the 128-byte swizzle, three tiles in flight.
+// by a 3-D tensor copy with the 128-byte swizzle, two tiles in flight per
+// CTA and four CTAs resident per SM.
 //
 //   Rowwise pass: thread t owns row t / 2 and the two 1 x 16 blocks of its
 //   half (t mod 2) of the 64 columns; four 16-byte shared loads, block maxima
