@@ -72,8 +72,31 @@ __device__ __forceinline__ uint32_t block_scale(const SM& sm, float am, Norm& n,
 // Rare path of normalize16 (tiny, subnormal or non-positive scales).
 __device__ __noinline__ float div_slow(float u, float S, bool pos) { return pos ? ieee_div(u, S) : signed_zero(u); }
 
+// |u| bits below which Markstein's remainder can underflow (2^-100)
+constexpr uint32_t kTinyElem = 0x0D800000u;
+
+// Elements 0 < |u| < 2^-100 of a block whose maximum is at least 2^-90 get
+// x' from div.rn.  With round-to-nearest they cannot matter: |x'| / a <=
+// 2^-10, so |t| = |x'| / s < 0.01 and the code is +-0 whichever x' is
+// taken (the dequantized value and the residual follow).  Stochastic
+// rounding compares t itself with a random threshold, so its callers pass
+// TINY = true.
+template <bool TINY>
+__device__ __forceinline__ void fix_tiny(const float (&u)[16], float (&x)[16], const Norm& n, uint32_t sgn) {
+  if (!TINY) return;
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) any |= abs_bits(u[i]) - 1u < kTinyElem - 1u;
+  if (any) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (abs_bits(u[i]) - 1u < kTinyElem - 1u) x[i] = ieee_div(bitsf(fbits(u[i]) ^ sgn), n.S);
+  }
+}
+
 // x' = u / S for a whole block: one block-uniform branch, the fast path two
 // values per instruction.
+template <bool TINY>
 __device__ __forceinline__ void normalize16(const float (&u)[16], float (&x)[16], const Norm& n) {
   if (n.none) {
 #pragma unroll
@@ -86,6 +109,7 @@ __device__ __forceinline__ void normalize16(const float (&u)[16], float (&x)[16]
       const uint64_t nu = pk2(bitsf(fbits(u[i]) ^ 0x80000000u), bitsf(fbits(u[i + 1]) ^ 0x80000000u));
       upk2(markstein2(nu, S2, NR2), x[i], x[i + 1]);
     }
+    fix_tiny<TINY>(u, x, n, 0u);
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = div_slow(u[i], n.S, n.pos);
@@ -95,12 +119,14 @@ __device__ __forceinline__ void normalize16(const float (&u)[16], float (&x)[16]
 // normalize16 from the NEGATED values nu = -u (bf16 inputs widen to -u in
 // one instruction, so the negation the sign-safe Markstein form needs costs
 // nothing); same results.  Not for mode none.
+template <bool TINY>
 __device__ __forceinline__ void normalize16_neg(const float (&nu)[16], float (&x)[16], const Norm& n) {
   if (n.fast) {
     const float nr = bitsf(fbits(n.r) ^ 0x80000000u);
     const uint64_t S2 = pk2(n.S, n.S), NR2 = pk2(nr, nr);
 #pragma unroll
     for (int i = 0; i < 16; i += 2) upk2(markstein2(pk2(nu[i], nu[i + 1]), S2, NR2), x[i], x[i + 1]);
+    fix_tiny<TINY>(nu, x, n, 0x80000000u);
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = div_slow(bitsf(fbits(nu[i]) ^ 0x80000000u), n.S, n.pos);
@@ -151,6 +177,70 @@ __device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, 
   }
 }
 
+
+// Per-block steps for a block the FMA division sequences cover
+// (fast_block below): `a` = RN(am / S) is already known and no step needs a
+// fallback.  OUTER: an outer scale applies; NEG: the values arrive negated.
+template <bool SR, bool UE5M3, bool OUTER, bool NEG>
+__device__ __forceinline__ uint32_t block_fast(const float4* tab, const float (&v)[16], float a, float S, float r,
+                                               uint64_t seed, uint32_t step, uint32_t orient, uint64_t n0,
+                                               uint32_t& w0, uint32_t& w1) {
+  const uint32_t sc = encode_scale<UE5M3>(div_bmr(a, bitsf(kSixHi), bitsf(kSixLo)));
+  const float4 T = tab[sc];
+  Norm n;
+  n.none = !OUTER;
+  n.S = S;
+  n.r = r;
+  n.pos = true;
+  n.fast = true;
+  float x[16], dq[16];
+  if (NEG) normalize16_neg<SR>(v, x, n);
+  else normalize16<SR>(v, x, n);
+  encode16<SR, false>(x, T, n, seed, step, orient, n0, w0, w1, dq);
+  return sc;
+}
+
+// A block is covered by block_fast when its outer scale S and 1 / S are
+// normal, its |u| maximum am is 0 or at least 2^-90 and a = RN(am / S) is
+// below 2^126: the conditions under which block_scale and normalize16 take
+// no fallback (am = 0 gives a = +0 and signed-zero quotients either way).
+// Returns a.
+__device__ __forceinline__ bool fast_block(float am, float S, float R, float& a) {
+  a = div_markstein(am, S, R);
+  return (fbits(S) - 0x00800000u) < 0x7F000000u && (fbits(R) - 0x00800000u) < 0x7F000000u &&
+         fbits(am) - 1u >= kTiny - 1u && fbits(a) < 0x7E800000u;
+}
+
+// Outer scale S = RN(A / (scale_max * 6)) and R = RN(1 / S), called by a
+// whole warp: when every lane's A is at least 2^-90, S lies in
+// [2^-110, 2^117] and both come from the FMA sequences; otherwise the warp
+// takes the general path.
+template <bool UE5M3>
+__device__ __forceinline__ void outer_sr(float A, float& S, float& R) {
+  if (__all_sync(0xFFFFFFFFu, fbits(A) >= kTiny)) {
+    S = div_bmr(A, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
+    R = rcp_markstein(S);
+  } else {
+    S = outer_scale<UE5M3>(A);
+    R = ieee_rcp(S);
+  }
+}
+
+// outer_sr for two outer blocks at once (one branch for both).
+template <bool UE5M3>
+__device__ __forceinline__ void outer_sr2(float A0, float A1, float (&S)[2], float (&R)[2]) {
+  if (__all_sync(0xFFFFFFFFu, fbits(A0) >= kTiny && fbits(A1) >= kTiny)) {
+    S[0] = div_bmr(A0, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
+    S[1] = div_bmr(A1, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
+    R[0] = rcp_markstein(S[0]);
+    R[1] = rcp_markstein(S[1]);
+  } else {
+    S[0] = outer_scale<UE5M3>(A0);
+    S[1] = outer_scale<UE5M3>(A1);
+    R[0] = ieee_rcp(S[0]);
+    R[1] = ieee_rcp(S[1]);
+  }
+}
 
 // max |u| over 16 values (NaN propagates), as a tree of magnitude maxima.
 __device__ __forceinline__ float amax_pair(float a, float b) {

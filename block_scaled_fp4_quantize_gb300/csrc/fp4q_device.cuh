@@ -171,6 +171,20 @@ __device__ __forceinline__ float ieee_rcp(float s) {
   return r;
 }
 
+// RN(1 / s) for 2^-125 <= s <= 2^125 without the special-case handling of
+// rcp.rn: the hardware approximation y, the residual e = RN(1 - s y) (exact:
+// it fits in 24 bits when y is within an ulp of 1 / s) and one correction
+// RN(y + e y) (Markstein's reciprocal refinement, same paper as
+// div_markstein).  Its agreement with rcp.rn.f32 is checked for every
+// binary32 of the range by tests/gpu_rcp_check.cu.
+__device__ __forceinline__ float rcp_markstein(float s) {
+  float r;
+  asm("{\n\t.reg .f32 y, e;\n\trcp.approx.ftz.f32 y, %1;\n\tneg.f32 e, %1;\n\t"
+      "fma.rn.f32 e, e, y, 0f3F800000;\n\tfma.rn.f32 %0, e, y, y;\n\t}"
+      : "=f"(r) : "f"(s));
+  return r;
+}
+
 // RN(u / S) from r = RN(1 / S) by Markstein's correction step (P. Markstein,
 // "Computation of elementary functions on the IBM RISC System/6000
 // processor", IBM J. Res. Dev. 34(1), 1990): q = RN(u r), e = RN(q S - u)

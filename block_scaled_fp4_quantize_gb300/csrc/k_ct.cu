@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
         float4 T;
         const uint32_t sc = block_scale<UE5M3>(tv, amq, n, T);
         float x[16];
-        normalize16(u, x, n);
+        normalize16<SR>(u, x, n);
         if (staged) stage_block<IN_BF16>(xs, row, b, x);
         if (j.do_row) {
           float deq[16];
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
         n.pos = positive(n.S);
         n.fast = positive_normal(n.S) && positive_normal(n.r);
         sc = block_scale<UE5M3>(tv, cam[q], n, T);
-        normalize16(v, x, n);
+        normalize16<SR>(v, x, n);
       }
       const int64_t n0 = cbase + (int64_t)col * M32 + rbeg + 16 * q;
       float deq[16];

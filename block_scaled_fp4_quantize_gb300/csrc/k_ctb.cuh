@@ -20,7 +20,10 @@ constexpr int CST = 72;             // bytes per staged column of codes (64 + 8 
 // Shared memory (offsets from the 1024-byte aligned base)
 struct BL {
   __host__ __device__ static constexpr int raw(int s) { return s * BRAW; }
-  static constexpr int tab = BNS * BRAW;               // 256 x (s, zh, zl, -)
+  // columnwise codes for the tensor store: 2 x [64 columns][64 bytes],
+  // 64-byte swizzle (1024-byte aligned)
+  __host__ __device__ static constexpr int ccs(int s) { return BNS * BRAW + s * 4096; }
+  static constexpr int tab = BNS * BRAW + 2 * 4096;    // 256 x (s, zh, zl, -)
   static constexpr int codes = tab + 256 * 16;         // 64 columns x CST
   static constexpr int scales = codes + 64 * CST;      // 64 columns x 8
   static constexpr int red2d = scales + 64 * 8;        // 32 x u32: 2-D sub-tile maxima
@@ -118,8 +121,8 @@ __device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (
   float4 T;
   const uint32_t sc = block_scale<UE5M3>(tv, am, n, T);
   float x[16], dq[16];
-  if (NEG) normalize16_neg(v, x, n);
-  else normalize16(v, x, n);
+  if (NEG) normalize16_neg<SR>(v, x, n);
+  else normalize16<SR>(v, x, n);
   encode16<SR, false>(x, T, n, j.seed, j.step, orient, n0, w0, w1, dq);
   return sc;
 }
@@ -140,7 +143,8 @@ struct GroupCursor {
 };
 
 template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
-__global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
+                                                          const __grid_constant__ CUtensorMap cmap, int col_tma) {
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -241,9 +245,12 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
       if (i < cur.ntiles) issue_bf16_tile(&tmap, tile_at(i), smem + BL::raw(s), &bars[s]);
     }
     cur.next();
+    // the columnwise store of two tiles ago has read its staging buffer
+    if (!GR && t == 0 && col_tma) bulk_wait_read_1();
     const bool arrived = mbar_wait(&bars[slot], phase, 1u << 22);
     if (!__syncthreads_and(arrived)) {
       if (t == 0) {
+        if (!GR && col_tma) bulk_wait_all();
         atomicExch(&g_ctb_timeout, 1u);
         for (int d = 1; d < BNS; ++d) {
           const int i = it + d;
@@ -334,11 +341,9 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
         uint32_t g0 = fbits(am[0]), g1 = fbits(am[1]);
         if (ob >= 32) g0 = g1 = umax(g0, g1);
         if (ob == 64) { g0 = umax(g0, __shfl_xor_sync(0xFFFFFFFFu, g0, 1)); g1 = g0; }
-        S[0] = outer_scale<UE5M3>(bitsf(g0));
-        R[0] = ieee_rcp(S[0]);
+        outer_sr<UE5M3>(bitsf(g0), S[0], R[0]);
         if (ob == 16) {
-          S[1] = outer_scale<UE5M3>(bitsf(g1));
-          R[1] = ieee_rcp(S[1]);
+          outer_sr<UE5M3>(bitsf(g1), S[1], R[1]);
         } else {
           S[1] = S[0];
           R[1] = R[0];
@@ -369,9 +374,17 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
         }
       }
       uint32_t cw[4], scw = 0;
+      // the fast form with RNE only (stochastic rounding is Philox-bound and
+      // keeps the general form's register budget)
+      float ab[2] = {am[0], am[1]};
+      bool fast = !SR;
+      if (!SR && BO != BO_NONE) {
 #pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        float u[16];  // u, or -u with an outer scale
+        for (int b = 0; b < 2; ++b) fast = fast_block(am[b], S[b], R[b], ab[b]) && fast;
+        fast = __all_sync(0xFFFFFFFFu, fast);
+      }
+      // block b of this thread as u (or -u with an outer scale)
+      auto row_u = [&](int b, float (&u)[16]) {
         const uint32_t wd[8] = {a[2 * b].x, a[2 * b].y, a[2 * b].z, a[2 * b].w,
                                 a[2 * b + 1].x, a[2 * b + 1].y, a[2 * b + 1].z, a[2 * b + 1].w};
 #pragma unroll
@@ -379,9 +392,26 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
           u[2 * i] = BO == BO_NONE ? bf16lo(wd[i]) : nbf16lo(wd[i]);
           u[2 * i + 1] = BO == BO_NONE ? bf16hi(wd[i]) : nbf16hi(wd[i]);
         }
-        const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, am[b], S[b], R[b], none, j, 0u,
-                                                                  (uint64_t)(rel + 16 * b), cw[2 * b], cw[2 * b + 1]);
-        scw |= sc << (8 * b);
+      };
+      if (fast) {  // one branch for both blocks: straight-line code the scheduler can interleave
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          float u[16];
+          row_u(b, u);
+          scw |= block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE>(tab, u, ab[b], S[b], R[b], j.seed, j.step, 0u,
+                                                                      (uint64_t)(rel + 16 * b), cw[2 * b],
+                                                                      cw[2 * b + 1])
+                 << (8 * b);
+        }
+      } else {
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          float u[16];
+          row_u(b, u);
+          scw |= quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, am[b], S[b], R[b], none, j, 0u,
+                                                       (uint64_t)(rel + 16 * b), cw[2 * b], cw[2 * b + 1])
+                 << (8 * b);
+        }
       }
       if (rvalid) {
         const int nb = (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
@@ -462,10 +492,9 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
 #pragma unroll
         for (int c = 0; c < 2; ++c) g[c] = redc[(2 * lane + c) * 4 + grp];
       }
+      outer_sr2<UE5M3>(bitsf(g[0]), bitsf(g[1]), S, R);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        S[c] = outer_scale<UE5M3>(bitsf(g[c]));
-        R[c] = ieee_rcp(S[c]);
         const int64_t k = p.k0 + 2 * lane + c;
         if (j.col_outer && k < K && mvalid && ((16 * warp) & (ob - 1)) == 0)
           j.col_outer[(cbase + k * cstride + mb) >> lob] = S[c];
@@ -488,21 +517,61 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
         R[c] = ieee_rcp(S[c]);
       }
     }
+    float ac[2] = {cam[0], cam[1]};
+    bool cfast = !SR;
+    if (!SR && BO != BO_NONE) {
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float u[16];  // u, or -u with an outer scale (the transformed z with RHT)
+      for (int c = 0; c < 2; ++c) cfast = fast_block(cam[c], S[c], R[c], ac[c]) && cfast;
+      cfast = __all_sync(0xFFFFFFFFu, cfast);
+    }
+    // column c of this lane as u (or -u with an outer scale; the transformed
+    // z with the Hadamard transform)
+    auto col_u = [&](int c, float (&u)[16]) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         u[i] = RHT ? (c ? z1[i] : z0[i])
                    : (BO == BO_NONE ? (c ? bf16hi(wv[i]) : bf16lo(wv[i])) : (c ? nbf16hi(wv[i]) : nbf16lo(wv[i])));
-      const int64_t k = p.k0 + 2 * lane + c;
-      uint32_t w0, w1;
-      const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE && !RHT>(tab, u, cam[c], S[c], R[c], none, j, 1u,
-                                                                         (uint64_t)(cbase + k * cstride + mb), w0, w1);
-      *reinterpret_cast<uint2*>(cst + (2 * lane + c) * CST + 8 * warp) = make_uint2(w0, w1);
+    };
+    // codes of column 2 lane + c, rows 16 warp .. + 15: row 2 lane + c of
+    // the tensor-store box at byte 8 warp, whose 16-byte chunk index the
+    // 64-byte swizzle XORs with (row / 2) mod 4 = lane mod 4; or the padded
+    // staging rows of the thread copy-out
+    unsigned char* cbuf = smem + BL::ccs(it & 1);
+    auto col_stage = [&](int c, uint32_t w0, uint32_t w1, uint32_t sc) {
+      if (!GR && col_tma)
+        *reinterpret_cast<uint2*>(cbuf + ((((2 * lane + c) << 6) + 8 * warp) ^ ((lane & 3) << 4))) = make_uint2(w0, w1);
+      else
+        *reinterpret_cast<uint2*>(cst + (2 * lane + c) * CST + 8 * warp) = make_uint2(w0, w1);
       sst[(2 * lane + c) * 8 + warp] = (uint8_t)sc;
+    };
+    if (cfast) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float u[16];
+        col_u(c, u);
+        uint32_t w0, w1;
+        const uint32_t sc = block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE && !RHT>(
+            tab, u, ac[c], S[c], R[c], j.seed, j.step, 1u, (uint64_t)(cbase + (p.k0 + 2 * lane + c) * cstride + mb),
+            w0, w1);
+        col_stage(c, w0, w1, sc);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float u[16];
+        col_u(c, u);
+        uint32_t w0, w1;
+        const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE && !RHT>(
+            tab, u, cam[c], S[c], R[c], none, j, 1u, (uint64_t)(cbase + (p.k0 + 2 * lane + c) * cstride + mb), w0, w1);
+        col_stage(c, w0, w1, sc);
+      }
     }
+    if (!GR && col_tma) fence_proxy_async();
     __syncthreads();
+    if (!GR && col_tma && t == 0) {  // the tile's columnwise codes: [64 columns][128 rows / 2] bytes
+      tma_store3(&cmap, cbuf, (int)(p.m0 >> 1), (int)p.k0, (int)p.g);
+      bulk_commit();
+    }
     if (BO == BO_T1D && ob > 16 && ((16 * warp) & (ob - 1)) == 0) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) redc[(2 * lane + c) * 4 + ((16 * warp) >> lob)] = 0u;
@@ -512,7 +581,7 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
       const int col = t >> 2, ch = t & 3;
       const int64_t k = p.k0 + col;
       const int64_t m1 = p.m0 + 32 * ch;
-      if (k < K && m1 < gend) {
+      if ((GR || !col_tma) && k < K && m1 < gend) {
         const int nb = (int)min((int64_t)2, (gend - m1) / 16);
         const uint2 c0 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch);
         const uint2 c1 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch + 8);
@@ -553,6 +622,7 @@ __global__ void __launch_bounds__(BT, RHT ? 3 : 4) ctb_kernel(const QuantJob j, 
     }
     __syncthreads();
   }
+  if (!GR && col_tma && t == 0) bulk_wait_all();
 }
 
 bool make_bf16_map(const QuantJob& j, CUtensorMap* map) {
@@ -567,8 +637,27 @@ bool make_bf16_map(const QuantJob& j, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map of the columnwise codes [G][K][M / 2] bytes for the tile
+// store (box: 64 columns x 64 bytes, 64-byte swizzle: the inner extent of
+// the box equals the swizzle span).  Needs 16-byte aligned rows (M a
+// multiple of 32) and a 16-byte aligned base; false when the codes leave by
+// the thread copy-out instead.
+bool make_col_map(const QuantJob& j, CUtensorMap* map) {
+  if (j.ngroups > 0 || !j.do_col || j.M % 32 || (reinterpret_cast<uintptr_t>(j.col_codes) & 15u)) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(j.M / 2), (cuuint64_t)j.K, (cuuint64_t)j.G};
+  const cuuint64_t strides[2] = {(cuuint64_t)(j.M / 2), (cuuint64_t)j.K * (cuuint64_t)(j.M / 2)};
+  const cuuint32_t box[3] = {64u, 64u, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, j.col_codes, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
-cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
+cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,
+                         cudaStream_t st) {
   auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT>;
   static int per_sm_cache[128] = {0};
   int dev = 0;
@@ -587,23 +676,25 @@ cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, cudaStream_t
   const int64_t tiles = j.ngroups > 0 ? ((j.M + BM - 1) / BM + j.ngroups) * ((j.K + BK - 1) / BK)
                                       : j.G * ((j.M + BM - 1) / BM) * ((j.K + BK - 1) / BK);
   const int64_t cap = (int64_t)num_sms() * per_sm;
-  kern<<<(int)(tiles < cap ? tiles : cap), BT, BL::total, st>>>(j, map);
+  kern<<<(int)(tiles < cap ? tiles : cap), BT, BL::total, st>>>(j, map, cmap, col_tma);
   return cudaGetLastError();
 }
 
 template <bool SR, bool UE5M3, bool GR, bool RHT>
-cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
+cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,
+                         cudaStream_t st) {
   if constexpr (RHT) {  // the transform is defined with no outer scale or 1-D outer blocks
-    if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true>(j, map, st);
-    return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, st);
+    if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true>(j, map, cmap, col_tma, st);
+    return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, cmap, col_tma, st);
   } else {
-    if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false>(j, map, st);
-    if (j.s_src == S_TENSORWISE_WS || j.mode == 1) return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false>(j, map, st);
+    if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false>(j, map, cmap, col_tma, st);
+    if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
+      return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false>(j, map, cmap, col_tma, st);
     if (j.s_src == S_IN_TILE)
-      return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false>(j, map, st)
-                        : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false>(j, map, st);
-    return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_B2D, GR, false>(j, map, st)
-                      : launch_ctb_t<SR, UE5M3, BO_B1D, GR, false>(j, map, st);
+      return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false>(j, map, cmap, col_tma, st)
+                        : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false>(j, map, cmap, col_tma, st);
+    return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_B2D, GR, false>(j, map, cmap, col_tma, st)
+                      : launch_ctb_t<SR, UE5M3, BO_B1D, GR, false>(j, map, cmap, col_tma, st);
   }
 }
 
@@ -611,12 +702,16 @@ cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, cudaStream_t
 // cannot be built.
 template <bool GR, bool RHT>
 bool launch_ctb_all(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
-  CUtensorMap map;
+  CUtensorMap map, cmap;
   if (!make_bf16_map(j, &map)) return false;
+  const int col_tma = make_col_map(j, &cmap) ? 1 : 0;
+  if (!col_tma) cmap = map;  // unused by the kernel
   if (j.sr)
-    *err = j.ue5m3 ? launch_ctb_o<true, true, GR, RHT>(j, map, st) : launch_ctb_o<true, false, GR, RHT>(j, map, st);
+    *err = j.ue5m3 ? launch_ctb_o<true, true, GR, RHT>(j, map, cmap, col_tma, st)
+                   : launch_ctb_o<true, false, GR, RHT>(j, map, cmap, col_tma, st);
   else
-    *err = j.ue5m3 ? launch_ctb_o<false, true, GR, RHT>(j, map, st) : launch_ctb_o<false, false, GR, RHT>(j, map, st);
+    *err = j.ue5m3 ? launch_ctb_o<false, true, GR, RHT>(j, map, cmap, col_tma, st)
+                   : launch_ctb_o<false, false, GR, RHT>(j, map, cmap, col_tma, st);
   return true;
 }
 

@@ -177,23 +177,30 @@ __global__ void __launch_bounds__(RT) row_kernel(const QuantJob j) {
       } else if (RO == RO_WARP) {
         uint32_t g = fbits(am);
         for (int o = 1; o < per; o <<= 1) g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
-        n.S = outer_scale<UE5M3>(bitsf(g));
-        n.r = ieee_rcp(n.S);
+        outer_sr<UE5M3>(bitsf(g), n.S, n.r);
         if (j.row_outer && j.do_row && valid[q] && (lane & (per - 1)) == 0) j.row_outer[b[q] >> lper] = n.S;
       } else if (RO == RO_BUFFER) {
         if (valid[q]) n.S = j.row_outer[per_pow2 ? (b[q] >> lper) : b[q] / per];
         n.r = ieee_rcp(n.S);
       }
-      n.pos = n.none || positive(n.S);
-      n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
-      float4 T;
-      const uint32_t sc = block_scale<UE5M3>(tv, am, n, T);
-      float x[16];
-      normalize16(u, x, n);
-      uint32_t w0, w1;
+      uint32_t sc, w0, w1;
       float dq[16];
-      if (deq) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, (uint64_t)(16 * b[q]), w0, w1, dq);
-      else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, (uint64_t)(16 * b[q]), w0, w1, dq);
+      // round-to-nearest quantize without dequantized values: the fast form
+      // when every lane's block is in its range (one warp-uniform branch)
+      float a = am;
+      const bool fast = !SR && !deq && __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
+      if (fast) {
+        sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, 0ull, 0u, 0u, 0ull, w0, w1);
+      } else {
+        n.pos = n.none || positive(n.S);
+        n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
+        float4 T;
+        sc = block_scale<UE5M3>(tv, am, n, T);
+        float x[16];
+        normalize16<SR>(u, x, n);
+        if (deq) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, (uint64_t)(16 * b[q]), w0, w1, dq);
+        else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, (uint64_t)(16 * b[q]), w0, w1, dq);
+      }
       if (!valid[q]) continue;
       if (j.row_codes) {
         *reinterpret_cast<uint2*>(j.row_codes + 8 * b[q]) = make_uint2(w0, w1);

@@ -224,6 +224,45 @@ def test_tensorwise_amax_special_values(orc, dtype, shape):
         assert_same(g, r)
 
 
+def _tiny_regions(shape, seed):
+    """Lognormal data with 16 x 16 regions scaled into the ranges where the
+    FMA division sequences do not apply (|u| below 2^-90, bf16 subnormals),
+    zeroed regions, and lone tiny or zero elements inside normal blocks."""
+    G, M, K = shape
+    g = torch.Generator("cpu").manual_seed(seed)
+    x = W.lognormal(shape, seed, sigma=1.5, dtype=torch.float32)
+    for scale in (2.0 ** -100, 2.0 ** -120, 2.0 ** -135, 0.0, 2.0 ** -60):
+        for _ in range(6):
+            i = int(torch.randint(0, M // 16, (1,), generator=g)) * 16
+            k = int(torch.randint(0, K // 16, (1,), generator=g)) * 16
+            x[:, i:i + 16, k:k + 16] *= scale
+    idx = torch.randint(0, G * M * K, (64,), generator=g)
+    x.view(-1)[idx[:32]] *= 2.0 ** -110
+    x.view(-1)[idx[32:]] = 0.0
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
+                                dict(mode="outer_block", outer_block_size=16),
+                                dict(mode="outer_block", outer_block_size=32),
+                                dict(mode="outer_block", outer_block_size=64),
+                                dict(mode="outer_block", outer_block_size=64, scale_format="ue5m3"),
+                                dict(mode="outer_block", outer_block_size=32, outer_2d=True),
+                                dict(mode="outer_block", outer_block_size=64, outer_2d=True)],
+                         ids=["none", "tensorwise", "ob16", "ob32", "ob64", "ob64-ue5m3", "ob32-2d", "ob64-2d"])
+def test_tiny_and_zero_blocks(orc, kw, kernel):
+    """Blocks and outer blocks whose maxima fall below the range of the fast
+    division sequences (and all-zero blocks) next to ordinary ones, so that
+    lanes of one warp take different paths: every orientation, RNE and SR."""
+    x = _tiny_regions((1, 256, 384), 41)
+    for mask in ((True, False), (False, True), (True, True)):
+        for stochastic in (False, True):
+            k = dict(kw, rowwise=mask[0], columnwise=mask[1], stochastic=stochastic, seed=5, step=9)
+            _, g = gpu_quantize(x, **k)
+            r = oracle_quantize(orc, x, **k)
+            assert_same(g, r)
+
+
 @pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
                                 dict(mode="outer_block", outer_block_size=16),
                                 dict(mode="outer_block", outer_block_size=64),
