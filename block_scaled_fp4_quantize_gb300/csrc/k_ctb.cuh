@@ -20,17 +20,21 @@ constexpr int CST = 72;             // bytes per staged column of codes (64 + 8 
 // Shared memory (offsets from the 1024-byte aligned base)
 struct BL {
   __host__ __device__ static constexpr int raw(int s) { return s * BRAW; }
-  // columnwise codes for the tensor store: 2 x [64 columns][64 bytes],
-  // 64-byte swizzle (1024-byte aligned)
+  // Staging of the columnwise codes, scales and 1-D outer maxima comes in
+  // two buffers picked by tile parity, so that one CTA barrier per tile
+  // separates a tile's writes from its readers and the next tile's writes.
+  // Codes: for the tensor store, [64 columns][64 bytes] with the 64-byte
+  // swizzle (ccs, 1024-byte aligned); for the thread copy-out, 64 columns x
+  // CST bytes (cst, the same region).
   __host__ __device__ static constexpr int ccs(int s) { return BNS * BRAW + s * 4096; }
-  static constexpr int tab = BNS * BRAW + 2 * 4096;    // 256 x (s, zh, zl, -)
-  static constexpr int codes = tab + 256 * 16;         // 64 columns x CST
-  static constexpr int scales = codes + 64 * CST;      // 64 columns x 8
-  static constexpr int red2d = scales + 64 * 8;        // 32 x u32: 2-D sub-tile maxima
-  static constexpr int redc = red2d + 32 * 4;          // 64 x 4 u32: column 1-D outer maxima
-  static constexpr int sr2d = redc + 256 * 4;          // 32 x (S, 1 / S)
-  static constexpr int bars = sr2d + 32 * 8;           // BNS mbarriers
-  static constexpr int total = bars + 8 * BNS + 1024;  // + alignment slack
+  __host__ __device__ static constexpr int cst(int s) { return BNS * BRAW + s * 64 * CST; }
+  static constexpr int tab = BNS * BRAW + 2 * 64 * CST;                     // 256 x (s, zh, zl, -)
+  __host__ __device__ static constexpr int scales(int s) { return tab + 256 * 16 + s * 512; }  // 64 x 8
+  static constexpr int red2d = tab + 256 * 16 + 2 * 512;                    // 32 x u32: 2-D sub-tile maxima
+  __host__ __device__ static constexpr int redc(int s) { return red2d + 128 + s * 1024; }  // 64 x 4 u32
+  static constexpr int sr2d = red2d + 128 + 2 * 1024;                       // 32 x (S, 1 / S)
+  static constexpr int bars = sr2d + 32 * 8;                                // BNS mbarriers
+  static constexpr int total = bars + 8 * BNS + 1024;                       // + alignment slack
 };
 
 // Outer-scale source of a launch
@@ -149,10 +153,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   float4* tab = reinterpret_cast<float4*>(smem + BL::tab);
-  unsigned char* cst = smem + BL::codes;
-  unsigned char* sst = smem + BL::scales;
   uint32_t* red2d = reinterpret_cast<uint32_t*>(smem + BL::red2d);
-  uint32_t* redc = reinterpret_cast<uint32_t*>(smem + BL::redc);
   float2* sr2d = reinterpret_cast<float2*>(smem + BL::sr2d);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BL::bars);
 
@@ -186,7 +187,8 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   }
   build_scale_table<UE5M3>(tab, t, BT);
   if (t < 32) red2d[t] = 0u;
-  redc[t] = 0u;
+  reinterpret_cast<uint32_t*>(smem + BL::redc(0))[t] = 0u;
+  reinterpret_cast<uint32_t*>(smem + BL::redc(1))[t] = 0u;
 
   const bool none = BO == BO_NONE;
   const int ob = j.ob;
@@ -221,6 +223,9 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   uint32_t phase = 0;
   for (int it = 0; cur.valid(); ++it) {
     const unsigned char* raw = smem + BL::raw(slot);
+    unsigned char* cst = smem + BL::cst(it & 1);
+    unsigned char* sst = smem + BL::scales(it & 1);
+    uint32_t* redc = reinterpret_cast<uint32_t*>(smem + BL::redc(it & 1));
     TilePos p = cur.pos<BM>();
     // the tile's group: rows [goff, gend), columnwise index of (k, m) =
     // cbase + k * cstride + m (the group's own [K, rows] transpose)
@@ -245,21 +250,11 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       if (i < cur.ntiles) issue_bf16_tile(&tmap, tile_at(i), smem + BL::raw(s), &bars[s]);
     }
     cur.next();
-    // the columnwise store of two tiles ago has read its staging buffer
-    if (!GR && t == 0 && col_tma) bulk_wait_read_1();
-    const bool arrived = mbar_wait(&bars[slot], phase, 1u << 22);
-    if (!__syncthreads_and(arrived)) {
-      if (t == 0) {
-        if (!GR && col_tma) bulk_wait_all();
-        atomicExch(&g_ctb_timeout, 1u);
-        for (int d = 1; d < BNS; ++d) {
-          const int i = it + d;
-          if (cur.idx + (d - 1) * (int)gridDim.x < cur.ntiles)
-            mbar_wait(&bars[i % BNS], (uint32_t)(i / BNS) & 1u, 1u << 22);
-        }
-      }
-      return;
-    }
+    // Each thread waits for the tile itself (no CTA barrier).  A wait that
+    // runs out raises the error flag and the walk goes on with whatever the
+    // slot holds: every later wait is bounded and every barrier is still
+    // reached by all threads.
+    if (!mbar_wait(&bars[slot], phase, 1u << 22)) atomicExch(&g_ctb_timeout, 1u);
     if (++slot == BNS) {
       slot = 0;
       phase ^= 1u;
@@ -567,6 +562,9 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       }
     }
     if (!GR && col_tma) fence_proxy_async();
+    // the previous tile's store has read its buffer, which the next tile's
+    // writers (past the barrier below) take over
+    if (!GR && col_tma && t == 0) bulk_wait_read_0();
     __syncthreads();
     if (!GR && col_tma && t == 0) {  // the tile's columnwise codes: [64 columns][128 rows / 2] bytes
       tma_store3(&cmap, cbuf, (int)(p.m0 >> 1), (int)p.k0, (int)p.g);
@@ -620,7 +618,6 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         }
       }
     }
-    __syncthreads();
   }
   if (!GR && col_tma && t == 0) bulk_wait_all();
 }
