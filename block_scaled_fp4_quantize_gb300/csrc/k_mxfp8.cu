@@ -49,6 +49,24 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 __device__ __forceinline__ float pow2f(int e) { return bitsf((uint32_t)(e + 127) << 23); }  // -126 <= e <= 127
 
+// Codes of a byte of two E2M1 values as binary16 pairs (exact), low nibble
+// in the low half.
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h) : "r"(byte));
+  return h;
+}
+
+// E4M3 bytes of a binary16 pair times 2^d (1 <= d <= 9: the products are
+// exact in binary16 and in E4M3), low half in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_f16x2_scaled(uint32_t h, uint32_t p2) {
+  uint32_t r;
+  asm("{\n\t.reg .b32 m;\n\t.reg .b16 t;\n\tmul.rn.f16x2 m, %1, %2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f16x2 t, m;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(r) : "r"(h), "r"(p2));
+  return r;
+}
+
 template <bool IN_BF16>
 __device__ __forceinline__ void load_block32(const void* x, int64_t idx, float (&v)[32], uint32_t& amax) {
   // 32 elements from element index idx (16-byte aligned)
@@ -94,24 +112,30 @@ __device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32]
   const int E = mx_exp(amax);
   const float inv = pow2f(-E), sc = E >= -126 ? pow2f(E) : 0.0f;
   uint32_t qb[16];  // E2M1 code bytes
-  uint32_t qmax = 0;
+  const uint64_t INV2 = pk2(inv, inv);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    qb[i] = e2m1x2_rne(ieee_mul(v[2 * i], inv), ieee_mul(v[2 * i + 1], inv));
-    qmax = umax(qmax, umax(qb[i] & 7u, (qb[i] >> 4) & 7u));
+    float a, b;
+    upk2(mul2(pk2(v[2 * i], v[2 * i + 1]), INV2), a, b);  // v 2^-E, two per instruction
+    qb[i] = e2m1x2_rne(a, b);
   }
+  // the largest code magnitude is the code of the block maximum (the
+  // rounding is monotone); for a poisoned block it is not used
+  const uint32_t qmax = e2m1x2_rne(ieee_mul(bitsf(amax), inv), 0.0f) & 7u;
   // projected values y = e2m1(q) 2^E (exact), recomputed from the codes
   // for each output so that no 32-value array stays live
   const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
   if (j.y || j.col_codes) {
 #pragma unroll
+    const uint64_t SC2 = pk2(sc, sc);
     for (int q = 0; q < 4; ++q) {
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float g0, g1;
         e2m1x2_decode(qb[4 * q + i], g0, g1);
-        w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(ieee_mul(g0, sc), ieee_mul(g1, sc));
+        upk2(mul2(pk2(g0, g1), SC2), g0, g1);
+        w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(g0, g1);
       }
       if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
         *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ (((rr >> 4) & 1) << 2)) << 4)) =
@@ -136,14 +160,14 @@ __device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32]
     const int fl = qmax <= 1u ? -1 : (int)(qmax >> 1) - 1;
     int X = qmax == 0u ? -127 : E + fl - 8;
     X = X < -127 ? -127 : X;
-    const float s2 = pow2f(E - X);  // 2^(E - X) in [2^1, 2^9]
+    // 2^(E - X) in [2^1, 2^9] as a binary16 pair; e2m1(q) 2^(E - X) is exact
+    // in binary16 and in E4M3
+    const uint32_t p2 = (uint32_t)(E - X + 15) << 10, P2 = p2 | (p2 << 16);
     uint32_t cw[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      float g[4];
-      e2m1x2_decode(qb[2 * i], g[0], g[1]);
-      e2m1x2_decode(qb[2 * i + 1], g[2], g[3]);
-      cw[i] = e4m3x2(ieee_mul(g[0], s2), ieee_mul(g[1], s2)) | (e4m3x2(ieee_mul(g[2], s2), ieee_mul(g[3], s2)) << 16);
+      cw[i] = e4m3x2_f16x2_scaled(e2m1x2_f16x2(qb[2 * i]), P2) |
+              (e4m3x2_f16x2_scaled(e2m1x2_f16x2(qb[2 * i + 1]), P2) << 16);
       if (poison) cw[i] = 0x7F7F7F7Fu;
     }
     uint4* d = reinterpret_cast<uint4*>(j.row_codes + n);
@@ -188,13 +212,16 @@ __device__ __forceinline__ void col_work(const QuantJob& j, const unsigned char*
     int X = ex == 0 ? -127 : ex - 127 - 8;
     X = X < -127 ? -127 : X;
     const float inv = pow2f(-X);
+    const uint64_t INV2 = pk2(inv, inv);
     uint32_t cw[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float v[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[e] = c ? bf16hi(wv[4 * i + e]) : bf16lo(wv[4 * i + e]);
-      cw[i] = e4m3x2(ieee_mul(v[0], inv), ieee_mul(v[1], inv)) | (e4m3x2(ieee_mul(v[2], inv), ieee_mul(v[3], inv)) << 16);
+      upk2(mul2(pk2(v[0], v[1]), INV2), v[0], v[1]);  // v 2^-X, two per instruction
+      upk2(mul2(pk2(v[2], v[3]), INV2), v[2], v[3]);
+      cw[i] = e4m3x2(v[0], v[1]) | (e4m3x2(v[2], v[3]) << 16);
       if (nan) cw[i] = 0x7F7F7F7Fu;
     }
     const int64_t n = (g * K + k + c) * M + mb;  // block start in the [G, K, M] columnwise outputs
