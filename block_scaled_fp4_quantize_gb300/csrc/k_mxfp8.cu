@@ -30,7 +30,12 @@ namespace {
 
 constexpr int XT = 256;
 constexpr int XM = 128, XK = 64;
-constexpr int YS = XK * 2;  // staged row stride in bytes; 16-byte units XOR-swizzled by bit 4 of the row
+// staged row stride in bytes; 16-byte unit u of row r sits at unit
+// u ^ swz(r), swz(r) = (r mod 8) ^ 4 ((r / 16) mod 2): the rowwise stores of
+// four consecutive rows and the columnwise loads of rows r and r + 16 both
+// spread over all banks
+constexpr int YS = XK * 2;
+__device__ __forceinline__ int ys_swz(int r) { return (r & 7) ^ (((r >> 4) & 1) << 2); }
 
 // MXFP4 block exponent (see k_mxfp4.cu): least E with 6 * 2^E >= max(A, 6 * 2^-126), capped at 125.
 __device__ __forceinline__ int mx_exp(uint32_t amax_bits) {
@@ -138,7 +143,7 @@ __device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32]
         w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(g0, g1);
       }
       if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
-        *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ (((rr >> 4) & 1) << 2)) << 4)) =
+        *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ ys_swz(rr)) << 4)) =
             make_uint4(w[0], w[1], w[2], w[3]);
       if (j.y && OUT_BF16) reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n)[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -194,9 +199,11 @@ __device__ __forceinline__ void col_work(const QuantJob& j, const unsigned char*
   const bool valid = k < K && mb < M;  // K % 32 == 0: both columns or neither
   uint32_t wv[16];
   {
-    const unsigned char* base = ys + (32 * rb + 16 * half) * YS + (((col0 >> 3) ^ (half << 2)) << 4) + (col0 & 7) * 2;
+    // row 32 rb + 16 half + i: swz = (i mod 8) ^ 4 half
+    const unsigned char* base = ys + (32 * rb + 16 * half) * YS + (col0 & 7) * 2;
+    const int cu = (col0 >> 3) ^ (half << 2);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(base + i * YS);
+    for (int i = 0; i < 16; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(base + i * YS + ((cu ^ (i & 7)) << 4));
   }
   uint32_t mx = bf16x2_amax(wv[0], wv[1]);
 #pragma unroll
