@@ -37,7 +37,7 @@ __device__ __forceinline__ float outer_scale(float A) {
 
 template <bool UE5M3>
 __device__ __forceinline__ uint32_t encode_scale(float v) {
-  if (UE5M3) return enc_scale(v, scale_fmt(1));
+  if (UE5M3) return enc_ue5m3(v);
   return enc_e4m3_hw(v);
 }
 

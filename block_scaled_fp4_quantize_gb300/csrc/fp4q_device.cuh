@@ -93,6 +93,24 @@ __device__ __forceinline__ uint32_t enc_scale(float v, const ScaleFmt& f) {
   return code < f.maxcode ? code : f.maxcode;
 }
 
+// UE5M3 code of v >= 0 (finite): enc_scale with the UE5M3 format in fewer
+// steps.  Normal range (v >= 2^-14): round the binary32 significand to 3
+// bits, ties to even, on the bit pattern (a carry moves into the exponent)
+// and rebias the exponent from 127 to 15.  Subnormal range: m = RN(v 2^17)
+// from one FMA onto 2^23 (v 2^17 < 8 is exact, the sum rounds to an
+// integer with ties to even); m = 8 is the smallest normal code.  Saturates
+// at 0xFE.  Equal to enc_scale for every finite v >= 0
+// (tests/gpu_scale_check.cu).
+__device__ __forceinline__ uint32_t enc_ue5m3(float v) {
+  const uint32_t b = fbits(v);
+  const uint32_t r = (b + 0x7FFFFu + ((b >> 20) & 1u)) >> 20;
+  const uint32_t n = r - ((127u - 15u) << 3);
+  float s;
+  asm("fma.rn.f32 %0, %1, 0f48000000, 0f4B000000;" : "=f"(s) : "f"(v));
+  const uint32_t code = b < 0x38800000u ? (fbits(s) & 0xFu) : n;
+  return code < 0xFEu ? code : 0xFEu;
+}
+
 __device__ __forceinline__ float dec_scale(uint32_t c, const ScaleFmt& f) {
   const uint32_t e = c >> 3, m = c & 7u;
   if (e == 0) return ieee_mul((float)m, bitsf((uint32_t)(127 - 2 - f.bias) << 23));

@@ -1,6 +1,6 @@
 // Exhaustive check of rcp_markstein against the IEEE reciprocal rcp.rn.f32
 // for every binary32 s with 2^-125 <= s <= 2^125, both signs (test
-// infrastructure: built and run by tests/test_gpu_rcp.py).
+// infrastructure: built and run by tests/test_gpu_device_numerics.py).
 //
 // Prints "checked N mismatches M" and, for the first mismatches, the input
 // bits with both results; exits 0 when the run completed (whatever M is).

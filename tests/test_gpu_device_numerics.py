@@ -1,0 +1,44 @@
+"""Exhaustive checks of device numerics that replace a general routine with
+a shorter one, each a small CUDA program built here:
+
+- rcp_markstein (RN(1 / S) from the hardware reciprocal approximation and
+  one Markstein correction) against rcp.rn.f32 for every binary32 of the
+  range the kernels use (2^-125 .. 2^125, both signs);
+- enc_ue5m3 against the general scale encoder with the UE5M3 format for
+  every finite binary32 v >= 0.
+
+Each requires no mismatch."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(ROOT, "block_scaled_fp4_quantize_gb300", "csrc")
+
+
+def _run_check(tmp_path, name):
+    exe = str(tmp_path / name)
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-I", CSRC,
+                    os.path.join(HERE, name + ".cu"), "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stdout + out.stderr
+    m = re.search(r"checked (\d+) mismatches (\d+)", out.stdout)
+    assert m, out.stdout
+    return int(m.group(1)), int(m.group(2)), out.stdout
+
+
+@pytest.mark.gpu
+def test_rcp_markstein_matches_ieee_reciprocal(tmp_path):
+    n, bad, log = _run_check(tmp_path, "gpu_rcp_check")
+    assert n == 2 * (0x7E000000 - 0x01000000 + 1)
+    assert bad == 0, log
+
+
+@pytest.mark.gpu
+def test_enc_ue5m3_matches_general_encoder(tmp_path):
+    n, bad, log = _run_check(tmp_path, "gpu_scale_check")
+    assert n == 0x7F800000
+    assert bad == 0, log
