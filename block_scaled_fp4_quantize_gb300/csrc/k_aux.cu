@@ -1,6 +1,7 @@
 // k_aux.cu -- tensorwise amax, outer-scale pre-pass and dequantize kernels.
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
+#include "fp4q_tma.cuh"
 
 namespace fp4q {
 namespace {
@@ -101,6 +102,7 @@ __device__ __forceinline__ void amax_unit(const uint4 w, const float* res, uint3
 // iteration, a scalar tail, one atomicMax per CTA.
 template <bool IN_BF16, bool RES>
 __global__ void __launch_bounds__(256) tensor_amax_flat_kernel(const QuantJob j, uint32_t* amax) {
+  pdl_wait_then_release();
   __shared__ uint32_t sh[8];
   constexpr int EPV = IN_BF16 ? 8 : 4;
   const int64_t n = j.G * j.M * j.K;
@@ -375,14 +377,9 @@ cudaError_t launch_tensor_amax(const QuantJob& j, uint32_t* amax_ws, cudaStream_
                     (!j.residual || vec_aligned(j.residual, 0));
   if (flat) {
     const int grid = grid_for(n / (j.in_bf16 ? 8 : 4) / 4 + 1, 256, 4);
-    if (j.in_bf16) {
-      if (j.residual) tensor_amax_flat_kernel<true, true><<<grid, 256, 0, st>>>(j, amax_ws);
-      else tensor_amax_flat_kernel<true, false><<<grid, 256, 0, st>>>(j, amax_ws);
-    } else {
-      if (j.residual) tensor_amax_flat_kernel<false, true><<<grid, 256, 0, st>>>(j, amax_ws);
-      else tensor_amax_flat_kernel<false, false><<<grid, 256, 0, st>>>(j, amax_ws);
-    }
-    return cudaGetLastError();
+    auto kern = j.in_bf16 ? (j.residual ? tensor_amax_flat_kernel<true, true> : tensor_amax_flat_kernel<true, false>)
+                          : (j.residual ? tensor_amax_flat_kernel<false, true> : tensor_amax_flat_kernel<false, false>);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), 0, st, j, amax_ws);
   }
   tensor_amax_kernel<<<grid_for(n, 256, 8), 256, 0, st>>>(j, amax_ws);
   return cudaGetLastError();

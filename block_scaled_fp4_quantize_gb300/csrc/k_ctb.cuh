@@ -149,6 +149,7 @@ struct GroupCursor {
 template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
 __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                           const __grid_constant__ CUtensorMap cmap, int col_tma) {
+  pdl_wait_then_release();
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -673,8 +674,8 @@ cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtens
   const int64_t tiles = j.ngroups > 0 ? ((j.M + BM - 1) / BM + j.ngroups) * ((j.K + BK - 1) / BK)
                                       : j.G * ((j.M + BM - 1) / BM) * ((j.K + BK - 1) / BK);
   const int64_t cap = (int64_t)num_sms() * per_sm;
-  kern<<<(int)(tiles < cap ? tiles : cap), BT, BL::total, st>>>(j, map, cmap, col_tma);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(BT), (size_t)BL::total, st, j, map, cmap,
+                    col_tma);
 }
 
 template <bool SR, bool UE5M3, bool GR, bool RHT>

@@ -16,6 +16,7 @@
 #include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
+#include "fp4q_tma.cuh"
 
 namespace fp4q {
 namespace {
@@ -104,6 +105,7 @@ struct TabView {
 
 template <bool IN_BF16, bool SR, bool UE5M3, int RO>
 __global__ void __launch_bounds__(RT) row_kernel(const QuantJob j) {
+  pdl_wait_then_release();
   __shared__ float4 tab[256];
   build_scale_table<UE5M3>(tab, threadIdx.x, RT);
   const TabView tv{tab};
@@ -252,8 +254,7 @@ cudaError_t launch_row_t(const QuantJob& j, cudaStream_t st) {
   const int64_t nblk = j.G * j.M * j.K / 16;
   const int64_t need = (nblk + RT * RU - 1) / (RT * RU);
   const int64_t cap = (int64_t)num_sms() * per_sm;
-  kern<<<(int)(need < cap ? need : cap), RT, 0, st>>>(j);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)(need < cap ? need : cap)), dim3(RT), 0, st, j);
 }
 
 template <bool IN_BF16, bool SR, bool UE5M3>
