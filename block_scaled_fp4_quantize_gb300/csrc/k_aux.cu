@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(256) outer_2d_kernel(const QuantJob j) {
 // microblock, two in flight per thread; OUTER: 0 none, 1 one scale, 2 1-D.
 template <bool OUT_BF16, int OUTER>
 __global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
+  pdl_wait_then_release();
   const ScaleFmt f = scale_fmt(j.ue5m3);
   const int64_t nmb = j.G * j.R * (j.C / 16);
   const int lob = j.ob > 0 ? 31 - __clz(j.ob) : 0;
@@ -423,16 +424,12 @@ cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st) {
   const int vec = vec_aligned(j.y, 16);
   if (vec && !j.sl.mma && !(j.mode == 2 && j.outer_2d) && (reinterpret_cast<uintptr_t>(j.codes) & 7u) == 0) {
     const int grid = grid_for((nmb + 1) / 2, 256, 8);
-    if (j.out_bf16) {
-      if (j.mode == 0) dequant_flat_kernel<true, 0><<<grid, 256, 0, st>>>(j);
-      else if (j.mode == 1) dequant_flat_kernel<true, 1><<<grid, 256, 0, st>>>(j);
-      else dequant_flat_kernel<true, 2><<<grid, 256, 0, st>>>(j);
-    } else {
-      if (j.mode == 0) dequant_flat_kernel<false, 0><<<grid, 256, 0, st>>>(j);
-      else if (j.mode == 1) dequant_flat_kernel<false, 1><<<grid, 256, 0, st>>>(j);
-      else dequant_flat_kernel<false, 2><<<grid, 256, 0, st>>>(j);
-    }
-    return cudaGetLastError();
+    void (*kern)(const DequantJob) =
+        j.out_bf16 ? (j.mode == 0 ? dequant_flat_kernel<true, 0> : j.mode == 1 ? dequant_flat_kernel<true, 1>
+                                                                                 : dequant_flat_kernel<true, 2>)
+                   : (j.mode == 0 ? dequant_flat_kernel<false, 0> : j.mode == 1 ? dequant_flat_kernel<false, 1>
+                                                                                  : dequant_flat_kernel<false, 2>);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), 0, st, j);
   }
   const int grid = grid_for(nmb, 256, 8);
   if (j.out_bf16) dequant_kernel<true><<<grid, 256, 0, st>>>(j, vec);

@@ -24,6 +24,7 @@
 //     maxima meet with one shuffle.
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
+#include "fp4q_tma.cuh"
 
 namespace fp4q {
 namespace {
@@ -131,8 +132,8 @@ __device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32]
   // for each output so that no 32-value array stays live
   const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
   if (j.y || j.col_codes) {
-#pragma unroll
     const uint64_t SC2 = pk2(sc, sc);
+#pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint32_t w[4];
 #pragma unroll
@@ -239,6 +240,7 @@ __device__ __forceinline__ void col_work(const QuantJob& j, const unsigned char*
 
 template <bool IN_BF16, bool OUT_BF16>
 __global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t tiles_m, int64_t tiles_k) {
+  pdl_wait_then_release();
   __shared__ __align__(16) unsigned char ys[XM * YS];  // projected tile, bf16
   const int t = threadIdx.x;
   const int64_t tile = blockIdx.x;
@@ -262,8 +264,8 @@ __global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t 
 template <bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_t(const QuantJob& j, cudaStream_t st) {
   const int64_t tiles_m = (j.M + XM - 1) / XM, tiles_k = (j.K + XK - 1) / XK;
-  mxfp8_kernel<IN_BF16, OUT_BF16><<<(unsigned)(j.G * tiles_m * tiles_k), XT, 0, st>>>(j, tiles_m, tiles_k);
-  return cudaGetLastError();
+  return launch_pdl(mxfp8_kernel<IN_BF16, OUT_BF16>, dim3((unsigned)(j.G * tiles_m * tiles_k)), dim3(XT), 0, st, j,
+                    tiles_m, tiles_k);
 }
 
 }  // namespace
