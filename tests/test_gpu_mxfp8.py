@@ -58,3 +58,10 @@ def test_rowwise_only_any_rows(orc):
     _check(orc, x, columnwise=False)
     with pytest.raises(fq.FP4QError):
         fq.mxfp4_project_mxfp8(x.cuda(), columnwise=True)  # M % 32 != 0
+
+
+def test_more_tiles_than_resident_ctas(orc):
+    # 2 x 16 x 33 = 1056 tiles of 128 x 64, more than one wave of resident
+    # CTAs, with a half-filled last tile column
+    x = W.lognormal((2, 2048, 2080), 83, sigma=4.0)
+    _check(orc, x)
