@@ -157,3 +157,16 @@ def lognormal(shape, seed, sigma=2.0, dtype=torch.bfloat16):
     mag = torch.exp(torch.randn(*shape, generator=g) * sigma)
     sgn = torch.where(torch.rand(*shape, generator=g) < 0.5, -1.0, 1.0)
     return (mag * sgn).to(dtype)
+
+
+def large_rows(M, K, seed, device="cuda", chunk_rows=16384):
+    """bf16 [M, K] on ``device``: row r ~ N(0, 1) * 2^((r mod 16) - 8), drawn
+    in slabs of ``chunk_rows`` rows from one generator seeded ``seed`` (for
+    tensors too large to build on the host)."""
+    g = torch.Generator(device).manual_seed(seed)
+    x = torch.empty(M, K, dtype=torch.bfloat16, device=device)
+    for r0 in range(0, M, chunk_rows):
+        r1 = min(M, r0 + chunk_rows)
+        sc = torch.exp2(torch.arange(r0, r1, device=device, dtype=torch.float32).remainder(16) - 8.0)
+        x[r0:r1] = (torch.randn(r1 - r0, K, generator=g, device=device, dtype=torch.float32) * sc[:, None]).to(torch.bfloat16)
+    return x
