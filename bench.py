@@ -232,11 +232,13 @@ def _extra_workloads():
 
     def dequantize_activations(iters, warmup, opts):
         x = W.activations().to(dev)
-        qd = fq.quantize(x, mode="outer_block", outer_block_size=64)
-        yd = torch.empty(1, M, K, dtype=torch.bfloat16, device=dev)
-        ms = _events_time(lambda i: fq.dequantize(qd, "row", torch.bfloat16, out=yd), iters, warmup)
-        return ("codes+scales+S of bf16[16384,2880] -> bf16", codes + M * K // 16 + M * K // 64 * 4 + M * K * 2,
-                ms, 1)
+        nb = codes + M * K // 16 + M * K // 64 * 4 + M * K * 2
+        # rotating sets of (codes, scales, S) and outputs, together above L2
+        qds = [fq.quantize(x, mode="outer_block", outer_block_size=64) for _ in range(_sets_for(nb))]
+        yds = [torch.empty(1, M, K, dtype=torch.bfloat16, device=dev) for _ in qds]
+        ms = _events_time(lambda i: fq.dequantize(qds[i % len(qds)], "row", torch.bfloat16, out=yds[i % len(qds)]),
+                          iters, warmup)
+        return "codes+scales+S of bf16[16384,2880] -> bf16", nb, ms, 1
 
     def _moe(fmt):
         def run(iters, warmup, opts):
