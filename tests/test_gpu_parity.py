@@ -151,6 +151,28 @@ def test_dequantize_matrix(orc, kw, orient, out_dtype):
     assert_same({"y": host_np(y)}, {"y": ref})
 
 
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"),
+                                dict(mode="outer_block", outer_block_size=16),
+                                dict(mode="outer_block", outer_block_size=48, scale_format="ue5m3")],
+                         ids=["none", "tensorwise", "ob16", "ob48-ue5m3"])
+@pytest.mark.parametrize("shape", [(1, 37, 48), (3, 5, 16), (1, 1, 32)], ids=["37x48", "3x5x16", "1x32"])
+def test_dequantize_ragged_counts(orc, kw, shape, out_dtype):
+    """Microblock counts that are not a multiple of four (111, 15 and 2): the
+    wide flat kernel's last microblocks go one per thread."""
+    G, M, K = shape
+    if kw.get("outer_block_size", 16) > K:
+        pytest.skip("outer block wider than the row")
+    x = W.lognormal(shape, 26, sigma=2.5)
+    q, g = gpu_quantize(x, rowwise=True, columnwise=False, **kw)
+    y = fq.dequantize(q, orient="row", out_dtype=out_dtype)
+    okw = oracle_kw(kw)
+    ref = orc.dequantize(g["row_codes"], g["row_scales"], g, G=G, M=M, K=K, orient=ROW,
+                         out_dtype="bf16" if out_dtype == torch.bfloat16 else "fp32",
+                         mode=okw["mode"], ob=okw["ob"], outer_2d=False, fmt=okw["fmt"])
+    assert_same({"y": host_np(y)}, {"y": ref})
+
 def test_precomputed_outer_scale_round_trip(orc):
     x = W.activations(M=128, K=256, n_cols=2, n_rows=1)
     for kw in (dict(mode="outer_block", outer_block_size=64, outer_2d=True),
