@@ -42,3 +42,21 @@ def test_enc_ue5m3_matches_general_encoder(tmp_path):
     n, bad, log = _run_check(tmp_path, "gpu_scale_check")
     assert n == 0x7F800000
     assert bad == 0, log
+
+
+@pytest.mark.gpu
+def test_hardware_encoders_match_the_oracle(tmp_path, orc):
+    """The E2M1 (cvt.rn.satfinite.e2m1x2.f32) and E4M3 scale
+    (cvt.rn.satfinite.e4m3x2.f32) conversions against the oracle's encoders
+    for every finite binary32 >= 0, and the E2M1 sign rule on the device."""
+    so = orc.build()
+    exe = str(tmp_path / "gpu_encoder_check")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I", CSRC,
+                    os.path.join(HERE, "gpu_encoder_check.cu"), "-o", exe, "-L", os.path.dirname(so), "-lorc",
+                    "-Xlinker", "-rpath=" + os.path.dirname(so)], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stdout + out.stderr
+    m = re.search(r"checked (\d+) mismatches (\d+)", out.stdout)
+    assert m, out.stdout
+    assert int(m.group(1)) == 2 * 0x7F800000
+    assert int(m.group(2)) == 0, out.stdout
