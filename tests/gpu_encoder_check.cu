@@ -9,10 +9,13 @@
 //     code(-t) == code(t) | 8 (the sign bit kept, -0 included);
 //   - enc_e4m3_hw (cvt.rn.satfinite.e4m3x2.f32): the E4M3 scale code of
 //     every finite binary32 v >= 0 against orc_scale_encode in the E4M3
-//     format (nearest, ties to the even code, saturation at 448).
+//     format (nearest, ties to the even code, saturation at 448);
+//   - e2m1_sr (the branch-free stochastic rounding): the E2M1 code of every
+//     binary32 t in [0, 8] with the random word w = hash(t) against
+//     orc_e2m1_sr, and code(-t, w) == code(t, w) | 8 on the device.
 //
-// Prints "checked N mismatches M" (N = both encoders over all 0x7F800000
-// patterns) and the first mismatches; exits 0 when the run completed.
+// Prints "checked N mismatches M" (N = 2 x 0x7F800000 + 0x41000001 codes)
+// and the first mismatches; exits 0 when the run completed.
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -26,8 +29,13 @@
 
 extern "C" uint8_t orc_e2m1_rne(double t);
 extern "C" uint8_t orc_scale_encode(int fmt, float v);
+extern "C" uint8_t orc_e2m1_sr(double t, uint32_t w);
 
 constexpr uint32_t kN = 0x7F800000u;  // every finite binary32 >= 0 (bit patterns 0 .. 0x7F7FFFFF)
+constexpr uint32_t kS = 0x41000001u;  // binary32 0 .. 8
+
+// the random word of pattern b (a multiplicative hash)
+__host__ __device__ inline uint32_t word_of(uint32_t b) { return (b * 2654435761u) ^ 0x5BD1E995u; }
 
 __global__ void encode_all(uint8_t* e2, uint8_t* e4, unsigned long long* asym) {
   for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < kN; b += gridDim.x * blockDim.x) {
@@ -40,32 +48,43 @@ __global__ void encode_all(uint8_t* e2, uint8_t* e4, unsigned long long* asym) {
   }
 }
 
+__global__ void round_sr_all(uint8_t* sr, unsigned long long* asym) {
+  for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < kS; b += gridDim.x * blockDim.x) {
+    const uint32_t w = word_of(b);
+    const uint32_t c = fp4q::e2m1_sr(fp4q::bitsf(b), w);
+    if (fp4q::e2m1_sr(fp4q::bitsf(b | 0x80000000u), w) != (c | 8u)) atomicAdd(asym, 1ull);
+    sr[b] = (uint8_t)c;
+  }
+}
+
 int main() {
-  uint8_t *d2 = nullptr, *d4 = nullptr;
+  uint8_t *d2 = nullptr, *d4 = nullptr, *ds = nullptr;
   unsigned long long* dasym = nullptr;
-  if (cudaMalloc(&d2, kN) != cudaSuccess || cudaMalloc(&d4, kN) != cudaSuccess ||
+  if (cudaMalloc(&d2, kN) != cudaSuccess || cudaMalloc(&d4, kN) != cudaSuccess || cudaMalloc(&ds, kS) != cudaSuccess ||
       cudaMalloc(&dasym, sizeof(*dasym)) != cudaSuccess) {
     std::printf("cuda alloc failed\n");
     return 2;
   }
   cudaMemset(dasym, 0, sizeof(*dasym));
   encode_all<<<152 * 8, 256>>>(d2, d4, dasym);
+  round_sr_all<<<152 * 8, 256>>>(ds, dasym);
   if (cudaDeviceSynchronize() != cudaSuccess) {
     std::printf("kernel failed\n");
     return 2;
   }
-  std::vector<uint8_t> e2(kN), e4(kN);
+  std::vector<uint8_t> e2(kN), e4(kN), esr(kS);
   unsigned long long asym = 0;
   if (cudaMemcpy(e2.data(), d2, kN, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(e4.data(), d4, kN, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(esr.data(), ds, kS, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(&asym, dasym, sizeof(asym), cudaMemcpyDeviceToHost) != cudaSuccess) {
     std::printf("copy failed\n");
     return 2;
   }
   // the oracle over the same patterns, in slices across the host's cores
   const unsigned nt = std::thread::hardware_concurrency() ? std::thread::hardware_concurrency() : 4;
-  std::vector<unsigned long long> bad2(nt, 0), bad4(nt, 0);
-  std::vector<uint32_t> first2(nt, 0xFFFFFFFFu), first4(nt, 0xFFFFFFFFu);
+  std::vector<unsigned long long> bad2(nt, 0), bad4(nt, 0), bads(nt, 0);
+  std::vector<uint32_t> first2(nt, 0xFFFFFFFFu), first4(nt, 0xFFFFFFFFu), firsts(nt, 0xFFFFFFFFu);
   std::vector<std::thread> pool;
   for (unsigned k = 0; k < nt; ++k) {
     pool.emplace_back([&, k] {
@@ -79,17 +98,22 @@ int main() {
         if (e4[b] != orc_scale_encode(0, v)) {
           if (bad4[k]++ == 0) first4[k] = b;
         }
+        if (b < kS && esr[b] != orc_e2m1_sr((double)v, word_of(b))) {
+          if (bads[k]++ == 0) firsts[k] = b;
+        }
       }
     });
   }
   for (auto& th : pool) th.join();
-  unsigned long long m2 = 0, m4 = 0;
+  unsigned long long m2 = 0, m4 = 0, ms = 0;
   for (unsigned k = 0; k < nt; ++k) {
     m2 += bad2[k];
     m4 += bad4[k];
+    ms += bads[k];
   }
-  std::printf("checked %llu mismatches %llu\n", 2ull * kN, m2 + m4 + asym);
-  std::printf("e2m1 mismatches %llu, e2m1 sign asymmetries %llu, e4m3 mismatches %llu\n", m2, asym, m4);
+  std::printf("checked %llu mismatches %llu\n", 2ull * kN + kS, m2 + m4 + ms + asym);
+  std::printf("e2m1 mismatches %llu, sign asymmetries %llu, e4m3 mismatches %llu, sr mismatches %llu\n", m2, asym,
+              m4, ms);
   for (unsigned k = 0; k < nt; ++k) {
     if (first2[k] != 0xFFFFFFFFu) {
       float v;
@@ -100,6 +124,12 @@ int main() {
       float v;
       std::memcpy(&v, &first4[k], 4);
       std::printf("e4m3 v=%08x device=%02x oracle=%02x\n", first4[k], e4[first4[k]], orc_scale_encode(0, v));
+    }
+    if (firsts[k] != 0xFFFFFFFFu) {
+      float v;
+      std::memcpy(&v, &firsts[k], 4);
+      std::printf("sr t=%08x w=%08x device=%x oracle=%x\n", firsts[k], word_of(firsts[k]), esr[firsts[k]],
+                  orc_e2m1_sr((double)v, word_of(firsts[k])));
     }
   }
   return 0;
