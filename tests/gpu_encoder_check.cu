@@ -12,10 +12,14 @@
 //     format (nearest, ties to the even code, saturation at 448);
 //   - e2m1_sr (the branch-free stochastic rounding): the E2M1 code of every
 //     binary32 t in [0, 8] with the random word w = hash(t) against
-//     orc_e2m1_sr, and code(-t, w) == code(t, w) | 8 on the device.
+//     orc_e2m1_sr, and code(-t, w) == code(t, w) | 8 on the device;
+//   - philox4x32_10 (the random words of stochastic rounding): 2^26
+//     counters and keys that vary in every word, all four output words,
+//     against orc_philox4x32_10.
 //
-// Prints "checked N mismatches M" (N = 2 x 0x7F800000 + 0x41000001 codes)
-// and the first mismatches; exits 0 when the run completed.
+// Prints "checked N mismatches M" (N = 2 x 0x7F800000 + 0x41000001 codes +
+// 2^26 Philox blocks) and the first mismatches; exits 0 when the run
+// completed.
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -30,12 +34,24 @@
 extern "C" uint8_t orc_e2m1_rne(double t);
 extern "C" uint8_t orc_scale_encode(int fmt, float v);
 extern "C" uint8_t orc_e2m1_sr(double t, uint32_t w);
+extern "C" void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]);
 
 constexpr uint32_t kN = 0x7F800000u;  // every finite binary32 >= 0 (bit patterns 0 .. 0x7F7FFFFF)
 constexpr uint32_t kS = 0x41000001u;  // binary32 0 .. 8
 
+constexpr uint32_t kP = 1u << 26;     // Philox blocks
+
 // the random word of pattern b (a multiplicative hash)
 __host__ __device__ inline uint32_t word_of(uint32_t b) { return (b * 2654435761u) ^ 0x5BD1E995u; }
+// Philox counter and key of block i: every word varies
+__host__ __device__ inline void philox_in(uint32_t i, uint32_t (&c)[4], uint32_t (&k)[2]) {
+  c[0] = i * 0x9E3779B9u;
+  c[1] = ~i;
+  c[2] = i * 0x85EBCA6Bu + 7u;
+  c[3] = i & 3u;
+  k[0] = word_of(i);
+  k[1] = i ^ 0xA5A5A5A5u;
+}
 
 __global__ void encode_all(uint8_t* e2, uint8_t* e4, unsigned long long* asym) {
   for (uint32_t b = blockIdx.x * blockDim.x + threadIdx.x; b < kN; b += gridDim.x * blockDim.x) {
@@ -57,10 +73,20 @@ __global__ void round_sr_all(uint8_t* sr, unsigned long long* asym) {
   }
 }
 
+__global__ void philox_all(uint4* out) {
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < kP; i += gridDim.x * blockDim.x) {
+    uint32_t c[4], k[2];
+    philox_in(i, c, k);
+    out[i] = fp4q::philox4x32_10(make_uint4(c[0], c[1], c[2], c[3]), k[0], k[1]);
+  }
+}
+
 int main() {
   uint8_t *d2 = nullptr, *d4 = nullptr, *ds = nullptr;
+  uint4* dp = nullptr;
   unsigned long long* dasym = nullptr;
   if (cudaMalloc(&d2, kN) != cudaSuccess || cudaMalloc(&d4, kN) != cudaSuccess || cudaMalloc(&ds, kS) != cudaSuccess ||
+      cudaMalloc(&dp, (size_t)kP * sizeof(uint4)) != cudaSuccess ||
       cudaMalloc(&dasym, sizeof(*dasym)) != cudaSuccess) {
     std::printf("cuda alloc failed\n");
     return 2;
@@ -68,22 +94,25 @@ int main() {
   cudaMemset(dasym, 0, sizeof(*dasym));
   encode_all<<<152 * 8, 256>>>(d2, d4, dasym);
   round_sr_all<<<152 * 8, 256>>>(ds, dasym);
+  philox_all<<<152 * 8, 256>>>(dp);
   if (cudaDeviceSynchronize() != cudaSuccess) {
     std::printf("kernel failed\n");
     return 2;
   }
   std::vector<uint8_t> e2(kN), e4(kN), esr(kS);
+  std::vector<uint4> ph(kP);
   unsigned long long asym = 0;
   if (cudaMemcpy(e2.data(), d2, kN, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(e4.data(), d4, kN, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(esr.data(), ds, kS, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(ph.data(), dp, (size_t)kP * sizeof(uint4), cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(&asym, dasym, sizeof(asym), cudaMemcpyDeviceToHost) != cudaSuccess) {
     std::printf("copy failed\n");
     return 2;
   }
   // the oracle over the same patterns, in slices across the host's cores
   const unsigned nt = std::thread::hardware_concurrency() ? std::thread::hardware_concurrency() : 4;
-  std::vector<unsigned long long> bad2(nt, 0), bad4(nt, 0), bads(nt, 0);
+  std::vector<unsigned long long> bad2(nt, 0), bad4(nt, 0), bads(nt, 0), badp(nt, 0);
   std::vector<uint32_t> first2(nt, 0xFFFFFFFFu), first4(nt, 0xFFFFFFFFu), firsts(nt, 0xFFFFFFFFu);
   std::vector<std::thread> pool;
   for (unsigned k = 0; k < nt; ++k) {
@@ -101,19 +130,29 @@ int main() {
         if (b < kS && esr[b] != orc_e2m1_sr((double)v, word_of(b))) {
           if (bads[k]++ == 0) firsts[k] = b;
         }
+        if (b < kP) {
+          uint32_t c[4], key[2], o[4];
+          philox_in(b, c, key);
+          orc_philox4x32_10(c, key, o);
+          const uint4 d = ph[b];
+          if (d.x != o[0] || d.y != o[1] || d.z != o[2] || d.w != o[3]) {
+            if (badp[k]++ == 0) std::printf("philox i=%u device=%08x oracle=%08x\n", b, d.x, o[0]);
+          }
+        }
       }
     });
   }
   for (auto& th : pool) th.join();
-  unsigned long long m2 = 0, m4 = 0, ms = 0;
+  unsigned long long m2 = 0, m4 = 0, ms = 0, mp = 0;
   for (unsigned k = 0; k < nt; ++k) {
     m2 += bad2[k];
     m4 += bad4[k];
     ms += bads[k];
+    mp += badp[k];
   }
-  std::printf("checked %llu mismatches %llu\n", 2ull * kN + kS, m2 + m4 + ms + asym);
-  std::printf("e2m1 mismatches %llu, sign asymmetries %llu, e4m3 mismatches %llu, sr mismatches %llu\n", m2, asym,
-              m4, ms);
+  std::printf("checked %llu mismatches %llu\n", 2ull * kN + kS + kP, m2 + m4 + ms + mp + asym);
+  std::printf("e2m1 mismatches %llu, sign asymmetries %llu, e4m3 mismatches %llu, sr mismatches %llu, "
+              "philox mismatches %llu\n", m2, asym, m4, ms, mp);
   for (unsigned k = 0; k < nt; ++k) {
     if (first2[k] != 0xFFFFFFFFu) {
       float v;

@@ -49,8 +49,9 @@ def test_hardware_encoders_match_the_oracle(tmp_path, orc):
     """The E2M1 (cvt.rn.satfinite.e2m1x2.f32) and E4M3 scale
     (cvt.rn.satfinite.e4m3x2.f32) conversions against the oracle's encoders
     for every finite binary32 >= 0, the stochastic E2M1 rounding against the
-    oracle's for every binary32 in [0, 8] (one hashed random word each), and
-    the sign rule of both on the device."""
+    oracle's for every binary32 in [0, 8] (one hashed random word each), the
+    sign rule of both on the device, and Philox4x32-10 against the oracle's
+    on 2^26 counters and keys."""
     so = orc.build()
     exe = str(tmp_path / "gpu_encoder_check")
     subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I", CSRC,
@@ -60,5 +61,5 @@ def test_hardware_encoders_match_the_oracle(tmp_path, orc):
     assert out.returncode == 0, out.stdout + out.stderr
     m = re.search(r"checked (\d+) mismatches (\d+)", out.stdout)
     assert m, out.stdout
-    assert int(m.group(1)) == 2 * 0x7F800000 + 0x41000001
+    assert int(m.group(1)) == 2 * 0x7F800000 + 0x41000001 + (1 << 26)
     assert int(m.group(2)) == 0, out.stdout
