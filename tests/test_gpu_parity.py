@@ -464,6 +464,40 @@ def test_sr_ef_weight_loop(orc):
                     {"W": Wo, "r": ro})
 
 
+def test_stored_weight_update_tracking():
+    """fp4-train "Motivation" / "Correctness" (the stored-weight experiment):
+    with FP4 weights updated by tiny steps, round-to-nearest stalls while
+    stochastic rounding and error feedback follow the fp32 trajectory, error
+    feedback most closely.  The fp32 [8192, 8192] weight starts on the FP4
+    grid (one RNE QDQ); 500 steps W <- qdq(W - 1e-4 g_t), mode none, against
+    W_ref <- W_ref - 1e-4 g_t in binary32.  Tracking is the cosine between
+    W_T - W_0 and W_ref - W_0.  Qualitative (the pages report losses of an
+    unnamed model, not these numbers); the measured values are printed."""
+    T, M, K = 500, 8192, 8192
+    W0, _ = W.sr_ef_weight()
+    W0 = fq.qdq(W0.cuda(), mode="none", out_dtype=torch.float32)[0]
+    Wref = W0.clone()
+    var = {"rtn": (False, False), "rtn_ef": (False, True), "sr": (True, False), "sr_ef": (True, True)}
+    Ws = {k: W0.clone() for k in var}
+    rs = {k: (torch.zeros_like(W0) if ef else None) for k, (_, ef) in var.items()}
+    for t in range(T):
+        g = W.sr_ef_gradient(t, M, K, device="cuda")
+        Wref = Wref - g * 1e-4
+        for k, (sr, _) in var.items():
+            Ws[k] = fq.qdq(Ws[k] - g * 1e-4, mode="none", stochastic=sr, seed=0, step=t, residual=rs[k],
+                           out_dtype=torch.float32)[0]
+    d = (Wref - W0).double()
+    cos, moved = {}, {}
+    for k in var:
+        dk = (Ws[k] - W0).double()
+        cos[k] = float((dk * d).sum() / (dk.norm() * d.norm()).clamp_min(1e-300))
+        moved[k] = float((Ws[k] != W0).double().mean())
+    print("tracking cosine", cos, "fraction of weights moved", moved)
+    assert moved["rtn"] < 0.01 and abs(cos["rtn"]) < 0.05       # round-to-nearest stalls
+    assert cos["sr"] > 0.05                                       # SR follows, noisily
+    assert cos["sr_ef"] > cos["sr"] and cos["rtn_ef"] > cos["sr"]  # error feedback follows closer
+    assert cos["rtn_ef"] > 0.5
+
 def test_sr_mean_on_gpu():
     """fp4-train 'Correctness': SR of 2.3 averages 2.300 (RTN 2.000)."""
     blk = torch.full((16,), 2.3)
