@@ -415,6 +415,7 @@ def test_activations_full_size(orc, kernel):
         yr = host_np(fq.dequantize(q, "row", torch.float32))[0]
         yc = host_np(fq.dequantize(q, "col", torch.float32))[0].T
         snr[kw["mode"]] = (snr_db(xf, yr), snr_db(xf, yc))
+    print("SNR dB (rowwise, columnwise):", snr)
     assert snr["outer_block"][0] >= snr["tensorwise"][0]
     assert snr["outer_block"][1] >= snr["tensorwise"][1]
 
