@@ -30,10 +30,10 @@ struct BL {
   __host__ __device__ static constexpr int cst(int s) { return BNS * BRAW + s * 64 * CST; }
   static constexpr int tab = BNS * BRAW + 2 * 64 * CST;                     // 256 x (s, zh, zl, -)
   __host__ __device__ static constexpr int scales(int s) { return tab + 256 * 16 + s * 512; }  // 64 x 8
-  static constexpr int red2d = tab + 256 * 16 + 2 * 512;                    // 32 x u32: 2-D sub-tile maxima
-  __host__ __device__ static constexpr int redc(int s) { return red2d + 128 + s * 1024; }  // 64 x 4 u32
-  static constexpr int sr2d = red2d + 128 + 2 * 1024;                       // 32 x (S, 1 / S)
-  static constexpr int bars = sr2d + 32 * 8;                                // BNS mbarriers
+  // 2-D sub-tile maxima: 2 x 32 u32, picked by tile parity
+  static constexpr int red2d = tab + 256 * 16 + 2 * 512;
+  __host__ __device__ static constexpr int redc(int s) { return red2d + 256 + s * 1024; }  // 64 x 4 u32
+  static constexpr int bars = red2d + 256 + 2 * 1024;                       // BNS mbarriers
   static constexpr int total = bars + 8 * BNS + 1024;                       // + alignment slack
 };
 
@@ -155,7 +155,6 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   float4* tab = reinterpret_cast<float4*>(smem + BL::tab);
   uint32_t* red2d = reinterpret_cast<uint32_t*>(smem + BL::red2d);
-  float2* sr2d = reinterpret_cast<float2*>(smem + BL::sr2d);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BL::bars);
 
   // grouped inputs: rows [goff[e], goff[e + 1]) form group e, quantized as
@@ -187,7 +186,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     }
   }
   build_scale_table<UE5M3>(tab, t, BT);
-  if (t < 32) red2d[t] = 0u;
+  if (t < 64) red2d[t] = 0u;
   reinterpret_cast<uint32_t*>(smem + BL::redc(0))[t] = 0u;
   reinterpret_cast<uint32_t*>(smem + BL::redc(1))[t] = 0u;
 
@@ -290,7 +289,10 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     }
     }
 
-    // 2-D outer scales of the tile's ob x ob sub-blocks
+    // 2-D outer scales of the tile's ob x ob sub-blocks: the maxima meet in
+    // the tile's half of red2d; after one barrier every thread derives the S
+    // and 1 / S it needs from them
+    uint32_t* r2 = red2d + 32 * (it & 1);
     if (BO == BO_T2D) {
       uint32_t v = umax(fbits(am[0]), fbits(am[1]));
       uint32_t v0 = fbits(am[0]), v1 = fbits(am[1]);
@@ -308,24 +310,22 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         const int sb0 = (32 * rh) >> lob, sb1 = (32 * rh + 16) >> lob;
         const int srow = (16 * warp) >> lob;
         if (ob == 16) {
-          red2d[srow * nbk + sb0] = v0;
-          red2d[srow * nbk + sb1] = v1;
+          r2[srow * nbk + sb0] = v0;
+          r2[srow * nbk + sb1] = v1;
         } else {
-          atomicMax(&red2d[srow * nbk + sb0], v0);
-          if (sb1 != sb0) atomicMax(&red2d[srow * nbk + sb1], v1);
+          atomicMax(&r2[srow * nbk + sb0], v0);
+          if (sb1 != sb0) atomicMax(&r2[srow * nbk + sb1], v1);
         }
       }
       __syncthreads();
+      // the next tile's half: its last readers (the previous tile) are past
+      // the previous tile's final barrier, its next writers past this one's
+      if (t < 32) red2d[32 * ((it + 1) & 1) + t] = 0u;
       const int nsub = (BM >> lob) * nbk;
-      if (t < nsub) {
-        const float A = bitsf(red2d[t]);
-        red2d[t] = 0u;
-        const float S = outer_scale<UE5M3>(A);
-        sr2d[t] = make_float2(S, ieee_rcp(S));
+      if (t < nsub && j.tile_outer) {
         const int64_t mi = p.m0 + (int64_t)(t / nbk) * ob, kj = p.k0 + (int64_t)(t % nbk) * ob;
-        if (j.tile_outer && mi < gend && kj < K) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = S;
+        if (mi < gend && kj < K) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = outer_scale<UE5M3>(bitsf(r2[t]));
       }
-      __syncthreads();
     }
 
     if (j.do_row) {
@@ -352,11 +352,13 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
           }
         }
       } else if (BO == BO_T2D) {
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const float2 sr = sr2d[((16 * warp + (lane >> 1)) >> lob) * (64 >> lob) + ((32 * rh + 16 * b) >> lob)];
-          S[b] = sr.x;
-          R[b] = sr.y;
+        const int i0 = ((16 * warp + (lane >> 1)) >> lob) * (64 >> lob);
+        outer_sr<UE5M3>(bitsf(r2[i0 + ((32 * rh) >> lob)]), S[0], R[0]);
+        if (ob == 16) {
+          outer_sr<UE5M3>(bitsf(r2[i0 + ((32 * rh + 16) >> lob)]), S[1], R[1]);
+        } else {
+          S[1] = S[0];
+          R[1] = R[0];
         }
       } else if (BO == BO_B1D || BO == BO_B2D) {
 #pragma unroll
@@ -496,12 +498,10 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
           j.col_outer[(cbase + k * cstride + mb) >> lob] = S[c];
       }
     } else if (BO == BO_T2D) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float2 sr = sr2d[((16 * warp) >> lob) * (64 >> lob) + ((2 * lane + c) >> lob)];
-        S[c] = sr.x;
-        R[c] = sr.y;
-      }
+      // columns 2 lane and 2 lane + 1 lie in one sub-block (ob >= 16)
+      outer_sr<UE5M3>(bitsf(r2[((16 * warp) >> lob) * (64 >> lob) + ((2 * lane) >> lob)]), S[0], R[0]);
+      S[1] = S[0];
+      R[1] = R[0];
     } else if (BO == BO_B1D || BO == BO_B2D) {
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
