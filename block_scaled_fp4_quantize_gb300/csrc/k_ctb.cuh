@@ -146,7 +146,7 @@ struct GroupCursor {
   }
 };
 
-template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC>
 __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                           const __grid_constant__ CUtensorMap cmap, int col_tma) {
   pdl_wait_then_release();
@@ -191,9 +191,10 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   reinterpret_cast<uint32_t*>(smem + BL::redc(1))[t] = 0u;
 
   const bool none = BO == BO_NONE;
-  const int ob = j.ob;
-  const int lob = ob > 0 ? 31 - __clz(ob) : 0;
-  const bool ob_pow2 = ob > 0 && (ob & (ob - 1)) == 0;
+  // OBC: the outer block size fixed at compile time (0: taken from the job)
+  const int ob = OBC ? OBC : j.ob;
+  const int lob = OBC ? (OBC == 64 ? 6 : OBC == 32 ? 5 : 4) : (ob > 0 ? 31 - __clz(ob) : 0);
+  const bool ob_pow2 = OBC ? true : (ob > 0 && (ob & (ob - 1)) == 0);
   const int64_t mob = ob > 0 ? j.M / ob : 0, kob = ob > 0 ? j.K / ob : 0;
   float S_u = 1.0f, r_u = 1.0f;
   int64_t s_group = -1;  // group whose tensorwise scale S_u holds (grouped path)
@@ -653,10 +654,10 @@ bool make_col_map(const QuantJob& j, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool SR, bool UE5M3, int BO, bool GR, bool RHT>
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC = 0>
 cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,
                          cudaStream_t st) {
-  auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT>;
+  auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT, OBC>;
   static int per_sm_cache[128] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -688,6 +689,11 @@ cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, const CUtens
     if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false>(j, map, cmap, col_tma, st);
     if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
       return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false>(j, map, cmap, col_tma, st);
+    if constexpr (!SR) {  // the common 64-element outer block, its size folded into the code
+      if (j.s_src == S_IN_TILE && j.ob == 64)
+        return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false, 64>(j, map, cmap, col_tma, st)
+                          : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false, 64>(j, map, cmap, col_tma, st);
+    }
     if (j.s_src == S_IN_TILE)
       return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false>(j, map, cmap, col_tma, st)
                         : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false>(j, map, cmap, col_tma, st);
