@@ -146,7 +146,9 @@ struct GroupCursor {
   }
 };
 
-template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC>
+// FT: every tile is whole (M a multiple of 128 rows, K of 64 columns, no
+// groups), so the edge checks fold away.
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC, bool FT>
 __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                           const __grid_constant__ CUtensorMap cmap, int col_tma) {
   pdl_wait_then_release();
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 
     // ------------------------------------------------------------ rowwise
     const int64_t m = p.m0 + rr;
-    const bool rvalid = m < gend;
+    const bool rvalid = FT || m < gend;
     const int64_t rel = (p.g * M + m) * K + p.k0 + 32 * rh;  // flat index of this thread's first element
     uint4 a[4] = {};
     float am[2] = {0.0f, 0.0f};
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       const int nsub = (BM >> lob) * nbk;
       if (t < nsub && j.tile_outer) {
         const int64_t mi = p.m0 + (int64_t)(t / nbk) * ob, kj = p.k0 + (int64_t)(t % nbk) * ob;
-        if (mi < gend && kj < K) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = outer_scale<UE5M3>(bitsf(r2[t]));
+        if (FT || (mi < gend && kj < K)) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = outer_scale<UE5M3>(bitsf(r2[t]));
       }
     }
 
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             const int64_t e = rel + 16 * b;
-            if (p.k0 + 32 * rh + 16 * b < K && (e & (ob - 1)) == 0) j.row_outer[e >> lob] = S[b];
+            if ((FT || p.k0 + 32 * rh + 16 * b < K) && (e & (ob - 1)) == 0) j.row_outer[e >> lob] = S[b];
           }
         }
       } else if (BO == BO_T2D) {
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const int64_t kb = p.k0 + 32 * rh + 16 * b;
-          if (rvalid && kb < K) {
+          if (rvalid && (FT || kb < K)) {
             if (BO == BO_B1D) S[b] = j.row_outer[ob_pow2 ? ((rel + 16 * b) >> lob) : (rel + 16 * b) / ob];
             else S[b] = j.tile_outer[(p.g * mob + m / ob) * kob + kb / ob];
           }
@@ -413,7 +415,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         }
       }
       if (rvalid) {
-        const int nb = (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
+        const int nb = FT ? 2 : (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
         // scale byte offset: linear rel / 16; tensor-core tiles: the tile of
         // (m0 / 128, k0 / 64), row rr of it, columns 2 rh and 2 rh + 1
         const int64_t so = j.rsl.mma ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
@@ -476,7 +478,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       }
     }
     const int64_t mb = p.m0 + 16 * warp;  // first row of this lane's blocks
-    const bool mvalid = mb < gend;
+    const bool mvalid = FT || mb < gend;
     float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
     if (BO == BO_UNIFORM) {
       S[0] = S[1] = S_u;
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int64_t k = p.k0 + 2 * lane + c;
-        if (j.col_outer && k < K && mvalid && ((16 * warp) & (ob - 1)) == 0)
+        if (j.col_outer && (FT || k < K) && mvalid && ((16 * warp) & (ob - 1)) == 0)
           j.col_outer[(cbase + k * cstride + mb) >> lob] = S[c];
       }
     } else if (BO == BO_T2D) {
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int64_t k = p.k0 + 2 * lane + c;
-        if (k < K && mvalid) {
+        if ((FT || k < K) && mvalid) {
           if (BO == BO_B1D) S[c] = j.col_outer[ob_pow2 ? ((cbase + k * cstride + mb) >> lob) : (cbase + k * cstride + mb) / ob];
           else S[c] = j.tile_outer[(p.g * mob + (ob_pow2 ? (mb >> lob) : mb / ob)) * kob + (ob_pow2 ? (k >> lob) : k / ob)];
         }
@@ -581,8 +583,8 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       const int col = t >> 2, ch = t & 3;
       const int64_t k = p.k0 + col;
       const int64_t m1 = p.m0 + 32 * ch;
-      if ((GR || !col_tma) && k < K && m1 < gend) {
-        const int nb = (int)min((int64_t)2, (gend - m1) / 16);
+      if ((GR || !col_tma) && (FT || (k < K && m1 < gend))) {
+        const int nb = FT ? 2 : (int)min((int64_t)2, (gend - m1) / 16);
         const uint2 c0 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch);
         const uint2 c1 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch + 8);
         uint8_t* d = j.col_codes + (cbase + k * cstride + m1) / 2;
@@ -595,8 +597,8 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       }
       if (t < 64) {
         const int64_t kk = p.k0 + t;
-        if (kk < K) {
-          const int nbm = (int)min((int64_t)8, (gend - p.m0) / 16);
+        if (FT || kk < K) {
+          const int nbm = FT ? 8 : (int)min((int64_t)8, (gend - p.m0) / 16);
           const uint2 v = *reinterpret_cast<const uint2*>(sst + t * 8);
           if (j.csl.mma) {
             // scale columns m0 / 16 + 4 h .. + 3 of row kk: 4 bytes of tile
@@ -654,10 +656,10 @@ bool make_col_map(const QuantJob& j, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC = 0>
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC = 0, bool FT = false>
 cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,
                          cudaStream_t st) {
-  auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT, OBC>;
+  auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT, OBC, FT>;
   static int per_sm_cache[128] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -686,6 +688,16 @@ cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, const CUtens
     if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true>(j, map, cmap, col_tma, st);
     return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, cmap, col_tma, st);
   } else {
+    if constexpr (!SR && !GR) {  // whole tiles: the edge checks folded away
+      if (j.M % BM == 0 && j.K % BK == 0) {
+        if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false, 0, true>(j, map, cmap, col_tma, st);
+        if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
+          return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false, 0, true>(j, map, cmap, col_tma, st);
+        if (j.s_src == S_IN_TILE && j.ob == 64)
+          return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false, 64, true>(j, map, cmap, col_tma, st)
+                            : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false, 64, true>(j, map, cmap, col_tma, st);
+      }
+    }
     if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false>(j, map, cmap, col_tma, st);
     if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
       return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false>(j, map, cmap, col_tma, st);

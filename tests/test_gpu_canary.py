@@ -81,6 +81,12 @@ QUANT_CASES = [
     ("ct-bf16-hadamard", (1, 80, 176), torch.bfloat16, dict(mode="outer_block", outer_block_size=16,
                                                             col_hadamard=True, hadamard_signs=0x1234), True, True),
     ("ct-fp32", (1, 80, 176), torch.float32, dict(mode="outer_block", outer_block_size=16), True, True),
+    # whole tiles (M a multiple of 128, K of 64): the kernels' no-edge forms
+    ("ct-bf16-whole-ob64", (2, 256, 192), torch.bfloat16, dict(mode="outer_block", outer_block_size=64), True, True),
+    ("ct-bf16-whole-2d", (1, 128, 128), torch.bfloat16, dict(mode="outer_block", outer_block_size=64, outer_2d=True),
+     True, True),
+    ("ct-bf16-whole-none", (1, 128, 320), torch.bfloat16, dict(mode="none"), True, True),
+    ("ct-bf16-whole-tensorwise", (3, 128, 64), torch.bfloat16, dict(mode="tensorwise"), True, True),
     ("tile-inner2d", (1, 96, 96), torch.bfloat16, dict(mode="outer_block", outer_block_size=32, inner_2d=True),
      True, True),
 ]
