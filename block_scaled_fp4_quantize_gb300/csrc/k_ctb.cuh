@@ -147,10 +147,13 @@ struct GroupCursor {
 };
 
 // FT: every tile is whole (M a multiple of 128 rows, K of 64 columns, no
-// groups), so the edge checks fold away.
+// groups), both orientations are written, the columnwise codes leave by the
+// tensor store, the row codes are 16-byte aligned and the inner scales use
+// the linear layout, so the edge checks and these branches fold away.
 template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC, bool FT>
 __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
-                                                          const __grid_constant__ CUtensorMap cmap, int col_tma) {
+                                                          const __grid_constant__ CUtensorMap cmap, int col_tma_) {
+  const int col_tma = FT ? 1 : col_tma_;
   pdl_wait_then_release();
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -211,8 +214,8 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     r_u = ieee_rcp(S_u);
   }
   const int64_t M = j.M, K = j.K;
-  const bool row_wide = (K % 32) == 0 && ((reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0) &&
-                        ((reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0);
+  const bool row_wide = FT || ((K % 32) == 0 && ((reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0) &&
+                               ((reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0));
 
   // rowwise ownership
   const int rr = t >> 1, rh = t & 1;
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     const int64_t rel = (p.g * M + m) * K + p.k0 + 32 * rh;  // flat index of this thread's first element
     uint4 a[4] = {};
     float am[2] = {0.0f, 0.0f};
-    if (j.do_row || BO == BO_T2D) {
+    if (FT || j.do_row || BO == BO_T2D) {
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       a[q] = *reinterpret_cast<const uint4*>(raw + (rr * 8 + ((4 * rh + q) ^ (rr & 7))) * 16);
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       }
     }
 
-    if (j.do_row) {
+    if (FT || j.do_row) {
       float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
       if (BO == BO_UNIFORM) {
         S[0] = S[1] = S_u;
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         const int nb = FT ? 2 : (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
         // scale byte offset: linear rel / 16; tensor-core tiles: the tile of
         // (m0 / 128, k0 / 64), row rr of it, columns 2 rh and 2 rh + 1
-        const int64_t so = j.rsl.mma ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
+        const int64_t so = (!FT && j.rsl.mma) ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
                                            ((rr & 31) << 4) + ((rr >> 5) << 2) + 2 * rh
                                      : rel / 16;
         if (nb == 2 && row_wide) {
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     }
 
     // --------------------------------------------------------- columnwise
-    if (!j.do_col) {  // rowwise-only call (tensor-core scale layout)
+    if (!FT && !j.do_col) {  // rowwise-only call (tensor-core scale layout)
       __syncthreads();
       continue;
     }
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         if (FT || kk < K) {
           const int nbm = FT ? 8 : (int)min((int64_t)8, (gend - p.m0) / 16);
           const uint2 v = *reinterpret_cast<const uint2*>(sst + t * 8);
-          if (j.csl.mma) {
+          if (!FT && j.csl.mma) {
             // scale columns m0 / 16 + 4 h .. + 3 of row kk: 4 bytes of tile
             // (kk / 128, m0 / 64 + h)
             uint8_t* d = j.col_scales + ((p.g * j.csl.nrb + (kk >> 7)) * j.csl.ncb + (p.m0 >> 6)) * 512 +
@@ -689,7 +692,8 @@ cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, const CUtens
     return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, cmap, col_tma, st);
   } else {
     if constexpr (!SR && !GR) {  // whole tiles: the edge checks folded away
-      if (j.M % BM == 0 && j.K % BK == 0) {
+      if (j.M % BM == 0 && j.K % BK == 0 && col_tma && j.do_row && j.do_col && !j.rsl.mma && !j.csl.mma &&
+          (reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0 && (reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0) {
         if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false, 0, true>(j, map, cmap, col_tma, st);
         if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
           return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false, 0, true>(j, map, cmap, col_tma, st);
