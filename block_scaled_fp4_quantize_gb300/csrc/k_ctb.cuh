@@ -687,13 +687,21 @@ cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtens
 template <bool SR, bool UE5M3, bool GR, bool RHT>
 cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,
                          cudaStream_t st) {
+  // whole tiles: the edge checks folded away
+  const bool whole = j.M % BM == 0 && j.K % BK == 0 && col_tma && j.do_row && j.do_col && !j.rsl.mma && !j.csl.mma &&
+                     (reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0;
   if constexpr (RHT) {  // the transform is defined with no outer scale or 1-D outer blocks
+    if constexpr (!SR && !GR) {
+      if (whole && j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true, 0, true>(j, map, cmap, col_tma, st);
+      if (whole && j.s_src == S_IN_TILE && j.ob == 64)
+        return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true, 64, true>(j, map, cmap, col_tma, st);
+    }
     if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true>(j, map, cmap, col_tma, st);
     return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, cmap, col_tma, st);
   } else {
-    if constexpr (!SR && !GR) {  // whole tiles: the edge checks folded away
-      if (j.M % BM == 0 && j.K % BK == 0 && col_tma && j.do_row && j.do_col && !j.rsl.mma && !j.csl.mma &&
-          (reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0 && (reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0) {
+    if constexpr (!SR && !GR) {
+      if (whole) {
         if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false, 0, true>(j, map, cmap, col_tma, st);
         if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
           return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false, 0, true>(j, map, cmap, col_tma, st);

@@ -46,6 +46,19 @@ def test_rht_matches_oracle(orc, case, signs):
         assert_same(g, r)
 
 
+
+@pytest.mark.parametrize("case", [dict(mode="none"), dict(mode="outer_block", outer_block_size=64),
+                                  dict(mode="outer_block", outer_block_size=64, scale_format="ue5m3")],
+                         ids=["none", "ob64", "ob64-ue5m3"])
+def test_rht_whole_tiles(orc, case):
+    """M a multiple of 128 and K of 64: the kernel's whole-tile form."""
+    x = W.lognormal((2, 256, 192), 93, sigma=2.5)
+    x[1, 128:144, 70] = 3.3895314e38
+    for mask in ((False, True), (True, True)):
+        kw = dict(case, rowwise=mask[0], columnwise=mask[1], col_hadamard=True, hadamard_signs=0x5A0F)
+        _, g = gpu_quantize(x, **kw)
+        assert_same(g, _oracle(orc, x, kw))
+
 def test_rht_all_bf16_patterns_and_mma_layout(orc):
     x = W.all_bf16_patterns()
     kw = dict(mode="outer_block", outer_block_size=32, rowwise=True, columnwise=True, col_hadamard=True,
