@@ -146,14 +146,17 @@ struct GroupCursor {
   }
 };
 
-// FT: every tile is whole (M a multiple of 128 rows, K of 64 columns, no
-// groups), both orientations are written, the columnwise codes leave by the
-// tensor store, the row codes are 16-byte aligned and the inner scales use
-// the linear layout, so the edge checks and these branches fold away.
-template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC, bool FT>
+// FT, bit 0: every tile is whole along K (K a multiple of 64), so the
+// column edge checks fold away.  Bit 1: whole along M too (M a multiple of
+// 128, no groups), both orientations are written, the columnwise codes
+// leave by the tensor store, the row codes are 16-byte aligned and the
+// inner scales use the linear layout, so the row edge checks and these
+// branches fold away as well.
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC, int FT>
 __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                           const __grid_constant__ CUtensorMap cmap, int col_tma_) {
-  const int col_tma = FT ? 1 : col_tma_;
+  constexpr bool FTK = (FT & 1) != 0, FTM = (FT & 2) != 0;
+  const int col_tma = FTM ? 1 : col_tma_;
   pdl_wait_then_release();
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     r_u = ieee_rcp(S_u);
   }
   const int64_t M = j.M, K = j.K;
-  const bool row_wide = FT || ((K % 32) == 0 && ((reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0) &&
+  const bool row_wide = FTM || ((K % 32) == 0 && ((reinterpret_cast<uintptr_t>(j.row_codes) & 15u) == 0) &&
                                ((reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0));
 
   // rowwise ownership
@@ -268,11 +271,11 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 
     // ------------------------------------------------------------ rowwise
     const int64_t m = p.m0 + rr;
-    const bool rvalid = FT || m < gend;
+    const bool rvalid = FTM || m < gend;
     const int64_t rel = (p.g * M + m) * K + p.k0 + 32 * rh;  // flat index of this thread's first element
     uint4 a[4] = {};
     float am[2] = {0.0f, 0.0f};
-    if (FT || j.do_row || BO == BO_T2D) {
+    if (FTM || j.do_row || BO == BO_T2D) {
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       a[q] = *reinterpret_cast<const uint4*>(raw + (rr * 8 + ((4 * rh + q) ^ (rr & 7))) * 16);
@@ -330,11 +333,11 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       const int nsub = (BM >> lob) * nbk;
       if (t < nsub && j.tile_outer) {
         const int64_t mi = p.m0 + (int64_t)(t / nbk) * ob, kj = p.k0 + (int64_t)(t % nbk) * ob;
-        if (FT || (mi < gend && kj < K)) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = outer_scale<UE5M3>(bitsf(r2[t]));
+        if ((FTM || mi < gend) && (FTK || kj < K)) j.tile_outer[(p.g * mob + mi / ob) * kob + kj / ob] = outer_scale<UE5M3>(bitsf(r2[t]));
       }
     }
 
-    if (FT || j.do_row) {
+    if (FTM || j.do_row) {
       float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
       if (BO == BO_UNIFORM) {
         S[0] = S[1] = S_u;
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             const int64_t e = rel + 16 * b;
-            if ((FT || p.k0 + 32 * rh + 16 * b < K) && (e & (ob - 1)) == 0) j.row_outer[e >> lob] = S[b];
+            if ((FTK || p.k0 + 32 * rh + 16 * b < K) && (e & (ob - 1)) == 0) j.row_outer[e >> lob] = S[b];
           }
         }
       } else if (BO == BO_T2D) {
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           const int64_t kb = p.k0 + 32 * rh + 16 * b;
-          if (rvalid && (FT || kb < K)) {
+          if (rvalid && (FTK || kb < K)) {
             if (BO == BO_B1D) S[b] = j.row_outer[ob_pow2 ? ((rel + 16 * b) >> lob) : (rel + 16 * b) / ob];
             else S[b] = j.tile_outer[(p.g * mob + m / ob) * kob + kb / ob];
           }
@@ -418,10 +421,10 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         }
       }
       if (rvalid) {
-        const int nb = FT ? 2 : (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
+        const int nb = FTK ? 2 : (int)min((int64_t)2, (K - p.k0 - 32 * rh) / 16);
         // scale byte offset: linear rel / 16; tensor-core tiles: the tile of
         // (m0 / 128, k0 / 64), row rr of it, columns 2 rh and 2 rh + 1
-        const int64_t so = (!FT && j.rsl.mma) ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
+        const int64_t so = (!FTM && j.rsl.mma) ? ((p.g * j.rsl.nrb + (p.m0 >> 7)) * j.rsl.ncb + (p.k0 >> 6)) * 512 +
                                            ((rr & 31) << 4) + ((rr >> 5) << 2) + 2 * rh
                                      : rel / 16;
         if (nb == 2 && row_wide) {
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
     }
 
     // --------------------------------------------------------- columnwise
-    if (!FT && !j.do_col) {  // rowwise-only call (tensor-core scale layout)
+    if (!FTM && !j.do_col) {  // rowwise-only call (tensor-core scale layout)
       __syncthreads();
       continue;
     }
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       }
     }
     const int64_t mb = p.m0 + 16 * warp;  // first row of this lane's blocks
-    const bool mvalid = FT || mb < gend;
+    const bool mvalid = FTM || mb < gend;
     float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
     if (BO == BO_UNIFORM) {
       S[0] = S[1] = S_u;
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int64_t k = p.k0 + 2 * lane + c;
-        if (j.col_outer && (FT || k < K) && mvalid && ((16 * warp) & (ob - 1)) == 0)
+        if (j.col_outer && (FTK || k < K) && mvalid && ((16 * warp) & (ob - 1)) == 0)
           j.col_outer[(cbase + k * cstride + mb) >> lob] = S[c];
       }
     } else if (BO == BO_T2D) {
@@ -512,7 +515,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int64_t k = p.k0 + 2 * lane + c;
-        if ((FT || k < K) && mvalid) {
+        if ((FTK || k < K) && mvalid) {
           if (BO == BO_B1D) S[c] = j.col_outer[ob_pow2 ? ((cbase + k * cstride + mb) >> lob) : (cbase + k * cstride + mb) / ob];
           else S[c] = j.tile_outer[(p.g * mob + (ob_pow2 ? (mb >> lob) : mb / ob)) * kob + (ob_pow2 ? (k >> lob) : k / ob)];
         }
@@ -586,8 +589,8 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       const int col = t >> 2, ch = t & 3;
       const int64_t k = p.k0 + col;
       const int64_t m1 = p.m0 + 32 * ch;
-      if ((GR || !col_tma) && (FT || (k < K && m1 < gend))) {
-        const int nb = FT ? 2 : (int)min((int64_t)2, (gend - m1) / 16);
+      if ((GR || !col_tma) && (FTK || k < K) && (FTM || m1 < gend)) {
+        const int nb = FTM ? 2 : (int)min((int64_t)2, (gend - m1) / 16);
         const uint2 c0 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch);
         const uint2 c1 = *reinterpret_cast<const uint2*>(cst + col * CST + 16 * ch + 8);
         uint8_t* d = j.col_codes + (cbase + k * cstride + m1) / 2;
@@ -600,10 +603,10 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
       }
       if (t < 64) {
         const int64_t kk = p.k0 + t;
-        if (FT || kk < K) {
-          const int nbm = FT ? 8 : (int)min((int64_t)8, (gend - p.m0) / 16);
+        if (FTK || kk < K) {
+          const int nbm = FTM ? 8 : (int)min((int64_t)8, (gend - p.m0) / 16);
           const uint2 v = *reinterpret_cast<const uint2*>(sst + t * 8);
-          if (!FT && j.csl.mma) {
+          if (!FTM && j.csl.mma) {
             // scale columns m0 / 16 + 4 h .. + 3 of row kk: 4 bytes of tile
             // (kk / 128, m0 / 64 + h)
             uint8_t* d = j.col_scales + ((p.g * j.csl.nrb + (kk >> 7)) * j.csl.ncb + (p.m0 >> 6)) * 512 +
@@ -659,7 +662,7 @@ bool make_col_map(const QuantJob& j, CUtensorMap* map) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC = 0, bool FT = false>
+template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC = 0, int FT = 0>
 cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,
                          cudaStream_t st) {
   auto kern = ctb_kernel<SR, UE5M3, BO, GR, RHT, OBC, FT>;
@@ -693,30 +696,36 @@ cudaError_t launch_ctb_o(const QuantJob& j, const CUtensorMap& map, const CUtens
                      (reinterpret_cast<uintptr_t>(j.row_scales) & 1u) == 0;
   if constexpr (RHT) {  // the transform is defined with no outer scale or 1-D outer blocks
     if constexpr (!SR && !GR) {
-      if (whole && j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true, 0, true>(j, map, cmap, col_tma, st);
+      if (whole && j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true, 0, 3>(j, map, cmap, col_tma, st);
       if (whole && j.s_src == S_IN_TILE && j.ob == 64)
-        return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true, 64, true>(j, map, cmap, col_tma, st);
+        return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true, 64, 3>(j, map, cmap, col_tma, st);
     }
     if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, true>(j, map, cmap, col_tma, st);
     return launch_ctb_t<SR, UE5M3, BO_T1D, GR, true>(j, map, cmap, col_tma, st);
   } else {
     if constexpr (!SR && !GR) {
       if (whole) {
-        if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false, 0, true>(j, map, cmap, col_tma, st);
+        if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false, 0, 3>(j, map, cmap, col_tma, st);
         if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
-          return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false, 0, true>(j, map, cmap, col_tma, st);
+          return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false, 0, 3>(j, map, cmap, col_tma, st);
         if (j.s_src == S_IN_TILE && j.ob == 64)
-          return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false, 64, true>(j, map, cmap, col_tma, st)
-                            : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false, 64, true>(j, map, cmap, col_tma, st);
+          return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false, 64, 3>(j, map, cmap, col_tma, st)
+                            : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false, 64, 3>(j, map, cmap, col_tma, st);
       }
     }
     if (j.s_src == S_ONE) return launch_ctb_t<SR, UE5M3, BO_NONE, GR, false>(j, map, cmap, col_tma, st);
     if (j.s_src == S_TENSORWISE_WS || j.mode == 1)
       return launch_ctb_t<SR, UE5M3, BO_UNIFORM, GR, false>(j, map, cmap, col_tma, st);
     if constexpr (!SR) {  // the common 64-element outer block, its size folded into the code
-      if (j.s_src == S_IN_TILE && j.ob == 64)
+      if (j.s_src == S_IN_TILE && j.ob == 64) {
+        if constexpr (GR) {  // ragged groups: whole along K only
+          if (j.K % BK == 0)
+            return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false, 64, 1>(j, map, cmap, col_tma, st)
+                              : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false, 64, 1>(j, map, cmap, col_tma, st);
+        }
         return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false, 64>(j, map, cmap, col_tma, st)
                           : launch_ctb_t<SR, UE5M3, BO_T1D, GR, false, 64>(j, map, cmap, col_tma, st);
+      }
     }
     if (j.s_src == S_IN_TILE)
       return j.outer_2d ? launch_ctb_t<SR, UE5M3, BO_T2D, GR, false>(j, map, cmap, col_tma, st)
