@@ -13,6 +13,8 @@
 // (binary32) with 256-bit loads, and a 1 x ob outer block is ob / 16
 // adjacent lanes, reduced with xor-shuffles.  No shared-memory tile, no
 // barrier in the loop; the only shared memory is the inner-scale table.
+// The bf16 round-to-nearest quantize takes a second form, row_bulk_kernel,
+// whose input arrives by 1-D bulk copies into shared memory (below).
 #include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
@@ -238,6 +240,163 @@ __global__ void __launch_bounds__(RT) row_kernel(const QuantJob j) {
   }
 }
 
+// ---- bf16 round-to-nearest quantize fed by 1-D bulk copies ----
+// The same per-block steps with the input moved by the copy engine: a CTA
+// walks chunks of QB blocks (8 KB of bf16; chunk c = blockIdx.x + i
+// gridDim.x), QS chunks in flight in shared memory, each completed on an
+// mbarrier (bounded waits), so the loads hold no registers while they are
+// in flight.  Thread t takes block t of the chunk, so the lanes of a 1 x ob
+// outer block stay adjacent (a chunk starts on a multiple of QB blocks).
+constexpr int QB = 256, QS = 4;
+
+__device__ unsigned int g_row_timeout = 0;
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+template <bool UE5M3, int RO>
+__global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
+  pdl_wait_then_release();
+  __shared__ __align__(128) unsigned char buf[QS][QB * 32];
+  __shared__ float4 tab[256];
+  __shared__ __align__(8) uint64_t bars[QS];
+  const int t = threadIdx.x, lane = t & 31;
+  const int64_t nblk = j.G * j.M * j.K / 16, nch = (nblk + QB - 1) / QB;
+  const unsigned char* xb = static_cast<const unsigned char*>(j.x);
+  auto issue = [&](int64_t c, int s) {
+    const int64_t nb = nblk - c * QB < QB ? nblk - c * QB : QB;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(&bars[s], (uint32_t)(nb * 32));
+    bulk_load(buf[s], xb + c * QB * 32, (uint32_t)(nb * 32), &bars[s]);
+  };
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < QS; ++s) mbar_init(&bars[s]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (t == 0) {
+#pragma unroll
+    for (int s = 0; s < QS - 1; ++s) {
+      const int64_t c = blockIdx.x + (int64_t)s * gridDim.x;
+      if (c < nch) issue(c, s);
+    }
+  }
+  build_scale_table<UE5M3>(tab, t, RT);
+  const TabView tv{tab};
+  const int per = RO == RO_WARP || RO == RO_BUFFER ? j.ob / 16 : 1;
+  const bool per_pow2 = (per & (per - 1)) == 0;
+  const int lper = 31 - __clz(per);
+  float S_u = 1.0f, r_u = 1.0f;
+  if (RO == RO_UNIFORM) {
+    if (j.s_src == S_TENSORWISE_WS) {
+      S_u = ieee_div(bitsf(*j.tw_amax), UE5M3 ? 688128.0f : 2688.0f);
+      if (blockIdx.x == 0 && t == 0 && j.tile_outer) j.tile_outer[0] = S_u;
+    } else {
+      S_u = j.tile_outer[0];
+    }
+    r_u = ieee_rcp(S_u);
+  }
+  __syncthreads();
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int64_t c = blockIdx.x; c < nch; c += gridDim.x) {
+    if (t == 0) {
+      const int64_t cn = c + (int64_t)(QS - 1) * gridDim.x;
+      if (cn < nch) issue(cn, slot == 0 ? QS - 1 : slot - 1);
+    }
+    if (!mbar_wait(&bars[slot], phase, 1u << 22)) atomicExch(&g_row_timeout, 1u);
+    const int64_t b = c * QB + t;
+    const bool valid = b < nblk;
+    Raw<true> raw;
+    if (valid) {
+      const uint4 lo = *reinterpret_cast<const uint4*>(buf[slot] + 32 * t);
+      const uint4 hi = *reinterpret_cast<const uint4*>(buf[slot] + 32 * t + 16);
+      raw.w[0] = lo.x; raw.w[1] = lo.y; raw.w[2] = lo.z; raw.w[3] = lo.w;
+      raw.w[4] = hi.x; raw.w[5] = hi.y; raw.w[6] = hi.z; raw.w[7] = hi.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) raw.w[i] = 0u;
+    }
+    float u[16];
+    unpack<true>(raw, u);
+    float am = raw_amax<true>(raw);
+    if (fbits(am) >= 0x7F800000u) {  // inf / NaN present: sanitize the block
+#pragma unroll
+      for (int i = 0; i < 16; ++i) u[i] = sanitize(u[i], 0x7F7F0000u);
+      am = amax16(u);
+    }
+    Norm n;
+    n.none = RO == RO_NONE;
+    n.S = 1.0f;
+    n.r = 1.0f;
+    if (RO == RO_UNIFORM) {
+      n.S = S_u;
+      n.r = r_u;
+    } else if (RO == RO_WARP) {
+      uint32_t g = fbits(am);
+      for (int o = 1; o < per; o <<= 1) g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
+      outer_sr<UE5M3>(bitsf(g), n.S, n.r);
+      if (j.row_outer && j.do_row && valid && (lane & (per - 1)) == 0) j.row_outer[b >> lper] = n.S;
+    } else if (RO == RO_BUFFER) {
+      if (valid) n.S = j.row_outer[per_pow2 ? (b >> lper) : b / per];
+      n.r = ieee_rcp(n.S);
+    }
+    uint32_t sc, w0, w1;
+    float a = am;
+    const bool fast = __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
+    if (fast) {
+      sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, 0ull, 0u, 0u, 0ull, w0, w1);
+    } else {
+      n.pos = n.none || positive(n.S);
+      n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
+      float4 T;
+      sc = block_scale<UE5M3>(tv, am, n, T);
+      float x[16], dq[16];
+      normalize16<false>(u, x, n);
+      encode16<false, false>(x, T, n, 0ull, 0u, 0u, 0ull, w0, w1, dq);
+    }
+    if (valid) {
+      *reinterpret_cast<uint2*>(j.row_codes + 8 * b) = make_uint2(w0, w1);
+      j.row_scales[b] = (uint8_t)sc;
+    }
+    __syncthreads();  // the slot is free for the copy issued next iteration
+    if (++slot == QS) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+template <bool UE5M3, int RO>
+cudaError_t launch_row_bulk_t(const QuantJob& j, cudaStream_t st) {
+  auto kern = row_bulk_kernel<UE5M3, RO>;
+  static int per_sm_cache[128] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128) dev = 0;
+  int& per_sm = per_sm_cache[dev];
+  if (per_sm == 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RT, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+  }
+  const int64_t nch = (j.G * j.M * j.K / 16 + QB - 1) / QB;
+  const int64_t cap = (int64_t)num_sms() * per_sm;
+  return launch_pdl(kern, dim3((unsigned)(nch < cap ? nch : cap)), dim3(RT), 0, st, j);
+}
+
+template <bool UE5M3>
+cudaError_t launch_row_bulk_o(const QuantJob& j, cudaStream_t st) {
+  if (j.s_src == S_ONE) return launch_row_bulk_t<UE5M3, RO_NONE>(j, st);
+  if (j.s_src == S_TENSORWISE_WS || j.mode == 1) return launch_row_bulk_t<UE5M3, RO_UNIFORM>(j, st);
+  if (j.s_src == S_IN_TILE) return launch_row_bulk_t<UE5M3, RO_WARP>(j, st);
+  return launch_row_bulk_t<UE5M3, RO_BUFFER>(j, st);
+}
+
 template <bool IN_BF16, bool SR, bool UE5M3, int RO>
 cudaError_t launch_row_t(const QuantJob& j, cudaStream_t st) {
   auto kern = row_kernel<IN_BF16, SR, UE5M3, RO>;
@@ -286,6 +445,9 @@ bool row_supports(const QuantJob& j) {
 }
 
 cudaError_t launch_row(const QuantJob& j, cudaStream_t st) {
+  // bf16 round-to-nearest quantize (codes out, no residual): the bulk-copy form
+  if (j.in_bf16 && !j.sr && !j.residual && j.qdq_orient == 0 && j.row_codes && j.G * j.M * j.K > 0)
+    return j.ue5m3 ? launch_row_bulk_o<true>(j, st) : launch_row_bulk_o<false>(j, st);
   return j.in_bf16 ? launch_row_d<true>(j, st) : launch_row_d<false>(j, st);
 }
 
