@@ -773,3 +773,95 @@ def test_col_hadamard_quantize_is_quantize_of_the_transform(orc):
         assert (got["col_codes"] == ref_col["col_codes"]).all() and (got["col_scales"] == ref_col["col_scales"]).all()
         if kw["mode"] == "outer_block":
             assert (got["col_outer"].view(np.uint32) == ref_col["col_outer"].view(np.uint32)).all()
+
+
+# ----------------------------------------------------------------------------
+# input sanitization (reading Q6 of "NaN-input sanitization")
+# ----------------------------------------------------------------------------
+
+BF16_MAX = bits_f32(0x7F7F0000)
+F32_MAX = float(np.finfo(np.float32).max)
+
+
+def _plant_nonfinite(x_f32, rng):
+    """Scatter NaN (both signs), +inf and -inf over x (binary32 values);
+    returns the positions of each kind."""
+    n = x_f32.size
+    pos = rng.permutation(n)[:4 * 12].reshape(4, 12)
+    flat = x_f32.reshape(-1)
+    flat[pos[0]] = np.float32(np.nan)
+    flat[pos[1]] = -np.float32(np.nan)
+    flat[pos[2]] = np.float32(np.inf)
+    flat[pos[3]] = -np.float32(np.inf)
+    return pos
+
+
+def _as_input(xf, dtype):
+    if dtype == "fp32":
+        return np.ascontiguousarray(xf, np.float32)
+    return bf16_np(torch.from_numpy(np.ascontiguousarray(xf, np.float32)).to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("kw", [dict(mode="none"), dict(mode="tensorwise"), dict(mode="outer_block", ob=32),
+                                dict(mode="outer_block", ob=32, outer_2d=True),
+                                dict(mode="outer_block", ob=16, inner_2d=True)],
+                         ids=["none", "tensorwise", "ob32", "ob32-2d", "ob16-in2d"])
+def test_nonfinite_inputs_read_as_sanitized_values(orc, dtype, kw):
+    """ALTO "Op-level test coverage" names NaN-input sanitization without its
+    rule; the reading is NaN -> +0 and +-inf -> +- the largest finite value of
+    the input dtype, before any amax.  A tensor holding NaN / +inf / -inf must
+    quantize, in both orientations, exactly like the same tensor with +0,
+    +max and -max written in those places (max = 0x7F7F in bf16, FLT_MAX in
+    binary32), error-feedback residual included.  A NaN read as -0, the
+    binary32 maximum used for bf16 input, or a non-finite value reaching an
+    amax all break the equality."""
+    rng = np.random.default_rng(40)
+    xf = rng.standard_normal((64, 96)).astype(np.float32)
+    pos = _plant_nonfinite(xf, rng)
+    mx = BF16_MAX if dtype == "bf16" else F32_MAX
+    xs = xf.copy().reshape(-1)
+    xs[pos[0]] = 0.0
+    xs[pos[1]] = 0.0
+    xs[pos[2]] = mx
+    xs[pos[3]] = -mx
+    a, b = _as_input(xf, dtype), _as_input(xs.reshape(64, 96), dtype)
+    assert not np.array_equal(a, b)
+    qa = orc.quantize(a, out_mask=3, **kw)
+    qb = orc.quantize(b, out_mask=3, **kw)
+    for k, v in qa.items():
+        if v is not None:
+            np.testing.assert_array_equal(v.view(np.uint8), qb[k].view(np.uint8), err_msg=k)
+    # error feedback: u = sanitize(x + r) with r = 0, residual u - deq finite
+    ra = np.zeros((1, 64, 96), np.float32)
+    rb = np.zeros((1, 64, 96), np.float32)
+    orc.quantize(a, residual=ra, **kw)
+    orc.quantize(b, residual=rb, **kw)
+    assert np.all(np.isfinite(ra))
+    np.testing.assert_array_equal(ra.view(np.uint32), rb.view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype,mx", [("bf16", BF16_MAX), ("fp32", F32_MAX)])
+def test_nonfinite_inputs_closed_form(orc, dtype, mx):
+    """The same reading written out on one 1 x 16 block per case.
+    Mode none: the block [NaN, +inf, -inf, 1, 0 ...] has amax = max (the
+    sanitized infinity), so the inner scale saturates at 448 (code 0x7E); the
+    NaN becomes code 0x0 (+0, not 0x8), +-inf code 0x7 / 0xF (+-6), and 1/448
+    rounds to +0.  Tensorwise: the scale is max / 2688 in binary32, which
+    tells the bf16 maximum from the binary32 one."""
+    xf = np.zeros((1, 16), np.float32)
+    xf[0, :4] = [np.nan, np.inf, -np.inf, 1.0]
+    x = _as_input(xf, dtype)
+    q = orc.quantize(x, mode="none")
+    assert q["row_scales"][0, 0, 0] == 0x7E
+    codes = _unpack(q["row_codes"])[0, 0]
+    assert list(codes[:4]) == [0x0, 0x7, 0xF, 0x0]
+    assert set(codes[4:]) == {0x0}
+    t = orc.quantize(x, mode="tensorwise")
+    want = np.float32(mx) / np.float32(2688.0)
+    assert t["tile_outer"][0].view(np.uint32) == want.view(np.uint32)
+    # a block of NaNs alone: every value +0, amax 0, scale 0, codes +0
+    z = _as_input(np.full((1, 16), np.nan, np.float32), dtype)
+    qz = orc.quantize(z, mode="tensorwise")
+    assert qz["tile_outer"][0] == 0.0 and not np.signbit(qz["tile_outer"][0])
+    assert qz["row_scales"][0, 0, 0] == 0 and set(_unpack(qz["row_codes"])[0, 0]) == {0x0}
