@@ -11,6 +11,8 @@ the library's CUDA kernels.  The library must be built for the GPU in use
     mxfp4_fake_quantize(x)      -> projected tensor
     mxfp4_fake_quantize_host(x) -> the same for a host tensor, streamed through the GPU
     tensor_amax(x)              -> max |x| (sanitized) as a 1-element fp32 tensor
+    to_fp4_operands(x)          -> codes / scales as torch FP4 / FP8 tensors for _scaled_mm
+    device_status()             -> raises if a kernel's bounded wait ran out
 """
 from __future__ import annotations
 
@@ -24,7 +26,8 @@ from . import _capi
 from ._capi import FP4QError
 
 __all__ = ["QuantizedFP4", "MXFP8Pair", "quantize", "quantize_grouped", "dequantize", "mxfp4_project_mxfp8", "qdq", "mxfp4_fake_quantize", "mxfp4_fake_quantize_host",
-           "tensor_amax", "build", "FP4QError", "query_sizes", "host_workspace_bytes"]
+           "tensor_amax", "build", "FP4QError", "query_sizes", "host_workspace_bytes", "tensorwise_workspace",
+           "workspace_amax", "device_status", "FP4Operands", "to_fp4_operands"]
 
 _MODES = {"none": _capi.MODE_NONE, "tensorwise": _capi.MODE_TENSORWISE, "outer_block": _capi.MODE_OUTER_BLOCK}
 _FMTS = {"e4m3": _capi.SCALE_E4M3, "ue5m3": _capi.SCALE_UE5M3}
@@ -73,7 +76,8 @@ def _view3d(x: torch.Tensor):
 
 def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_size=0, outer_2d=False,
             inner_2d=False, scale_format="e4m3", stochastic=False, seed=0, step=0, out_mask=_capi.OUT_ROW,
-            use_precomputed_outer=False, scale_layout="linear", col_hadamard=False, hadamard_signs=0):
+            use_precomputed_outer=False, scale_layout="linear", col_hadamard=False, hadamard_signs=0,
+            precomputed_amax=False, sr_global_rows=0, sr_row_offset=0, sr_matrix_offset=0):
     p = _capi.new_params(_lib())
     p.G, p.M, p.K, p.ld = G, M, K, ld
     p.in_dtype = _DT.get(in_dtype, -1)
@@ -91,6 +95,8 @@ def _params(G, M, K, ld, in_dtype, out_dtype=None, *, mode="none", outer_block_s
     p.scale_layout = _LAYOUTS[scale_layout]
     p.col_hadamard = int(bool(col_hadamard))
     p.hadamard_signs = int(hadamard_signs) & 0xFFFF
+    p.precomputed_amax = int(bool(precomputed_amax))
+    p.sr_global_rows, p.sr_row_offset, p.sr_matrix_offset = int(sr_global_rows), int(sr_row_offset), int(sr_matrix_offset)
     return p
 
 
@@ -141,7 +147,8 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
              step: int = 0, rowwise: bool = True, columnwise: bool = False,
              residual: Optional[torch.Tensor] = None, precomputed_outer: Optional[QuantizedFP4] = None,
              out: Optional[QuantizedFP4] = None, scale_layout: str = "linear", col_hadamard: bool = False,
-             hadamard_signs: int = 0) -> QuantizedFP4:
+             hadamard_signs: int = 0, tensorwise_amax: Optional[torch.Tensor] = None, sr_global_rows: int = 0,
+             sr_row_offset: int = 0, sr_matrix_offset: int = 0) -> QuantizedFP4:
     """NVFP4 / AMD-FP4 quantize of a CUDA bf16 or fp32 tensor ([M, K] or [G, M, K]).
 
     ``residual`` (fp32, [G, M, K] contiguous) enables error feedback and is
@@ -152,13 +159,24 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
     (see include/fp4q.h); the scale tensors are then flat padded byte
     buffers.  ``col_hadamard`` applies the random Hadamard transform along M
     (16-row blocks, sign mask ``hadamard_signs``) before the columnwise
-    quantization."""
+    quantization.
+
+    ``tensorwise_amax``: a workspace from ``tensorwise_workspace()`` whose
+    ``workspace_amax`` already holds the amax of the whole tensor (e.g. the
+    maximum over the shards of a tensor split across processes); the
+    tensorwise scale is then computed from it on the device.
+    ``sr_global_rows`` / ``sr_row_offset`` / ``sr_matrix_offset``: this
+    tensor is rows ``sr_row_offset ..`` (of ``sr_global_rows``) and matrices
+    ``sr_matrix_offset ..`` of a larger one, whose element positions key the
+    stochastic-rounding draws (see include/fp4q.h)."""
     x3, G, M, K, ld = _view3d(x)
     mask = (_capi.OUT_ROW if rowwise else 0) | (_capi.OUT_COL if columnwise else 0)
     p = _params(G, M, K, ld, x.dtype, mode=mode, outer_block_size=outer_block_size, outer_2d=outer_2d,
                 inner_2d=inner_2d, scale_format=scale_format, stochastic=stochastic, seed=seed, step=step,
                 out_mask=mask, use_precomputed_outer=precomputed_outer is not None, scale_layout=scale_layout,
-                col_hadamard=col_hadamard, hadamard_signs=hadamard_signs)
+                col_hadamard=col_hadamard, hadamard_signs=hadamard_signs,
+                precomputed_amax=tensorwise_amax is not None, sr_global_rows=sr_global_rows,
+                sr_row_offset=sr_row_offset, sr_matrix_offset=sr_matrix_offset)
     s = query_sizes(p)
     dev = x.device
     if out is None:
@@ -181,11 +199,40 @@ def quantize(x: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0, 
     o = _capi.Outputs(*[_ptr(getattr(q, n)) for n in
                         ("row_codes", "row_scales", "row_outer", "col_codes", "col_scales", "col_outer",
                          "tile_outer")])
-    ws = torch.empty(max(int(s.workspace), 1), dtype=torch.uint8, device=dev) if s.workspace else None
+    if tensorwise_amax is not None:
+        if tensorwise_amax.dtype != torch.uint8 or tensorwise_amax.numel() < s.workspace or not tensorwise_amax.is_cuda:
+            raise ValueError("tensorwise_amax must be a CUDA workspace from tensorwise_workspace()")
+        ws = tensorwise_amax
+    else:
+        ws = torch.empty(max(int(s.workspace), 1), dtype=torch.uint8, device=dev) if s.workspace else None
     st = _lib().fp4_quantize(ctypes.byref(p), _ptr(x3), ctypes.byref(o), _ptr(residual), _ptr(ws),
                              int(s.workspace), _stream(dev))
     _capi.check(st, "fp4_quantize")
     return q
+
+
+@dataclass
+class FP4Operands:
+    """Outputs of ``to_fp4_operands``: the same buffers as the QuantizedFP4,
+    viewed as torch's FP4 / FP8 dtypes."""
+    codes: torch.Tensor       # float4_e2m1fn_x2 [M, K/2] (or [G, M, K/2])
+    scales: torch.Tensor      # float8_e4m3fn, flat, 128 x 4 tiled tensor-core layout
+    quantized: QuantizedFP4   # the underlying uint8 buffers
+
+
+def to_fp4_operands(x: torch.Tensor, stochastic: bool = False, seed: int = 0, step: int = 0,
+                    residual: Optional[torch.Tensor] = None) -> FP4Operands:
+    """NVFP4 quantize of x ([M, K] or [G, M, K], bf16 / fp32) into the operand
+    form of torch's block-scaled FP4 matmul (fp4-train README, "API":
+    to_fp4_operands, packed fp4 + e4m3 scale as the torch FP4 dtypes for
+    ``_scaled_mm``): per-16 E4M3 scales along K in the tensor-core layout,
+    codes two per byte.  ``stochastic`` / ``seed`` / ``step`` / ``residual``
+    as for ``quantize``.  The views share the quantizer's buffers."""
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        raise RuntimeError("this torch has no float4_e2m1fn_x2 dtype")
+    q = quantize(x, stochastic=stochastic, seed=seed, step=step, residual=residual, scale_layout="mma")
+    codes = q.row_codes if x.dim() == 3 else q.row_codes[0]
+    return FP4Operands(codes.view(torch.float4_e2m1fn_x2), q.row_scales.view(torch.float8_e4m3fn), q)
 
 
 def quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, *, mode: str = "none", outer_block_size: int = 0,
@@ -269,7 +316,8 @@ def qdq(x: torch.Tensor, *, axis: int = -1, mode: str = "none", outer_block_size
         outer_2d: bool = False, inner_2d: bool = False, scale_format: str = "e4m3", stochastic: bool = False,
         seed: int = 0, step: int = 0, residual: Optional[torch.Tensor] = None,
         precomputed_outer: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
-        out: Optional[torch.Tensor] = None):
+        out: Optional[torch.Tensor] = None, tensorwise_amax: Optional[torch.Tensor] = None, sr_global_rows: int = 0,
+        sr_row_offset: int = 0, sr_matrix_offset: int = 0):
     """Quantize-dequantize along ``axis`` (-1: blocks along K; 0: along M).
 
     Returns (y, outer) with y [G, M, K] (or [M, K]) in ``out_dtype`` (x's dtype
@@ -279,7 +327,9 @@ def qdq(x: torch.Tensor, *, axis: int = -1, mode: str = "none", outer_block_size
     out_dtype = out_dtype or x.dtype
     p = _params(G, M, K, ld, x.dtype, out_dtype, mode=mode, outer_block_size=outer_block_size,
                 outer_2d=outer_2d, inner_2d=inner_2d, scale_format=scale_format, stochastic=stochastic,
-                seed=seed, step=step, out_mask=o, use_precomputed_outer=precomputed_outer is not None)
+                seed=seed, step=step, out_mask=o, use_precomputed_outer=precomputed_outer is not None,
+                precomputed_amax=tensorwise_amax is not None, sr_global_rows=sr_global_rows,
+                sr_row_offset=sr_row_offset, sr_matrix_offset=sr_matrix_offset)
     s = query_sizes(p)
     dev = x.device
     shp = _outer_shapes(G, M, K, mode, outer_block_size, outer_2d, o == _capi.OUT_ROW, o == _capi.OUT_COL)
@@ -289,7 +339,12 @@ def qdq(x: torch.Tensor, *, axis: int = -1, mode: str = "none", outer_block_size
     else:
         outer = torch.empty(oshape, dtype=torch.float32, device=dev) if oshape is not None else None
     y = out if out is not None else torch.empty(G, M, K, dtype=out_dtype, device=dev)
-    ws = torch.empty(int(s.workspace), dtype=torch.uint8, device=dev) if s.workspace else None
+    if tensorwise_amax is not None:
+        if tensorwise_amax.dtype != torch.uint8 or tensorwise_amax.numel() < s.workspace or not tensorwise_amax.is_cuda:
+            raise ValueError("tensorwise_amax must be a CUDA workspace from tensorwise_workspace()")
+        ws = tensorwise_amax
+    else:
+        ws = torch.empty(int(s.workspace), dtype=torch.uint8, device=dev) if s.workspace else None
     st = _lib().fp4_qdq(ctypes.byref(p), o, _ptr(x3), _ptr(y), _ptr(residual), _ptr(outer), _ptr(ws),
                         int(s.workspace), _stream(dev))
     _capi.check(st, "fp4_qdq")
@@ -392,6 +447,31 @@ def mxfp4_fake_quantize_host(x: torch.Tensor, out_dtype: Optional[torch.dtype] =
         if synchronize:
             torch.cuda.current_stream(dev).synchronize()
     return y if (x.dim() == 3 or out is not None) else y[0]
+
+
+TENSORWISE_WORKSPACE_BYTES = 256
+
+
+def tensorwise_workspace(device) -> torch.Tensor:
+    """A device workspace for tensorwise quantization whose first float
+    (``workspace_amax``) carries the tensor's amax: fill it with
+    ``tensor_amax(x, out=workspace_amax(ws))`` (and, across processes, an
+    all-reduce MAX of that float), then pass it as ``tensorwise_amax``."""
+    return torch.zeros(TENSORWISE_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+
+
+def workspace_amax(ws: torch.Tensor) -> torch.Tensor:
+    """The 1-element float32 view of a tensorwise workspace's amax."""
+    return ws[:4].view(torch.float32)
+
+
+def device_status(clear: bool = True, device=None) -> None:
+    """Wait for the current stream, then raise FP4QError(FP4Q_ERR_TIMEOUT) if
+    a kernel's bounded wait for its tile copy ran out on this device since the
+    flags were last cleared (the outputs of that call are not valid)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _capi.check(_lib().fp4q_device_status(int(bool(clear)), _stream(dev)), "fp4q_device_status")
 
 
 def tensor_amax(x: torch.Tensor, residual: Optional[torch.Tensor] = None,

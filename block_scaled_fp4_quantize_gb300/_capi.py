@@ -10,13 +10,13 @@ FP4Q_OK = 0
 STATUS = {
     0: "FP4Q_OK", -1: "FP4Q_ERR_NULL", -2: "FP4Q_ERR_DTYPE", -3: "FP4Q_ERR_SHAPE", -4: "FP4Q_ERR_MODE",
     -5: "FP4Q_ERR_UNSUPPORTED", -6: "FP4Q_ERR_WORKSPACE", -7: "FP4Q_ERR_CUDA", -8: "FP4Q_ERR_ABI",
-    -9: "FP4Q_ERR_ALIGN",
+    -9: "FP4Q_ERR_ALIGN", -10: "FP4Q_ERR_TIMEOUT",
 }
 BF16, FP32, FP16 = 1, 2, 3
 MODE_NONE, MODE_TENSORWISE, MODE_OUTER_BLOCK = 0, 1, 2
 SCALE_E4M3, SCALE_UE5M3 = 0, 1
 SCALE_LAYOUT_LINEAR, SCALE_LAYOUT_MMA = 0, 1
-ABI_VERSION = 3  # FP4Q_ABI_VERSION of include/fp4q.h
+ABI_VERSION = 4  # FP4Q_ABI_VERSION of include/fp4q.h
 RNE, STOCHASTIC = 0, 1
 OUT_ROW, OUT_COL = 1, 2
 
@@ -24,7 +24,7 @@ OUT_ROW, OUT_COL = 1, 2
 EXPORTS = ("fp4q_params_init", "fp4q_query_sizes", "fp4_quantize", "fp4_dequantize", "fp4_qdq",
            "mxfp4_fake_quantize", "mxfp4_fake_quantize_host", "mxfp4_project_mxfp8", "fp4_tensor_amax", "fp4_quantize_grouped",
            "fp4q_query_sizes_grouped", "fp4q_status_string",
-           "fp4q_abi_version", "fp4_quantize_noalloc")
+           "fp4q_abi_version", "fp4_quantize_noalloc", "fp4q_device_status", "fp4q_set_device_timeout_flag")
 
 
 class Params(ctypes.Structure):
@@ -36,6 +36,8 @@ class Params(ctypes.Structure):
         ("scale_format", ctypes.c_int32), ("rounding", ctypes.c_int32),
         ("seed", ctypes.c_uint64), ("step", ctypes.c_uint32), ("use_precomputed_outer", ctypes.c_int32),
         ("scale_layout", ctypes.c_int32), ("col_hadamard", ctypes.c_int32), ("hadamard_signs", ctypes.c_uint32),
+        ("precomputed_amax", ctypes.c_int32),
+        ("sr_global_rows", ctypes.c_int64), ("sr_row_offset", ctypes.c_int64), ("sr_matrix_offset", ctypes.c_int64),
     ]
 
 
@@ -100,6 +102,10 @@ def load(fast_math: bool = False, path: str | None = None):
     L.fp4q_status_string.argtypes = [I]
     L.fp4q_abi_version.restype = I
     L.fp4q_abi_version.argtypes = []
+    L.fp4q_device_status.restype = I
+    L.fp4q_device_status.argtypes = [I, P]
+    L.fp4q_set_device_timeout_flag.restype = I
+    L.fp4q_set_device_timeout_flag.argtypes = []
     if L.fp4q_abi_version() != ABI_VERSION:
         raise RuntimeError("libfp4q ABI version mismatch")
     _libs[key] = L

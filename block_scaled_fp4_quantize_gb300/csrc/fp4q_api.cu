@@ -1,7 +1,7 @@
 // fp4q_api.cu -- the C ABI: argument validation, path selection, launches.
 //
-// Nothing here allocates, frees or synchronizes; all work is enqueued on the
-// caller's stream.  Validation happens before any launch, so an error other
+// Nothing here allocates or frees, and only fp4q_device_status synchronizes;
+// all work is enqueued on the caller's stream.  Validation happens before any launch, so an error other
 // than FP4Q_ERR_CUDA leaves the stream untouched.
 #include <cstdint>
 #include <cstdlib>
@@ -40,7 +40,19 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0u; }
 
+// Workspace of a tensorwise quantize: the amax word (the rest is padding).
+constexpr size_t kTensorwiseWsBytes = 256;
+static_assert(kTensorwiseWsBytes <= FP4Q_NOALLOC_SCRATCH_BYTES,
+              "fp4_quantize_noalloc's static scratch must hold the tensorwise workspace");
+
 int esize(int32_t dt) { return dt == FP4Q_BF16 ? 2 : 4; }
+
+// The NVFP4 knobs that MXFP4 fake-quantize and the MXFP8 re-encode do not take.
+bool mx_knobs_default(const fp4q_params_t* p) {
+  return p->mode == FP4Q_MODE_NONE && p->outer_block_size == 0 && p->outer_2d == 0 && p->inner_2d == 0 &&
+         p->scale_format == FP4Q_SCALE_E4M3 && p->use_precomputed_outer == 0 && p->scale_layout == 0 &&
+         p->col_hadamard == 0 && p->precomputed_amax == 0;
+}
 
 int check_dtype(int32_t dt) {
   if (dt == FP4Q_BF16 || dt == FP4Q_FP32) return FP4Q_OK;
@@ -60,7 +72,14 @@ int check_nvfp4(const fp4q_params_t* p, uint32_t mask) {
   if ((p->outer_2d & ~1) || (p->inner_2d & ~1) || (p->use_precomputed_outer & ~1)) return FP4Q_ERR_MODE;
   if (p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR && p->scale_layout != FP4Q_SCALE_LAYOUT_MMA) return FP4Q_ERR_MODE;
   if (p->col_hadamard & ~1) return FP4Q_ERR_MODE;
+  if (p->precomputed_amax & ~1) return FP4Q_ERR_MODE;
+  if (p->precomputed_amax && (p->mode != FP4Q_MODE_TENSORWISE || p->use_precomputed_outer)) return FP4Q_ERR_MODE;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K) return FP4Q_ERR_SHAPE;
+  // the stochastic-rounding counter's global index (a block of a larger tensor)
+  if (p->sr_global_rows < 0 || p->sr_row_offset < 0 || p->sr_matrix_offset < 0) return FP4Q_ERR_SHAPE;
+  if (p->sr_global_rows && p->sr_row_offset + p->M > p->sr_global_rows) return FP4Q_ERR_SHAPE;
+  if (!p->sr_global_rows && p->sr_row_offset) return FP4Q_ERR_SHAPE;
+  if (p->G > 1 && p->sr_global_rows && p->sr_global_rows != p->M) return FP4Q_ERR_UNSUPPORTED;
   if (p->K % 16) return FP4Q_ERR_SHAPE;
   const bool col = (mask & FP4Q_OUT_COL) != 0u;
   if ((col || p->inner_2d) && p->M % 16) return FP4Q_ERR_SHAPE;
@@ -89,7 +108,7 @@ void sizes_for(const fp4q_params_t* p, uint32_t mask, fp4q_sizes_t* s) {
   s->col_outer = (outer && !p->outer_2d && col) ? (size_t)(G * K * (M / ob)) * sizeof(float) : 0;
   s->tile_outer = (outer && p->outer_2d) ? (size_t)(G * (M / ob) * (K / ob)) * sizeof(float)
                   : (p->mode == FP4Q_MODE_TENSORWISE ? sizeof(float) : 0);
-  s->workspace = (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer) ? 256 : 0;
+  s->workspace = (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer) ? kTensorwiseWsBytes : 0;
 }
 
 QuantJob base_job(const fp4q_params_t* p, const void* x, float* residual) {
@@ -113,6 +132,12 @@ QuantJob base_job(const fp4q_params_t* p, const void* x, float* residual) {
   const int mma = p->scale_layout == FP4Q_SCALE_LAYOUT_MMA;
   j.rsl = make_scale_layout(mma, p->M, p->K / 16);
   j.csl = make_scale_layout(mma, p->K, p->M / 16);
+  // global index of the SR counter: this call is block [g0 : + G, r0 : + M]
+  // of a [*, Mg, K] tensor (with G > 1, Mg == M and r0 == 0)
+  const int64_t Mg = p->sr_global_rows ? p->sr_global_rows : p->M;
+  j.sr_row_off = (p->sr_matrix_offset * Mg + p->sr_row_offset) * p->K;
+  j.sr_col_off = p->sr_matrix_offset * p->K * Mg + p->sr_row_offset;
+  j.sr_col_ld = Mg;
   return j;
 }
 
@@ -129,6 +154,7 @@ int prepare_outer(const fp4q_params_t* p, QuantJob& j, void* ws, cudaStream_t st
   if (p->mode == FP4Q_MODE_TENSORWISE) {
     j.s_src = S_TENSORWISE_WS;
     j.tw_amax = static_cast<uint32_t*>(ws);
+    if (p->precomputed_amax) return FP4Q_OK;  // the caller's amax is in the workspace
     return launch_tensor_amax(j, static_cast<uint32_t*>(ws), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
   }
   const int ob = p->outer_block_size;
@@ -218,7 +244,7 @@ int fp4_quantize(const fp4q_params_t* p, const void* x, const fp4q_outputs_t* ou
   if (residual && !aligned(residual, 16)) return FP4Q_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (empty) {
-    if (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer)
+    if (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer && !p->precomputed_amax)
       return cudaMemsetAsync(out->tile_outer, 0, sizeof(float), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
     return FP4Q_OK;
   }
@@ -276,6 +302,7 @@ int fp4_quantize_grouped(const fp4q_params_t* p, const void* x, const int64_t* o
   const bool row = mask & FP4Q_OUT_ROW, col = mask & FP4Q_OUT_COL;
   const bool small_ob = p->outer_block_size == 16 || p->outer_block_size == 32 || p->outer_block_size == 64;
   if (p->in_dtype != FP4Q_BF16 || p->inner_2d || p->scale_layout != FP4Q_SCALE_LAYOUT_LINEAR || p->col_hadamard ||
+      p->precomputed_amax || p->sr_global_rows || p->sr_row_offset || p->sr_matrix_offset ||
       (p->use_precomputed_outer && p->mode != FP4Q_MODE_OUTER_BLOCK) ||
       (p->mode == FP4Q_MODE_OUTER_BLOCK && col && !p->outer_2d && !small_ob && !p->use_precomputed_outer))
     return FP4Q_ERR_UNSUPPORTED;
@@ -350,7 +377,7 @@ int fp4_qdq(const fp4q_params_t* p, int orient, const void* x, void* y, float* r
   if (!aligned(outer, 4) || (residual && !aligned(residual, 16))) return FP4Q_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (empty) {
-    if (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer)
+    if (p->mode == FP4Q_MODE_TENSORWISE && !p->use_precomputed_outer && !p->precomputed_amax)
       return cudaMemsetAsync(outer, 0, sizeof(float), st) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
     return FP4Q_OK;
   }
@@ -407,10 +434,7 @@ int mxfp4_fake_quantize(const fp4q_params_t* p, const void* x, void* y, void* st
   if (rc) return rc;
   rc = check_dtype(p->out_dtype);
   if (rc) return rc;
-  if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
-      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0 ||
-      p->col_hadamard != 0)
-    return FP4Q_ERR_MODE;
+  if (!mx_knobs_default(p)) return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K || p->K % 32) return FP4Q_ERR_SHAPE;
   if (p->G == 0 || p->M == 0 || p->K == 0) return FP4Q_OK;
@@ -453,10 +477,7 @@ int mxfp4_project_mxfp8(const fp4q_params_t* p, const void* x, void* y, uint8_t*
   if (rc) return rc;
   rc = check_dtype(p->out_dtype);
   if (rc) return rc;
-  if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
-      p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0 ||
-      p->col_hadamard != 0)
-    return FP4Q_ERR_MODE;
+  if (!mx_knobs_default(p)) return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
   const uint32_t mask = p->out_mask;
   if (mask & ~3u) return FP4Q_ERR_MODE;
@@ -497,10 +518,28 @@ const char* fp4q_status_string(int status) {
     case FP4Q_ERR_CUDA: return "FP4Q_ERR_CUDA: a CUDA launch failed";
     case FP4Q_ERR_ABI: return "FP4Q_ERR_ABI: parameter struct size mismatch";
     case FP4Q_ERR_ALIGN: return "FP4Q_ERR_ALIGN: a buffer is not naturally aligned";
+    case FP4Q_ERR_TIMEOUT: return "FP4Q_ERR_TIMEOUT: a kernel's bounded wait for its tile copy ran out";
     default: return "unknown fp4q status";
   }
 }
 
 int fp4q_abi_version(void) { return FP4Q_ABI_VERSION; }
+
+int fp4q_device_status(int clear, void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP4Q_ERR_CUDA;
+  cudaError_t (*const readers[])(uint32_t*, bool) = {ctb_timeout_flag, ctb_grouped_timeout_flag,
+                                                      ctb_rht_timeout_flag, row_timeout_flag, ct_timeout_flag};
+  uint32_t any = 0;
+  for (auto rd : readers) {
+    uint32_t v = 0;
+    if (rd(&v, clear != 0) != cudaSuccess) return FP4Q_ERR_CUDA;
+    any |= v;
+  }
+  return any ? FP4Q_ERR_TIMEOUT : FP4Q_OK;
+}
+
+int fp4q_set_device_timeout_flag(void) {
+  return set_ctb_timeout_flag() == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
 
 }  // extern "C"

@@ -64,7 +64,7 @@ extern "C" int mxfp4_fake_quantize_host(const fp4q_params_t* p, const void* x, v
     return FP4Q_ERR_DTYPE;
   if (p->mode != FP4Q_MODE_NONE || p->outer_block_size != 0 || p->outer_2d != 0 || p->inner_2d != 0 ||
       p->scale_format != FP4Q_SCALE_E4M3 || p->use_precomputed_outer != 0 || p->scale_layout != 0 ||
-      p->col_hadamard != 0)
+      p->col_hadamard != 0 || p->precomputed_amax != 0)
     return FP4Q_ERR_MODE;
   if (p->rounding != FP4Q_RNE) return FP4Q_ERR_UNSUPPORTED;
   if (p->G < 0 || p->M < 0 || p->K < 0 || p->ld < p->K || p->K % 32) return FP4Q_ERR_SHAPE;

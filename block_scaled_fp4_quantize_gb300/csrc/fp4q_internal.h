@@ -98,7 +98,18 @@ struct QuantJob {
   GroupWs* gws;         // device workspace of the grouped path
   int col_rht;          // 1: Hadamard transform along M before the columnwise side
   uint32_t rht_signs;   // its sign mask (bit i: element i of each 16-block negated)
+  // global index of the stochastic-rounding counter: rowwise element with
+  // local flat index n draws word n + sr_row_off; columnwise element of row
+  // gk = g K + k (of x transposed), column m draws sr_col_off + gk sr_col_ld + m
+  int64_t sr_row_off, sr_col_off, sr_col_ld;
 };
+
+__host__ __device__ __forceinline__ uint64_t sr_row_n(const QuantJob& j, int64_t n) {
+  return (uint64_t)(n + j.sr_row_off);
+}
+__host__ __device__ __forceinline__ uint64_t sr_col_n(const QuantJob& j, int64_t gk, int64_t m) {
+  return (uint64_t)(j.sr_col_off + gk * j.sr_col_ld + m);
+}
 
 struct DequantJob {
   const uint8_t* codes;
@@ -144,5 +155,15 @@ cudaError_t launch_mxfp4(const MxJob& j, cudaStream_t st);
 cudaError_t launch_mxfp8(const QuantJob& j, cudaStream_t st);
 // grouped path: offsets check + tile prefix (+ per-group amax for tensorwise)
 cudaError_t launch_group_prep(const QuantJob& j, int align, bool amax, cudaStream_t st);
+
+// Bounded-wait timeout flags of the TMA-fed kernels, one per translation
+// unit that has such waits: read (and optionally clear) the flag of the
+// current device (synchronous copies), or set it as a timed-out wait would.
+cudaError_t ctb_timeout_flag(uint32_t* v, bool clear);
+cudaError_t ctb_grouped_timeout_flag(uint32_t* v, bool clear);
+cudaError_t ctb_rht_timeout_flag(uint32_t* v, bool clear);
+cudaError_t row_timeout_flag(uint32_t* v, bool clear);
+cudaError_t ct_timeout_flag(uint32_t* v, bool clear);
+cudaError_t set_ctb_timeout_flag();
 
 }  // namespace fp4q

@@ -28,7 +28,10 @@ void* g_scratch_addr[kMaxDevices] = {nullptr};
 
 // Device address of g_noalloc_scratch on the current device.  Looked up once
 // per device with that device current (the symbol's host-side name is only a
-// stand-in and must never be handed to a kernel).
+// stand-in and must never be handed to a kernel).  The address belongs to
+// the device's primary context, the one the CUDA runtime (and torch) uses;
+// after cudaDeviceReset, or from another context on the same device, it is
+// not valid.
 int scratch_address(void** addr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4Q_ERR_CUDA;
@@ -50,6 +53,9 @@ extern "C" int fp4_quantize_noalloc(const fp4q_params_t* p, const void* x, const
   fp4q_sizes_t s;
   int rc = fp4q_query_sizes(p, &s);
   if (rc != FP4Q_OK) return rc;
+  // a precomputed tensorwise amax travels in the caller's workspace, which
+  // this entry point does not take
+  if (p->precomputed_amax) return FP4Q_ERR_UNSUPPORTED;
   if (s.workspace > (size_t)FP4Q_NOALLOC_SCRATCH_BYTES) return FP4Q_ERR_WORKSPACE;
   void* ws = nullptr;
   if (s.workspace > 0) {

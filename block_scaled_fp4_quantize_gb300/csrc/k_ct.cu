@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
         if (staged) stage_block<IN_BF16>(xs, row, b, x);
         if (j.do_row) {
           float deq[16];
-          if (deq_row) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, (uint64_t)n0, cw[2 * q], cw[2 * q + 1], deq);
-          else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, (uint64_t)n0, cw[2 * q], cw[2 * q + 1], deq);
+          if (deq_row) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, n0), cw[2 * q], cw[2 * q + 1], deq);
+          else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, n0), cw[2 * q], cw[2 * q + 1], deq);
           scw |= sc << (8 * q);
           if (valid) {
             if (j.residual) {
@@ -600,10 +600,11 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
         sc = block_scale<UE5M3>(tv, cam[q], n, T);
         normalize16<SR>(v, x, n);
       }
-      const int64_t n0 = cbase + (int64_t)col * M32 + rbeg + 16 * q;
+      // SR index of the column block: row g K + k0 + col of x transposed
+      const uint64_t n0 = sr_col_n(j, p.g * j.K + p.k0 + col, p.m0 + rbeg + 16 * q);
       float deq[16];
-      if (j.qdq_orient == 2) encode16<SR, true>(x, T, n, j.seed, j.step, 1u, (uint64_t)n0, ccw[2 * q], ccw[2 * q + 1], deq);
-      else encode16<SR, false>(x, T, n, j.seed, j.step, 1u, (uint64_t)n0, ccw[2 * q], ccw[2 * q + 1], deq);
+      if (j.qdq_orient == 2) encode16<SR, true>(x, T, n, j.seed, j.step, 1u, n0, ccw[2 * q], ccw[2 * q + 1], deq);
+      else encode16<SR, false>(x, T, n, j.seed, j.step, 1u, n0, ccw[2 * q], ccw[2 * q + 1], deq);
       cscw |= sc << (8 * q);
       if (j.qdq_orient == 2 && kvalid && mb < j.M) {
 #pragma unroll
@@ -704,6 +705,15 @@ bool ct_supports(const QuantJob& j) {
 cudaError_t launch_ct(const QuantJob& j, cudaStream_t st) {
   if (j.in_bf16) return j.sr ? launch_c<true, true>(j, st) : launch_c<true, false>(j, st);
   return j.sr ? launch_c<false, true>(j, st) : launch_c<false, false>(j, st);
+}
+
+cudaError_t ct_timeout_flag(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_tile_timeout, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_tile_timeout, &z, sizeof z);
+  }
+  return e;
 }
 
 }  // namespace fp4q

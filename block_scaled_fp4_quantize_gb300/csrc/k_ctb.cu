@@ -41,4 +41,11 @@ bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   return launch_ctb_all<false, false>(j, st, err);
 }
 
+cudaError_t ctb_timeout_flag(uint32_t* v, bool clear) { return ctb_flag_rw(v, clear); }
+
+cudaError_t set_ctb_timeout_flag() {
+  const uint32_t one = 1;
+  return cudaMemcpyToSymbol(g_ctb_timeout, &one, sizeof one);
+}
+
 }  // namespace fp4q

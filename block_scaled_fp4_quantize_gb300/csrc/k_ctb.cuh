@@ -40,7 +40,19 @@ struct BL {
 // Outer-scale source of a launch
 enum BOuter : int { BO_NONE = 0, BO_UNIFORM, BO_T1D, BO_T2D, BO_B1D, BO_B2D };
 
+// Set by a tile wait that ran out (one flag per translation unit that
+// includes this body); read and cleared from the host by fp4q_device_status.
 __device__ unsigned int g_ctb_timeout = 0;
+
+// Host side: this translation unit's flag on the current device.
+inline cudaError_t ctb_flag_rw(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_ctb_timeout, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_ctb_timeout, &z, sizeof z);
+  }
+  return e;
+}
 
 __device__ __forceinline__ void issue_bf16_tile(const CUtensorMap* map, const TilePos& p, unsigned char* raw,
                                                 uint64_t* bar) {
@@ -406,7 +418,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
           float u[16];
           row_u(b, u);
           scw |= block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE>(tab, u, ab[b], S[b], R[b], j.seed, j.step, 0u,
-                                                                      (uint64_t)(rel + 16 * b), cw[2 * b],
+                                                                      sr_row_n(j, rel + 16 * b), cw[2 * b],
                                                                       cw[2 * b + 1])
                  << (8 * b);
         }
@@ -416,7 +428,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
           float u[16];
           row_u(b, u);
           scw |= quant_block<SR, UE5M3, BO != BO_NONE>(tab, u, am[b], S[b], R[b], none, j, 0u,
-                                                       (uint64_t)(rel + 16 * b), cw[2 * b], cw[2 * b + 1])
+                                                       sr_row_n(j, rel + 16 * b), cw[2 * b], cw[2 * b + 1])
                  << (8 * b);
         }
       }
@@ -537,6 +549,13 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         u[i] = RHT ? (c ? z1[i] : z0[i])
                    : (BO == BO_NONE ? (c ? bf16hi(wv[i]) : bf16lo(wv[i])) : (c ? nbf16hi(wv[i]) : nbf16lo(wv[i])));
     };
+    // SR index of column 2 lane + c's block: the group's own flat index in
+    // the concatenated group transposes, else the global index of x
+    // transposed (row g K + k)
+    auto col_sr = [&](int c) -> uint64_t {
+      const int64_t k = p.k0 + 2 * lane + c;
+      return GR ? (uint64_t)(cbase + k * cstride + mb) : sr_col_n(j, p.g * K + k, mb);
+    };
     // codes of column 2 lane + c, rows 16 warp .. + 15: row 2 lane + c of
     // the tensor-store box at byte 8 warp, whose 16-byte chunk index the
     // 64-byte swizzle XORs with (row / 2) mod 4 = lane mod 4; or the padded
@@ -556,8 +575,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         col_u(c, u);
         uint32_t w0, w1;
         const uint32_t sc = block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE && !RHT>(
-            tab, u, ac[c], S[c], R[c], j.seed, j.step, 1u, (uint64_t)(cbase + (p.k0 + 2 * lane + c) * cstride + mb),
-            w0, w1);
+            tab, u, ac[c], S[c], R[c], j.seed, j.step, 1u, col_sr(c), w0, w1);
         col_stage(c, w0, w1, sc);
       }
     } else {
@@ -567,7 +585,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         col_u(c, u);
         uint32_t w0, w1;
         const uint32_t sc = quant_block<SR, UE5M3, BO != BO_NONE && !RHT>(
-            tab, u, cam[c], S[c], R[c], none, j, 1u, (uint64_t)(cbase + (p.k0 + 2 * lane + c) * cstride + mb), w0, w1);
+            tab, u, cam[c], S[c], R[c], none, j, 1u, col_sr(c), w0, w1);
         col_stage(c, w0, w1, sc);
       }
     }

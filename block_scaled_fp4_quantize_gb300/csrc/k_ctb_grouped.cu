@@ -9,4 +9,6 @@ bool launch_ctb_grouped(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   return launch_ctb_all<true, false>(j, st, err);
 }
 
+cudaError_t ctb_grouped_timeout_flag(uint32_t* v, bool clear) { return ctb_flag_rw(v, clear); }
+
 }  // namespace fp4q

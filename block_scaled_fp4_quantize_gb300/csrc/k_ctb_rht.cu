@@ -14,4 +14,6 @@ bool launch_ctb_rht(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   return launch_ctb_all<false, true>(j, st, err);
 }
 
+cudaError_t ctb_rht_timeout_flag(uint32_t* v, bool clear) { return ctb_flag_rw(v, clear); }
+
 }  // namespace fp4q

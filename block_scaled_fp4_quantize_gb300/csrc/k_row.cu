@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(RT) row_kernel(const QuantJob j) {
         sc = block_scale<UE5M3>(tv, am, n, T);
         float x[16];
         normalize16<SR>(u, x, n);
-        if (deq) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, (uint64_t)(16 * b[q]), w0, w1, dq);
-        else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, (uint64_t)(16 * b[q]), w0, w1, dq);
+        if (deq) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, 16 * b[q]), w0, w1, dq);
+        else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, 16 * b[q]), w0, w1, dq);
       }
       if (!valid[q]) continue;
       if (j.row_codes) {
@@ -449,6 +449,15 @@ cudaError_t launch_row(const QuantJob& j, cudaStream_t st) {
   if (j.in_bf16 && !j.sr && !j.residual && j.qdq_orient == 0 && j.row_codes && j.G * j.M * j.K > 0)
     return j.ue5m3 ? launch_row_bulk_o<true>(j, st) : launch_row_bulk_o<false>(j, st);
   return j.in_bf16 ? launch_row_d<true>(j, st) : launch_row_d<false>(j, st);
+}
+
+cudaError_t row_timeout_flag(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_row_timeout, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_row_timeout, &z, sizeof z);
+  }
+  return e;
 }
 
 }  // namespace fp4q

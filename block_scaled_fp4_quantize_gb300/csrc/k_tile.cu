@@ -319,8 +319,8 @@ __global__ void __launch_bounds__(NTHR) quant_tile_kernel(const QuantJob j) {
       float deq[16];
       const uint64_t n0 = (uint64_t)((g * j.M + m) * j.K + kb);
       SegOut o;
-      if (deq_row) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, n0, deq);
-      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, n0, deq);
+      if (deq_row) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, sr_row_n(j, (int64_t)n0), deq);
+      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, sr_row_n(j, (int64_t)n0), deq);
       if (valid) {
         if (j.row_codes) *reinterpret_cast<uint2*>(j.row_codes + n0 / 2) = make_uint2(o.codes_lo, o.codes_hi);
         if (j.row_scales) j.row_scales[sf_offset(j.rsl, g, m, kb / 16)] = (uint8_t)o.sc;
@@ -377,8 +377,9 @@ __global__ void __launch_bounds__(NTHR) quant_tile_kernel(const QuantJob j) {
       float deq[16];
       const uint64_t n0 = (uint64_t)((g * j.K + k) * j.M + mb);
       SegOut o;
-      if (qdq_col) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, n0, deq);
-      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, n0, deq);
+      const uint64_t nsr = sr_col_n(j, g * j.K + k, mb);
+      if (qdq_col) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, nsr, deq);
+      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, nsr, deq);
       if (valid) {
         if (j.col_codes) *reinterpret_cast<uint2*>(j.col_codes + n0 / 2) = make_uint2(o.codes_lo, o.codes_hi);
         if (j.col_scales) j.col_scales[sf_offset(j.csl, g, k, mb / 16)] = (uint8_t)o.sc;

@@ -18,7 +18,8 @@
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates, frees or synchronizes; work is enqueued on `stream`
+ *     never allocates or frees, and synchronizes only in fp4q_device_status;
+ *     work is enqueued on `stream`
  *     (a cudaStream_t passed as void*, NULL = the legacy default stream) and
  *     runs asynchronously.  Input buffers are read-only; output buffers must
  *     not alias inputs or one another.
@@ -42,7 +43,7 @@
 extern "C" {
 #endif
 
-#define FP4Q_ABI_VERSION 3
+#define FP4Q_ABI_VERSION 4
 
 /* ---- status codes ------------------------------------------------------ */
 #define FP4Q_OK 0
@@ -55,6 +56,7 @@ extern "C" {
 #define FP4Q_ERR_CUDA (-7)        /* a CUDA launch or call failed                  */
 #define FP4Q_ERR_ABI (-8)         /* struct_size does not match this library       */
 #define FP4Q_ERR_ALIGN (-9)       /* an output buffer is not naturally aligned     */
+#define FP4Q_ERR_TIMEOUT (-10)    /* a kernel's bounded wait ran out (fp4q_device_status) */
 
 /* ---- enumerations -------------------------------------------------------- */
 #define FP4Q_BF16 1
@@ -89,7 +91,12 @@ extern "C" {
  *     use_precomputed_outer must be 0 in mode none (the same page,
  *     "Implementation": outer-side knobs outside outer-block mode are
  *     rejected);
- *   in_dtype and out_dtype are FP4Q_BF16 or FP4Q_FP32. */
+ *   in_dtype and out_dtype are FP4Q_BF16 or FP4Q_FP32;
+ *   precomputed_amax only in tensorwise mode and not together with
+ *     use_precomputed_outer;
+ *   sr_global_rows, sr_row_offset, sr_matrix_offset >= 0 and
+ *     sr_row_offset + M <= sr_global_rows (when nonzero); with G > 1,
+ *     sr_global_rows must be 0 or M (FP4Q_ERR_UNSUPPORTED otherwise). */
 typedef struct fp4q_params {
   uint32_t struct_size; /* = sizeof(fp4q_params_t); FP4Q_ERR_ABI otherwise        */
   uint32_t out_mask;    /* FP4Q_OUT_ROW | FP4Q_OUT_COL (quantize)                  */
@@ -114,6 +121,26 @@ typedef struct fp4q_params {
   int32_t col_hadamard; /* 1: random Hadamard transform along M before the
                            columnwise quantization (fp4_quantize, below)    */
   uint32_t hadamard_signs; /* bits 0-15: sign mask of that transform         */
+  int32_t precomputed_amax; /* tensorwise mode: 1 = the first 4 bytes of the
+                               workspace already hold the amax of the whole
+                               tensor (a binary32, e.g. the maximum over the
+                               row shards of a tensor split across processes,
+                               each from fp4_tensor_amax); the amax pass is
+                               skipped and S = amax / (scale_max * 6) is
+                               computed on the device and written to the
+                               tensorwise scale buffer                       */
+  /* Global index of the stochastic-rounding counter ("fp4-train" README,
+   * "Method": the random draw is keyed on (seed, step, global-index)).  When
+   * this call quantizes the block [sr_matrix_offset : + G, sr_row_offset : + M,
+   * 0 : K] of a larger tensor [*, sr_global_rows, K] (a shard), every element
+   * draws the word its position has in that tensor:
+   *   rowwise     ((g0 + g) * Mg + r0 + m) * K + k
+   *   columnwise  ((g0 + g) * K + k) * Mg + r0 + m   (the tensor transposed)
+   * with g0 = sr_matrix_offset, r0 = sr_row_offset and Mg = sr_global_rows
+   * (0: this call's M).  All zero: the call's own tensor. */
+  int64_t sr_global_rows;
+  int64_t sr_row_offset;
+  int64_t sr_matrix_offset;
 } fp4q_params_t;
 
 /* Inner-scale layouts.  An orientation's scales form, per matrix g, an
@@ -185,9 +212,11 @@ int fp4q_query_sizes(const fp4q_params_t *p, fp4q_sizes_t *sizes);
  *   buffer, rowwise only (FP4Q_ERR_UNSUPPORTED with FP4Q_OUT_COL); it is
  *   added to x before quantization and replaced by u - dequantize(q) (fp4-train
  *   README, "API": quantize(x, stochastic, residual, seed, step)).
- * workspace: device scratch of at least sizes.workspace bytes (256-byte
- *   aligned; only tensorwise mode without a precomputed scale needs any).
- *   Returns FP4Q_ERR_WORKSPACE if missing or too small. */
+ * workspace: device scratch of at least sizes.workspace bytes (16-byte
+ *   aligned; only tensorwise mode without a precomputed scale needs any:
+ *   its first 4 bytes receive the tensor's amax, or hold it already with
+ *   p->precomputed_amax).  Returns FP4Q_ERR_WORKSPACE if missing or too
+ *   small. */
 int fp4_quantize(const fp4q_params_t *p, const void *x, const fp4q_outputs_t *out, float *residual,
                  void *workspace, size_t workspace_bytes, void *stream);
 /* With p->col_hadamard = 1 the columnwise side quantizes z instead of u:
@@ -350,9 +379,31 @@ int mxfp4_fake_quantize_host(const fp4q_params_t *p, const void *x, void *y, voi
  *   device current); make that first call before any stream capture.
  *   All calls share the array and leave their last contents in it; the part
  *   that must start at zero is cleared by every call, but calls that overlap
- *   on the GPU (for example on two streams) race on it. */
+ *   on the GPU (for example on two streams) race on it.
+ *   The address looked up is the one of the device's primary context (the
+ *   context the CUDA runtime uses); the entry point is not for other
+ *   contexts, nor for use after cudaDeviceReset.  p->precomputed_amax is
+ *   rejected (FP4Q_ERR_UNSUPPORTED): that amax travels in a workspace. */
 int fp4_quantize_noalloc(const fp4q_params_t *p, const void *x, const fp4q_outputs_t *out, float *residual,
                          void *stream);
+
+/* Device-side failure status of the kernels' bounded waits.  The TMA-fed
+ * kernels wait on shared-memory barriers for their tile copies with an
+ * iteration limit; a wait that runs out sets a flag in device memory and the
+ * kernel goes on (its outputs are then not to be trusted) instead of hanging
+ * the GPU.  This call waits for `stream` (a cudaStream_t as void*, NULL =
+ * the legacy default stream) to finish -- the one entry point that
+ * synchronizes -- then reads the flags of the current device and, if
+ * `clear` is nonzero, resets them.  Returns FP4Q_ERR_TIMEOUT if any wait ran
+ * out since the flags were last cleared, FP4Q_ERR_CUDA if the stream or the
+ * copies failed, else FP4Q_OK.  The flags are per device and shared by all
+ * calls in the process. */
+int fp4q_device_status(int clear, void *stream);
+
+/* Sets the flag a timed-out wait of the tile kernels sets, on the current
+ * device, without running any kernel: for testing the status path of
+ * fp4q_device_status on a healthy GPU.  Returns FP4Q_OK or FP4Q_ERR_CUDA. */
+int fp4q_set_device_timeout_flag(void);
 
 /* Static string naming a status code. */
 const char *fp4q_status_string(int status);

@@ -16,6 +16,9 @@ binary32 as ``np.float32``.  Shapes follow the library's layout:
 * outer scales: 1-D rowwise ``[G, M, K/ob]``, 1-D columnwise ``[G, K, M/ob]``,
   2-D ``[G, M/ob, K/ob]`` (shared), tensorwise ``[1]``
 
+* inner scales in the tensor-core layout (``scale_layout_mma``): flat bytes,
+  128 x 4 blocks of 512 bytes per matrix
+
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 except the Philox stream beyond its published known-answer vectors and the
 statistics of stochastic rounding ("parity unpinned" for the exact SR word
@@ -113,6 +116,8 @@ def _lib():
         L.orc_mxfp4_project_mxfp8.argtypes = [ctypes.POINTER(Cfg), P, P, P, P, P, P]
         L.orc_rht16.restype = None
         L.orc_rht16.argtypes = [P, ctypes.c_uint32, ctypes.c_int32]
+        L.orc_scale_layout_mma.restype = None
+        L.orc_scale_layout_mma.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, P]
         L.orc_subnormals_ok.restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -275,6 +280,19 @@ def mxfp4_project_mxfp8(x, K=None, *, out_dtype=None, out_mask=ROW | COL, with_y
     rc = _lib().orc_mxfp4_project_mxfp8(ctypes.byref(cfg), _ptr(x), _ptr(out["y"]), _ptr(out["row_codes"]),
                                        _ptr(out["row_scales"]), _ptr(out["col_codes"]), _ptr(out["col_scales"]))
     assert rc == 0
+    return out
+
+
+def scale_layout_mma(lin):
+    """An orientation's [G, R, C] (or [R, C]) linear inner-scale bytes in the
+    tensor-core layout (128 x 4 blocks of 512 bytes, zero padding); returns
+    the flat byte buffer."""
+    a = np.ascontiguousarray(lin, np.uint8)
+    if a.ndim == 2:
+        a = a[None]
+    G, R, C = a.shape
+    out = np.zeros(G * (-(-R // 128)) * (-(-C // 4)) * 512, np.uint8)
+    _lib().orc_scale_layout_mma(_ptr(a), G, R, C, _ptr(out))
     return out
 
 

@@ -666,6 +666,34 @@ int orc_mxfp4_project_mxfp8(const orc_cfg *cf, const void *x, void *y, uint8_t *
   return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Inner scales in the layout NVFP4 tensor cores read ([FP4T] "Method": the  */
+/* block scales are stored "the layout NVFP4 tensor cores read").  The pages */
+/* do not spell that layout out; this is NVIDIA's published one (cuBLAS      */
+/* documentation, "1D Block Scaling Factors Layout"): an orientation's R x C */
+/* matrix of scale bytes (R rows, C = scales per row) is padded with zero    */
+/* bytes to a multiple of 128 rows and of 4 columns and cut into 128 x 4     */
+/* blocks; the blocks are stored one after another, 512 bytes each, in      */
+/* row-major order of (row block, column block); inside a block the rows    */
+/* are taken as 4 groups of 32 and the byte of row r, column c sits at      */
+/* 16 * (r mod 32) + 4 * (r div 32) + c, so one 16-byte line holds the 4    */
+/* columns of the rows r, r + 32, r + 64 and r + 96.  G matrices follow one */
+/* another, each padded.  lin is [G, R, C] row-major; out receives          */
+/* G * ceil(R/128) * ceil(C/4) * 512 bytes.                                  */
+/* ------------------------------------------------------------------------ */
+void orc_scale_layout_mma(const uint8_t *lin, int64_t G, int64_t R, int64_t C, uint8_t *out) {
+  int64_t row_blocks = (R + 127) / 128, col_blocks = (C + 3) / 4;
+  memset(out, 0, (size_t)(G * row_blocks * col_blocks * 512));
+  for (int64_t g = 0; g < G; g++)
+    for (int64_t r = 0; r < R; r++)
+      for (int64_t c = 0; c < C; c++) {
+        int64_t block = (g * row_blocks + r / 128) * col_blocks + c / 4;
+        int64_t rr = r % 128, cc = c % 4;
+        int64_t inside = 16 * (rr % 32) + 4 * (rr / 32) + cc;
+        out[block * 512 + inside] = lin[(g * R + r) * C + c];
+      }
+}
+
 /* Startup check used by the tests: subnormals survive a multiply (no
  * flush-to-zero in this process). */
 int orc_subnormals_ok(void) {

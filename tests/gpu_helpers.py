@@ -1,5 +1,10 @@
 """Shared helpers of the GPU parity tests: run the CUDA path and the oracle on
 the same host bytes and compare their outputs bit for bit."""
+import functools
+import multiprocessing
+import os
+from concurrent.futures import ProcessPoolExecutor
+
 import numpy as np
 import torch
 
@@ -90,3 +95,28 @@ def to_mma_layout(lin: np.ndarray) -> np.ndarray:
     pad[:, :R, :C] = lin
     t = pad.reshape(G, Rp // 128, 4, 32, Cp // 4, 4)          # g, tile row, r // 32, r % 32, tile col, c
     return np.ascontiguousarray(t.transpose(0, 1, 4, 3, 2, 5)).reshape(-1)
+
+
+MOE_KW = dict(mode="outer_block", outer_block_size=64, outer_2d=True, rowwise=True, columnwise=True)
+
+
+def _moe_expert_oracle(args):
+    """Worker: the oracle's quantize of MoE expert e (2-D 64 x 64 outer
+    scales, both orientations) in scale format fmt."""
+    e, fmt = args
+    import oracle
+    from block_scaled_fp4_quantize_gb300 import workloads as W
+
+    x = host_np(W.moe_expert(e))[None]
+    r = oracle.quantize(x, out_mask=ROW | COL, **oracle_kw(dict(MOE_KW, scale_format=fmt)))
+    return e, {k: v for k, v in r.items() if v is not None}
+
+
+@functools.lru_cache(maxsize=2)
+def moe_oracle(fmt: str, experts: int = 32):
+    """The oracle's outputs for every expert of the MoE workload, computed
+    once per format by a pool of spawned processes over the host cores
+    (spawned, not forked: the parent process holds a CUDA context)."""
+    workers = max(1, min(experts, os.cpu_count() or 1, 16))
+    with ProcessPoolExecutor(max_workers=workers, mp_context=multiprocessing.get_context("spawn")) as ex:
+        return dict(ex.map(_moe_expert_oracle, [(e, fmt) for e in range(experts)]))

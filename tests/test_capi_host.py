@@ -36,7 +36,7 @@ def test_header_declares_the_bound_functions():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.fp4q_abi_version() == 3
+    assert lib.fp4q_abi_version() == 4
     out = os.popen("nm -D --defined-only %s" % _capi._build.lib_path()).read()
     for name in declared_functions():
         assert re.search(r"\sT\s%s$" % name, out, re.M), name
@@ -45,8 +45,9 @@ def test_library_exports_every_declared_symbol(lib):
 def test_params_struct_layout_matches(lib):
     p = _capi.Params()
     lib.fp4q_params_init(ctypes.byref(p))
-    assert p.struct_size == ctypes.sizeof(_capi.Params) == 104
+    assert p.struct_size == ctypes.sizeof(_capi.Params) == 128
     assert (p.G, p.in_dtype, p.out_dtype, p.mode, p.out_mask, p.scale_layout) == (1, _capi.BF16, _capi.BF16, 0, 1, 0)
+    assert (p.precomputed_amax, p.sr_global_rows, p.sr_row_offset, p.sr_matrix_offset) == (0, 0, 0, 0)
     assert ctypes.sizeof(_capi.Outputs) == 7 * 8 and ctypes.sizeof(_capi.Sizes) == 8 * 8
 
 
@@ -100,6 +101,15 @@ def test_query_sizes(lib):
     (dict(scale_format=3), -4),
     (dict(rounding=2), -4),
     (dict(struct_size=80), -8),
+    (dict(struct_size=104), -8),                           # the previous ABI's struct
+    (dict(precomputed_amax=1), -4),                        # precomputed amax outside tensorwise mode
+    (dict(mode=1, precomputed_amax=1, use_precomputed_outer=1), -4),
+    (dict(mode=1, precomputed_amax=2), -4),
+    (dict(sr_global_rows=-1), -3),                         # SR counter's global index
+    (dict(sr_global_rows=200, sr_row_offset=100), -3),     # rows 100 .. 228 of 200
+    (dict(sr_row_offset=4), -3),                           # an offset needs the global row count
+    (dict(sr_matrix_offset=-2), -3),
+    (dict(G=2, sr_global_rows=512), -5),                   # several matrices must be whole
 ])
 def test_validation_codes(lib, kw, code):
     rc, _ = sizes(lib, **kw)

@@ -1,7 +1,7 @@
 """Inner scales in the tensor-core (128 x 4 tiled) layout: every kernel path
-writes the same bytes as the linear layout rearranged by the layout's
-definition (padding zero), codes unchanged; dequantize reads the layout; and
-NVFP4 GEMMs in torch (cuBLASLt) consume codes and scales as written."""
+writes the oracle's scales in the oracle's statement of the layout (padding
+zero), codes unchanged; dequantize reads the layout; and NVFP4 GEMMs in torch
+(cuBLASLt) consume the codes and scales of to_fp4_operands as written."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +9,7 @@ import torch
 import block_scaled_fp4_quantize_gb300 as fq
 from block_scaled_fp4_quantize_gb300 import workloads as W
 
-from gpu_helpers import host_np, to_mma_layout
+from gpu_helpers import host_np, oracle_quantize
 
 pytestmark = pytest.mark.gpu
 
@@ -41,21 +41,23 @@ CASES = [dict(mode="none"), dict(mode="tensorwise"), dict(mode="outer_block", ou
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("shape", [(1, 208, 320), (2, 256, 448), (1, 96, 64)], ids=["pad-rows", "g2", "small"])
 @pytest.mark.parametrize("case", CASES, ids=["none", "tensorwise", "ob64", "ob32-2d", "inner2d", "sr"])
-def test_mma_layout_equals_rearranged_linear(case, shape, dtype, kernel):
+def test_mma_layout_equals_oracle(orc, case, shape, dtype, kernel):
     G, M, K = shape
     ob = case.get("outer_block_size", 0)
     if ob and (K % ob or M % ob):
         pytest.skip("shape not divisible by the outer block")
-    x = W.lognormal(shape, 61, sigma=3.0, dtype=dtype).cuda()
+    xc = W.lognormal(shape, 61, sigma=3.0, dtype=dtype)
+    x = xc.cuda()
     for mask in ((True, False), (False, True), (True, True)):
         kw = dict(case, rowwise=mask[0], columnwise=mask[1])
         lin = fq.quantize(x, **kw)
         mma = fq.quantize(x, scale_layout="mma", **kw)
+        ref = oracle_quantize(orc, xc, **kw)
         for o in ("row", "col"):
             if getattr(lin, o + "_codes") is None:
                 continue
-            assert torch.equal(getattr(mma, o + "_codes"), getattr(lin, o + "_codes"))
-            want = to_mma_layout(host_np(getattr(lin, o + "_scales")))
+            assert (host_np(getattr(mma, o + "_codes")) == ref[o + "_codes"]).all(), (o, kw)
+            want = orc.scale_layout_mma(ref[o + "_scales"])
             got = host_np(getattr(mma, o + "_scales"))
             assert got.shape == want.shape and (got == want).all(), (o, kw)
             y_lin = fq.dequantize(lin, o, torch.float32)
@@ -63,44 +65,57 @@ def test_mma_layout_equals_rearranged_linear(case, shape, dtype, kernel):
             assert torch.equal(y_lin.view(torch.int32), y_mma.view(torch.int32))
 
 
-def test_mma_layout_padding_is_zero_on_reused_buffers():
+def test_mma_layout_padding_is_zero_on_reused_buffers(orc):
     """Padding bytes are cleared by every call, also in a reused buffer."""
-    x = W.lognormal((1, 208, 336), 62, sigma=2.0).cuda()
+    xc = W.lognormal((1, 208, 336), 62, sigma=2.0)
+    x = xc.cuda()
     q = fq.quantize(x, scale_layout="mma", rowwise=True, columnwise=True)
     q.row_scales.fill_(0xAB)
     q.col_scales.fill_(0xCD)
     fq.quantize(x, scale_layout="mma", rowwise=True, columnwise=True, out=q)
-    lin = fq.quantize(x, rowwise=True, columnwise=True)
-    assert (host_np(q.row_scales) == to_mma_layout(host_np(lin.row_scales))).all()
-    assert (host_np(q.col_scales) == to_mma_layout(host_np(lin.col_scales))).all()
+    ref = oracle_quantize(orc, xc, rowwise=True, columnwise=True)
+    assert (host_np(q.row_scales) == orc.scale_layout_mma(ref["row_scales"])).all()
+    assert (host_np(q.col_scales) == orc.scale_layout_mma(ref["col_scales"])).all()
 
 
-def _scaled_mm_nvfp4(a_codes, a_scales, b_codes, b_scales):
+def _scaled_mm_nvfp4(a, b):
     if not hasattr(torch, "float4_e2m1fn_x2"):
         pytest.skip("torch has no float4_e2m1fn_x2")
-    A = a_codes.view(torch.float4_e2m1fn_x2)
-    B = b_codes.view(torch.float4_e2m1fn_x2)
     try:
-        return torch._scaled_mm(A, B.t(), a_scales.view(torch.float8_e4m3fn), b_scales.view(torch.float8_e4m3fn),
-                                out_dtype=torch.bfloat16)
+        return torch._scaled_mm(a.codes, b.codes.t(), a.scales, b.scales, out_dtype=torch.bfloat16)
     except (RuntimeError, TypeError, NotImplementedError) as e:
         pytest.skip("torch._scaled_mm has no NVFP4 path here: %s" % str(e).splitlines()[0][:120])
 
 
+def test_to_fp4_operands_types_and_bytes(orc):
+    """fp4-train README, "API": to_fp4_operands returns the packed codes and
+    the E4M3 scales as torch's FP4 / FP8 dtypes, scales in the tensor-core
+    layout; their bytes are the oracle's."""
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        pytest.skip("torch has no float4_e2m1fn_x2")
+    xc = W.lognormal((208, 320), 65, sigma=2.0)
+    for stochastic in (False, True):
+        op = fq.to_fp4_operands(xc.cuda(), stochastic=stochastic, seed=4, step=7)
+        assert op.codes.dtype == torch.float4_e2m1fn_x2 and tuple(op.codes.shape) == (208, 160)
+        assert op.scales.dtype == torch.float8_e4m3fn
+        ref = oracle_quantize(orc, xc, stochastic=stochastic, seed=4, step=7)
+        assert (host_np(op.codes.view(torch.uint8)) == ref["row_codes"][0]).all()
+        assert (host_np(op.scales.view(torch.uint8)) == orc.scale_layout_mma(ref["row_scales"])).all()
+
+
 @pytest.mark.parametrize("mnk", [(256, 384, 512), (208, 128, 320)], ids=["aligned", "padded"])
 def test_nvfp4_gemm_reads_the_layout(mnk):
-    """A block-scaled FP4 GEMM (cuBLASLt through torch) reads our codes and
-    MMA-layout scales: its result equals the product of the dequantized
+    """A block-scaled FP4 GEMM (cuBLASLt through torch) reads the operands of
+    to_fp4_operands: its result equals the product of the dequantized
     operands up to binary32 accumulation order and the bf16 output rounding.
     A misplaced scale would change results by factors of 2 or more."""
     M, N, K = mnk
     a = W.lognormal((M, K), 63, sigma=2.0).cuda()
     b = W.lognormal((N, K), 64, sigma=2.0).cuda()
-    qa = fq.quantize(a, scale_layout="mma")
-    qb = fq.quantize(b, scale_layout="mma")
-    y = _scaled_mm_nvfp4(qa.row_codes[0], qa.row_scales, qb.row_codes[0], qb.row_scales)
-    da = fq.dequantize(qa, "row", torch.float32)[0].double()
-    db = fq.dequantize(qb, "row", torch.float32)[0].double()
+    oa, ob_ = fq.to_fp4_operands(a), fq.to_fp4_operands(b)
+    y = _scaled_mm_nvfp4(oa, ob_)
+    da = fq.dequantize(oa.quantized, "row", torch.float32)[0].double()
+    db = fq.dequantize(ob_.quantized, "row", torch.float32)[0].double()
     ref = da @ db.t()
     err = (y.double() - ref).abs()
     tol = 1e-2 * (da.abs() @ db.abs().t()) + 1e-30

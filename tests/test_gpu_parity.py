@@ -9,8 +9,8 @@ import torch
 import block_scaled_fp4_quantize_gb300 as fq
 from block_scaled_fp4_quantize_gb300 import workloads as W
 
-from gpu_helpers import (COL, ROW, assert_same, bf16_to_f32, gpu_quantize, host_np, oracle_kw, oracle_quantize,
-                         snr_db)
+from gpu_helpers import (COL, MOE_KW, ROW, assert_same, bf16_to_f32, gpu_quantize, host_np, moe_oracle, oracle_kw,
+                         oracle_quantize, snr_db)
 
 pytestmark = pytest.mark.gpu
 
@@ -423,19 +423,18 @@ def test_activations_full_size(orc, kernel):
 @pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
 def test_moe_experts_full_size(orc, fmt, kernel):
     """32 experts x bf16 [5760, 2880], 1 % outliers x 200: 2-D 64x64 outer
-    scales shared by rowwise and columnwise outputs; experts 0 and 31 are
-    checked against the oracle."""
+    scales shared by rowwise and columnwise outputs; every expert is checked
+    against the oracle (computed once per format over the host cores)."""
     G = 32
     x = torch.empty(G, 5760, 2880, dtype=torch.bfloat16)
     for e in range(G):
         x[e] = W.moe_expert(e)
-    kw = dict(mode="outer_block", outer_block_size=64, outer_2d=True, scale_format=fmt, rowwise=True,
-              columnwise=True)
-    q, g = gpu_quantize(x, **kw)
-    for e in (0, 31):
-        r = oracle_quantize(orc, x[e:e + 1], **kw)
+    q, g = gpu_quantize(x, scale_format=fmt, **MOE_KW)
+    ref = moe_oracle(fmt, G)
+    assert sorted(ref) == list(range(G))
+    for e in range(G):
         ge = {k: (None if v is None else v[e:e + 1]) for k, v in g.items()}
-        assert_same(ge, r)
+        assert_same(ge, ref[e])
 
 
 def test_sr_ef_weight_loop(orc):

@@ -865,3 +865,44 @@ def test_nonfinite_inputs_closed_form(orc, dtype, mx):
     qz = orc.quantize(z, mode="tensorwise")
     assert qz["tile_outer"][0] == 0.0 and not np.signbit(qz["tile_outer"][0])
     assert qz["row_scales"][0, 0, 0] == 0 and set(_unpack(qz["row_codes"])[0, 0]) == {0x0}
+
+
+# ----------------------------------------------------------------------------
+# inner scales in the tensor-core layout (NVIDIA's published block-scaling-
+# factor layout, read by block-scaled FP4 MMAs)
+# ----------------------------------------------------------------------------
+
+def test_scale_layout_mma_worked_positions(orc):
+    """Positions the cuBLAS description of the 128 x 4 block layout fixes:
+    within a 512-byte block, row r and column c go to 16 (r mod 32) +
+    4 (r div 32) + c; blocks follow in row-major order of (row block,
+    column block); a second matrix starts after the first one's blocks."""
+    G, R, C = 2, 200, 9            # 2 row blocks x 3 column blocks per matrix
+    lin = np.zeros((G, R, C), np.uint8)
+    want = {}
+    for (g, r, c), off in {(0, 0, 0): 0, (0, 0, 1): 1, (0, 1, 0): 16, (0, 31, 3): 16 * 31 + 3, (0, 32, 0): 4,
+                           (0, 96, 2): 14, (0, 127, 3): 511, (0, 0, 4): 512, (0, 0, 8): 1024,
+                           (0, 128, 0): 3 * 512, (0, 199, 5): 4 * 512 + 16 * (71 % 32) + 4 * (71 // 32) + 1,
+                           (1, 0, 0): 6 * 512, (1, 33, 6): 6 * 512 + 1 * 512 + 16 + 4 + 2}.items():
+        lin[g, r, c] = len(want) + 1
+        want[off] = len(want) + 1
+    out = orc.scale_layout_mma(lin)
+    assert out.size == G * 2 * 3 * 512
+    assert {int(i): int(out[i]) for i in np.flatnonzero(out)} == want
+
+
+def test_scale_layout_mma_is_a_zero_padded_permutation(orc):
+    """Every scale byte lands in exactly one place and every padding byte is
+    zero; the layout agrees with an independent formulation of the same
+    description (pad, cut into 128 x 4 blocks, interleave the four 32-row
+    groups of a block) written with array reshapes."""
+    from gpu_helpers import to_mma_layout
+
+    rng = np.random.default_rng(41)
+    for G, R, C in ((1, 128, 4), (2, 208, 20), (1, 33, 3), (3, 256, 180), (1, 5760, 180)):
+        lin = rng.integers(1, 256, size=(G, R, C), dtype=np.uint8)
+        out = orc.scale_layout_mma(lin)
+        assert out.size == G * (-(-R // 128)) * (-(-C // 4)) * 512
+        assert np.count_nonzero(out) == lin.size
+        assert np.array_equal(np.sort(out[out != 0]), np.sort(lin.ravel()))
+        np.testing.assert_array_equal(out, to_mma_layout(lin))

@@ -53,7 +53,7 @@ def test_shard_alignment():
     assert sharded.shard_alignment("tensorwise", inner_2d=True) == 16
 
 
-def _tensorwise_worker(rank, world, port, S_expected, fmt):
+def _tensorwise_worker(rank, world, port, amax_expected):
     dist.init_process_group("gloo", init_method="tcp://127.0.0.1:%d" % port, rank=rank, world_size=world)
     try:
         x = W.activations(M=512, K=256, n_cols=3, n_rows=1)
@@ -61,24 +61,26 @@ def _tensorwise_worker(rank, world, port, S_expected, fmt):
         x.view(-1)[300 * 256 + 5] = float("inf")  # in rank 1's rows
         lo, hi = sharded.row_range(x.shape[0], world, rank, 16)
         local = torch.tensor([_np_amax_bf16(x[lo:hi])], dtype=torch.float32)
-        S = sharded.tensorwise_scale(local, fmt)
-        assert S.dtype == torch.float32 and S.shape == (1,)
-        assert S.view(torch.int32).item() == np.float32(S_expected).view(np.int32), (rank, S.item(), S_expected)
+        a = sharded.allreduce_amax(local)
+        assert a is local and a.dtype == torch.float32 and a.shape == (1,)
+        assert a.view(torch.int32).item() == np.float32(amax_expected).view(np.int32), (rank, a.item(), amax_expected)
     finally:
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
-def test_tensorwise_scale_allreduce_two_ranks(orc, fmt):
-    """The all-reduced shard amax gives the oracle's tensorwise scale of the
-    whole tensor, bit for bit, on both ranks."""
+@pytest.mark.parametrize("fmt,denom", [("e4m3", 2688.0), ("ue5m3", 688128.0)])
+def test_tensorwise_amax_allreduce_two_ranks(orc, fmt, denom):
+    """The all-reduced shard amax is the whole tensor's, bit for bit, on both
+    ranks: divided by scale_max * 6 it gives the oracle's tensorwise scale
+    of the whole tensor (the library does that division on the device)."""
     x = W.activations(M=512, K=256, n_cols=3, n_rows=1)
     x.view(-1)[7] = float("nan")
     x.view(-1)[300 * 256 + 5] = float("inf")
     xb = x.view(torch.int16).numpy().view(np.uint16)[None]
     ref = orc.quantize(xb, mode="tensorwise", fmt=fmt, out_mask=1)
-    S_expected = float(ref["tile_outer"].reshape(-1)[0])
-    mp.spawn(_tensorwise_worker, args=(2, _free_port(), S_expected, fmt), nprocs=2, join=True)
+    amax = np.float32(_np_amax_bf16(x))
+    assert (amax / np.float32(denom)).view(np.uint32) == ref["tile_outer"].reshape(-1)[0].view(np.uint32)
+    mp.spawn(_tensorwise_worker, args=(2, _free_port(), float(amax)), nprocs=2, join=True)
 
 
 def _bench_dist_worker(rank, world, port):
