@@ -175,17 +175,85 @@ def ncu_traffic(kernel_key: str):
 # workloads (CUDA path)
 # ---------------------------------------------------------------------------
 
-def _events_time(fn, iters, warmup):
-    """Average ms per call of fn(i) with CUDA events on the current stream."""
+def _warm(fn, warmup, min_seconds=0.5):
+    """At least `warmup` calls, and calls for at least `min_seconds`, so the
+    GPU's clocks and the memory system reach steady state right before the
+    timed region (no idle gap follows)."""
     import torch
 
-    for i in range(warmup):
+    i = 0
+    t0 = time.perf_counter()
+    while i < warmup or time.perf_counter() - t0 < min_seconds:
         fn(i)
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    return i
+
+
+class StepGraph:
+    """`fn(i)` for i = 0 .. n-1 captured as CUDA graphs: one graph of up to
+    `chunk` consecutive calls replayed as often as needed, plus one graph
+    for the remainder, so that exactly n calls run.  The replays enqueue the
+    same kernels the eager calls do, without the Python launch path between
+    them (host-side hiccups then cannot leave the GPU idle inside the timed
+    region).  `ok` is False when capture failed (run eagerly then)."""
+
+    def __init__(self, fn, n, chunk=100):
+        import torch
+
+        self.fn, self.n, self.ok = fn, n, False
+        self.chunk = max(1, min(n, chunk))
+        self.reps, rem = divmod(n, self.chunk)
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                for i in range(3):
+                    fn(i)
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            self.g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g):
+                for i in range(self.chunk):
+                    fn(i)
+            self.r = None
+            if rem:
+                self.r = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(self.r):
+                    for i in range(rem):
+                        fn(self.reps * self.chunk + i)
+            torch.cuda.synchronize()
+            self.ok = True
+        except Exception as e:  # noqa: BLE001 -- any capture failure falls back to eager calls
+            self.error = repr(e)[:200]
+            torch.cuda.synchronize()
+
+    def run(self):
+        if not self.ok:
+            for i in range(self.n):
+                self.fn(i)
+            return
+        for _ in range(self.reps):
+            self.g.replay()
+        if self.r is not None:
+            self.r.replay()
+
+
+def _events_time(fn, iters, warmup, graph=True):
+    """Average ms per call of fn(i) with CUDA events on the current stream,
+    over `iters` calls after a warm-up; the calls run as CUDA graph replays
+    when they can be captured."""
+    import torch
+
+    sg = StepGraph(fn, iters) if graph else None
+    run = sg.run if sg is not None and sg.ok else (lambda: [fn(i) for i in range(iters)])
+    _warm(lambda i: run() if sg is not None and sg.ok else fn(i), warmup if sg is None or not sg.ok else 1,
+          min_seconds=0.3)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for i in range(iters):
-        fn(i)
+    run()
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / iters
@@ -229,6 +297,24 @@ def _extra_workloads():
 
     M, K = 16384, 2880
     codes = M * K // 2
+
+    def activations_tensorwise(iters, warmup, opts):
+        # the whole call (zero the amax word, amax pass, quantize pass) and
+        # its two passes timed apart: the amax pass into a workspace, and the
+        # quantize pass from that workspace's amax
+        run = _activations(dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4, 3)
+        desc, nb, ms, launches = run(iters, warmup, opts)
+        xs = [W.activations().to(dev)]
+        for _ in range(_sets_for(xs[0].numel() * 2) - 1):
+            xs.append(xs[0].clone())
+        wss = [fq.tensorwise_workspace(dev) for _ in xs]
+        qs = [fq.quantize(xx, rowwise=True, columnwise=True, mode="tensorwise") for xx in xs]
+        n = len(xs)
+        ms_amax = _events_time(lambda i: fq.tensor_amax(xs[i % n], out=fq.workspace_amax(wss[i % n])), iters, warmup)
+        ms_q = _events_time(lambda i: fq.quantize(xs[i % n], rowwise=True, columnwise=True, mode="tensorwise",
+                                                  tensorwise_amax=wss[i % n], out=qs[i % n]), iters, warmup)
+        return desc, nb, ms, launches, {"amax_pass_us": round(ms_amax * 1e3, 3),
+                                        "quantize_from_amax_us": round(ms_q * 1e3, 3)}
 
     def dequantize_activations(iters, warmup, opts):
         x = W.activations().to(dev)
@@ -299,8 +385,7 @@ def _extra_workloads():
         "small_nvfp4_quantize": (small_nvfp4_quantize, 200, 10),
         "activations_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64),
                                                  2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1), 50, 5),
-        "activations_tensorwise": (_activations(dict(mode="tensorwise"), 2 * codes + 2 * (M * K // 16) + 4, 3),
-                                   50, 5),
+        "activations_tensorwise": (activations_tensorwise, 50, 5),
         "activations_none": (_activations(dict(mode="none"), 2 * codes + 2 * (M * K // 16), 1), 50, 5),
         "activations_hadamard_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64,
                                                                col_hadamard=True, hadamard_signs=0xA5C3),
@@ -328,10 +413,13 @@ def extra_kernels(peak, only=None, iters=None, warmup=None, opts=None):
     for name, (fn, it, wu) in _extra_workloads().items():
         if only and name != only:
             continue
-        desc, nbytes, ms, launches = fn(iters or it, wu if warmup is None else warmup, opts or {})
+        res = fn(iters or it, wu if warmup is None else warmup, opts or {})
+        desc, nbytes, ms, launches = res[:4]
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"workload": desc, "bytes": nbytes, "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
                      "frac_of_hbm": round(gbs / peak, 4), "launches": launches}
+        if len(res) > 4:
+            out[name]["parts"] = res[4]
         torch.cuda.empty_cache()
     return out
 
@@ -354,18 +442,19 @@ def run_ours(args, dist):
     def step(i):
         fq.mxfp4_fake_quantize(xs[i & 1], out=ys[i & 1])
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
+    # the K timed steps as CUDA graph replays of the same calls (no Python
+    # launch path between kernels); eager calls if capture is not possible
+    sg = StepGraph(step, args.steps)
     sampler = ClockSampler(dev.index) if dist.rank == 0 else None
-    time.sleep(0.3 if sampler else 0)
+    t0 = time.time()
+    # warm-up: at least W steps and at least 0.5 s of them, right before the
+    # timed region, so that the clocks are at steady state when it starts
+    _warm(step, args.warmup, min_seconds=0.5)
     dist.barrier()
     torch.cuda.synchronize()
-    t0 = time.time()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record()
-    for i in range(args.steps):
-        step(i)
+    sg.run()
     ev1.record()
     torch.cuda.synchronize()
     dist.barrier()
@@ -386,8 +475,9 @@ def run_ours(args, dist):
     def e2e_step(i):
         fq.mxfp4_fake_quantize_host(xh, out=yh, workspace=ws, device=dev, synchronize=False)
 
-    e2e_ms = dist.max(_events_time(e2e_step, args.e2e_steps, 2))
+    e2e_ms = dist.max(_events_time(e2e_step, args.e2e_steps, 2, graph=False))
     torch.cuda.synchronize()
+    link = link_calibration(xh, yh, dev)
     del xs, ys, ws
 
     extras = None
@@ -415,12 +505,16 @@ def run_ours(args, dist):
         "data": "synthetic",
         "config": {"workload": "mxfp4_weight: MXFP4 fake-quantize bf16[8192,8192] ~N(0,0.02), 0.1% edge blocks, "
                                "bf16 out", "shape": [8192, 8192], "bytes_per_step": MXFP4_BYTES,
-                   "l2": "2 rotating input/output sets (537 MB > L2)", "parallelism": "replicas" if dist.world > 1 else "none"},
+                   "l2": "2 rotating input/output sets (537 MB > L2)", "parallelism": "replicas" if dist.world > 1 else "none",
+                   "timing": "CUDA events around K steps run as CUDA graph replays" if sg.ok else
+                             "CUDA events around K eager steps",
+                   "warmup_policy": "at least W steps and 0.5 s of steps, no idle gap before the timed region"},
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": peak_src,
                      "traffic": ncu_traffic("mxfp4_wide_kernel"), "kernel": "mxfp4_wide_kernel"},
         "e2e": {"value": round(MXFP4_BYTES / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "h2d_bytes_per_step": MXFP4_BYTES // 2, "d2h_bytes_per_step": MXFP4_BYTES // 2},
+                "h2d_bytes_per_step": MXFP4_BYTES // 2, "d2h_bytes_per_step": MXFP4_BYTES // 2,
+                "link": link, "frac_of_link": round(MXFP4_BYTES / (e2e_ms * 1e-3) / 1e9 / link["both_gbs"], 4)},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -428,6 +522,41 @@ def run_ours(args, dist):
     if extras is not None:
         line["kernels"] = extras
     return line
+
+
+def link_calibration(xh, yh, dev, reps=5):
+    """Host <-> device copy rates of the headline's pinned buffers on this
+    box: host-to-device alone, device-to-host alone, and both at once on two
+    streams (the overlap the end-to-end path relies on).  GB/s of bytes
+    moved; the best of `reps`."""
+    import torch
+
+    nb = xh.numel() * xh.element_size()
+    xd = torch.empty_like(xh, device=dev)
+    yd = torch.empty_like(yh, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(fn, nbytes):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - a)
+        return round(nbytes / min(ts) / 1e9, 1)
+
+    def both():
+        with torch.cuda.stream(s1):
+            xd.copy_(xh, non_blocking=True)
+        with torch.cuda.stream(s2):
+            yh.copy_(yd, non_blocking=True)
+
+    out = {"h2d_gbs": best(lambda: xd.copy_(xh, non_blocking=True), nb),
+           "d2h_gbs": best(lambda: yh.copy_(yd, non_blocking=True), nb),
+           "both_gbs": best(both, 2 * nb), "bytes_each_way": nb, "pinned": True}
+    del xd, yd
+    return out
 
 
 # ---------------------------------------------------------------------------
