@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["fp4q_api.cu", "k_tile.cu", "k_ct.cu", "k_ctb.cu", "k_ctb_grouped.cu", "k_ctb_rht.cu", "k_row.cu", "k_aux.cu", "k_mxfp4.cu", "k_mxfp8.cu", "fp4q_host.cu", "fp4q_noalloc.cu"]
+SOURCES = ["fp4q_api.cu", "k_tile.cu", "k_ct.cu", "k_ctb.cu", "k_ctb_grouped.cu", "k_ctb_rht.cu", "k_ctl.cu", "k_row.cu", "k_aux.cu", "k_mxfp4.cu", "k_mxfp8.cu", "fp4q_host.cu", "fp4q_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

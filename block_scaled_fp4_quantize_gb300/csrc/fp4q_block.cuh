@@ -214,32 +214,36 @@ __device__ __forceinline__ bool fast_block(float am, float S, float R, float& a)
 // Outer scale S = RN(A / (scale_max * 6)) and R = RN(1 / S), called by a
 // whole warp: when every lane's A is at least 2^-90, S lies in
 // [2^-110, 2^117] and both come from the FMA sequences; otherwise the warp
-// takes the general path.
+// takes the general path.  Returns true on the first branch (warp-uniform):
+// then S and R are normal and RN(am / S) < 2^126 for every am <= A.
 template <bool UE5M3>
-__device__ __forceinline__ void outer_sr(float A, float& S, float& R) {
+__device__ __forceinline__ bool outer_sr(float A, float& S, float& R) {
   if (__all_sync(0xFFFFFFFFu, fbits(A) >= kTiny)) {
     S = div_bmr(A, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
     R = rcp_markstein(S);
-  } else {
-    S = outer_scale<UE5M3>(A);
-    R = ieee_rcp(S);
+    return true;
   }
+  S = outer_scale<UE5M3>(A);
+  R = ieee_rcp(S);
+  return false;
 }
 
 // outer_sr for two outer blocks at once (one branch for both).
 template <bool UE5M3>
-__device__ __forceinline__ void outer_sr2(float A0, float A1, float (&S)[2], float (&R)[2]) {
+__device__ __forceinline__ bool outer_sr2(float A0, float A1, float (&S)[2], float (&R)[2]) {
   if (__all_sync(0xFFFFFFFFu, fbits(A0) >= kTiny && fbits(A1) >= kTiny)) {
     S[0] = div_bmr(A0, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
     S[1] = div_bmr(A1, bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
     R[0] = rcp_markstein(S[0]);
     R[1] = rcp_markstein(S[1]);
+    return true;
   } else {
     S[0] = outer_scale<UE5M3>(A0);
     S[1] = outer_scale<UE5M3>(A1);
     R[0] = ieee_rcp(S[0]);
     R[1] = ieee_rcp(S[1]);
   }
+  return false;
 }
 
 // max |u| over 16 values (NaN propagates), as a tree of magnitude maxima.
@@ -260,6 +264,27 @@ __device__ __forceinline__ float amax16(const float (&u)[16]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) m[i] = max_nan(m[2 * i], m[2 * i + 1]);
   return max_nan(max_nan(m[0], m[1]), max_nan(m[2], m[3]));
+}
+
+// Sanitized copy of a bf16 pair (NaN -> +0, +-inf -> +-largest finite).
+__device__ __forceinline__ uint32_t sanitize_bf16x2(uint32_t w) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t v = (w >> (16 * h)) & 0xFFFFu;
+    const uint32_t a = v & 0x7FFFu;
+    if (a > 0x7F80u) v = 0u;
+    else if (a == 0x7F80u) v = (v & 0x8000u) | 0x7F7Fu;
+    r |= v << (16 * h);
+  }
+  return r;
+}
+
+// max |.| of the two halves of a packed bf16 maximum, as binary32.
+__device__ __forceinline__ float bf16x2_hmax(uint32_t m) {
+  m &= 0x7FFF7FFFu;
+  const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+  return bitsf((hi > lo ? hi : lo) << 16);
 }
 
 // Inner-scale table in shared memory: entry c holds (DEC(c), zh, zl) with

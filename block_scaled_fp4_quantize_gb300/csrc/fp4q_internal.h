@@ -142,6 +142,7 @@ bool ct_supports(const QuantJob& j);
 bool row_supports(const QuantJob& j);
 bool ctb_supports(const QuantJob& j);
 bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err);
+bool launch_ctl(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 bool launch_ctb_grouped(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 bool launch_ctb_rht(const QuantJob& j, cudaStream_t st, cudaError_t* err);
 cudaError_t launch_row(const QuantJob& j, cudaStream_t st);
@@ -164,6 +165,7 @@ cudaError_t ctb_grouped_timeout_flag(uint32_t* v, bool clear);
 cudaError_t ctb_rht_timeout_flag(uint32_t* v, bool clear);
 cudaError_t row_timeout_flag(uint32_t* v, bool clear);
 cudaError_t ct_timeout_flag(uint32_t* v, bool clear);
+cudaError_t ctl_timeout_flag(uint32_t* v, bool clear);
 cudaError_t set_ctb_timeout_flag();
 
 }  // namespace fp4q

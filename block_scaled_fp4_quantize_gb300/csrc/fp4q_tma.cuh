@@ -153,5 +153,37 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Tensor map of the bf16 input [G][M][K] (row stride ld) for tiles of
+// `box_m` rows x 64 columns with the 128-byte swizzle.
+bool make_bf16_tile_map(const QuantJob& j, CUtensorMap* map, int box_m) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)j.K, (cuuint64_t)j.M, (cuuint64_t)j.G};
+  const cuuint64_t strides[2] = {(cuuint64_t)j.ld * 2, (cuuint64_t)j.M * (cuuint64_t)j.ld * 2};
+  const cuuint32_t box[3] = {64u, (cuuint32_t)box_m, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(j.x), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of the columnwise codes [G][K][M / 2] bytes for the tile
+// store (box: 64 columns x 64 bytes, 64-byte swizzle: the inner extent of
+// the box equals the swizzle span).  Needs 16-byte aligned rows (M a
+// multiple of 32) and a 16-byte aligned base; false when the codes leave by
+// the thread copy-out instead.
+bool make_col_map(const QuantJob& j, CUtensorMap* map) {
+  if (j.ngroups > 0 || !j.do_col || j.M % 32 || (reinterpret_cast<uintptr_t>(j.col_codes) & 15u)) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(j.M / 2), (cuuint64_t)j.K, (cuuint64_t)j.G};
+  const cuuint64_t strides[2] = {(cuuint64_t)(j.M / 2), (cuuint64_t)j.K * (cuuint64_t)(j.M / 2)};
+  const cuuint32_t box[3] = {64u, 64u, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, j.col_codes, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 }  // namespace fp4q

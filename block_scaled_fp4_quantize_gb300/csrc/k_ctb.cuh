@@ -61,27 +61,6 @@ __device__ __forceinline__ void issue_bf16_tile(const CUtensorMap* map, const Ti
   tma_load3(raw, map, (int)p.k0, (int)p.m0, (int)p.g, bar);
 }
 
-// Sanitized copy of a bf16 pair (NaN -> +0, +-inf -> +-largest finite).
-__device__ __forceinline__ uint32_t sanitize_bf16x2(uint32_t w) {
-  uint32_t r = 0;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t v = (w >> (16 * h)) & 0xFFFFu;
-    const uint32_t a = v & 0x7FFFu;
-    if (a > 0x7F80u) v = 0u;
-    else if (a == 0x7F80u) v = (v & 0x8000u) | 0x7F7Fu;
-    r |= v << (16 * h);
-  }
-  return r;
-}
-
-// max |.| of the two halves of a packed bf16 maximum, as binary32.
-__device__ __forceinline__ float bf16x2_hmax(uint32_t m) {
-  m &= 0x7FFF7FFFu;
-  const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
-  return bitsf((hi > lo ? hi : lo) << 16);
-}
-
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -650,35 +629,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   if (!GR && col_tma && t == 0) bulk_wait_all();
 }
 
-bool make_bf16_map(const QuantJob& j, CUtensorMap* map) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)j.K, (cuuint64_t)j.M, (cuuint64_t)j.G};
-  const cuuint64_t strides[2] = {(cuuint64_t)j.ld * 2, (cuuint64_t)j.M * (cuuint64_t)j.ld * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BM, 1u};
-  const cuuint32_t es[3] = {1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(j.x), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Tensor map of the columnwise codes [G][K][M / 2] bytes for the tile
-// store (box: 64 columns x 64 bytes, 64-byte swizzle: the inner extent of
-// the box equals the swizzle span).  Needs 16-byte aligned rows (M a
-// multiple of 32) and a 16-byte aligned base; false when the codes leave by
-// the thread copy-out instead.
-bool make_col_map(const QuantJob& j, CUtensorMap* map) {
-  if (j.ngroups > 0 || !j.do_col || j.M % 32 || (reinterpret_cast<uintptr_t>(j.col_codes) & 15u)) return false;
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)(j.M / 2), (cuuint64_t)j.K, (cuuint64_t)j.G};
-  const cuuint64_t strides[2] = {(cuuint64_t)(j.M / 2), (cuuint64_t)j.K * (cuuint64_t)(j.M / 2)};
-  const cuuint32_t box[3] = {64u, 64u, 1u};
-  const cuuint32_t es[3] = {1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, j.col_codes, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+bool make_bf16_map(const QuantJob& j, CUtensorMap* map) { return make_bf16_tile_map(j, map, BM); }
 
 template <bool SR, bool UE5M3, int BO, bool GR, bool RHT, int OBC = 0, int FT = 0>
 cudaError_t launch_ctb_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, int col_tma,

@@ -79,3 +79,59 @@ def test_bmr_and_markstein_match_ieee_division(tmp_path):
     r = subprocess.run([exe, "61"] + args, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "bmr 0 of" in r.stdout and "markstein 0 of" in r.stdout
+
+
+def _rn24(x):
+    """x > 0 rounded to 24 significant bits, ties to even (exact rationals)."""
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    q = x / Fraction(2) ** (e - 23)
+    n, r = divmod(q.numerator, q.denominator)
+    r = Fraction(r, q.denominator)
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2):
+        n += 1
+    return n * Fraction(2) ** (e - 23)
+
+
+def _rd24(x):
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    ulp = Fraction(2) ** (e - 23)
+    return (x // ulp) * ulp
+
+
+def test_bmr_is_exact_for_outer_scales_of_bf16_amax():
+    """The whole-tile cast-transpose kernel divides bf16 values u by an
+    outer scale S = RN(A / (scale_max * 6)) whose amax A is itself a bf16
+    value, so S's significand is that of RN(m / 21), m = 128 .. 255 (6 =
+    3 * 2, 448 = 7 * 2^6, 114688 = 7 * 2^14).  For each of those 128
+    divisors sigma, with zh = RD(1 / sigma) and zl = RN(1 / sigma - zh), the
+    known-divisor method RN(u zh + RN(u zl)) must equal RN(u / sigma) for
+    every dividend significand 1 .. 255 (exact rationals); and zl is at
+    least 2^-30, so zl scaled by 2^-e stays normal for S < 2^90.  The
+    device builds zh by a round-down division and zl as RN((1 - zh sigma) /
+    sigma), with 1 - zh sigma exact: checked here too."""
+    sigmas, zls = set(), []
+    for m in range(128, 256):
+        s = _rn24(Fraction(m, 21))
+        while s >= 2:
+            s /= 2
+        sigmas.add(s)
+        zh = _rd24(1 / s)
+        d = 1 / s - zh
+        zl = _rn24(d) if d else Fraction(0)
+        if d:
+            zls.append(zl)
+            e = 1 - zh * s                                       # one fused multiply-add
+            assert e == _rn24(e) and e / s == d
+        for y in range(1, 256):
+            got = _rn24(y * zh + (_rn24(y * zl) if zl else Fraction(0)))
+            assert got == _rn24(Fraction(y) / s), (m, y)
+    assert len(sigmas) == 128
+    assert min(zls) >= Fraction(1, 2 ** 30)

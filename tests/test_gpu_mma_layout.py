@@ -21,11 +21,13 @@ def _cuda():
     fq.build()
 
 
-@pytest.fixture(params=["fast", "tile", "general"])
+@pytest.fixture(params=["fast", "ctb", "tile", "general"])
 def kernel(request, monkeypatch):
-    for v in ("FP4Q_GENERAL_KERNEL", "FP4Q_NO_ROW_KERNEL", "FP4Q_NO_CTB_KERNEL"):
+    for v in ("FP4Q_GENERAL_KERNEL", "FP4Q_NO_ROW_KERNEL", "FP4Q_NO_CTB_KERNEL", "FP4Q_NO_CTL_KERNEL"):
         monkeypatch.delenv(v, raising=False)
-    if request.param == "general":
+    if request.param == "ctb":
+        monkeypatch.setenv("FP4Q_NO_CTL_KERNEL", "1")
+    elif request.param == "general":
         monkeypatch.setenv("FP4Q_GENERAL_KERNEL", "1")
     elif request.param == "tile":
         monkeypatch.setenv("FP4Q_NO_ROW_KERNEL", "1")

@@ -48,16 +48,19 @@ def _id(c):
                                  "in2d" if c["inner_2d"] else "in1d", c["scale_format"])
 
 
-@pytest.fixture(params=["fast", "tile", "general"])
+@pytest.fixture(params=["fast", "ctb", "tile", "general"])
 def kernel(request, monkeypatch):
     """Run a test on each quantizer kernel that can take it: the default
     choice (flat rowwise kernel for rowwise-only packed inputs, the bf16
-    cast-transpose kernel for columnwise bf16, else the cast-transpose tile
-    kernel), the cast-transpose tile kernel alone, and the general tile
-    kernel."""
-    for v in ("FP4Q_GENERAL_KERNEL", "FP4Q_NO_ROW_KERNEL", "FP4Q_NO_CTB_KERNEL"):
+    cast-transpose kernel for columnwise bf16 -- in its whole-tile form when
+    the call allows it --, else the cast-transpose tile kernel), the bf16
+    cast-transpose kernel without its whole-tile form, the cast-transpose
+    tile kernel alone, and the general tile kernel."""
+    for v in ("FP4Q_GENERAL_KERNEL", "FP4Q_NO_ROW_KERNEL", "FP4Q_NO_CTB_KERNEL", "FP4Q_NO_CTL_KERNEL"):
         monkeypatch.delenv(v, raising=False)
-    if request.param == "general":
+    if request.param == "ctb":
+        monkeypatch.setenv("FP4Q_NO_CTL_KERNEL", "1")
+    elif request.param == "general":
         monkeypatch.setenv("FP4Q_GENERAL_KERNEL", "1")
     elif request.param == "tile":
         monkeypatch.setenv("FP4Q_NO_ROW_KERNEL", "1")
