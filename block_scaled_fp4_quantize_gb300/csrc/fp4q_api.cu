@@ -127,6 +127,7 @@ QuantJob base_job(const fp4q_params_t* p, const void* x, float* residual) {
   j.ue5m3 = p->scale_format == FP4Q_SCALE_UE5M3;
   j.sr = p->rounding == FP4Q_STOCHASTIC;
   j.seed = p->seed;
+  j.srk = philox_keys(p->seed);
   j.step = p->step;
   j.out_bf16 = p->out_dtype == FP4Q_BF16;
   const int mma = p->scale_layout == FP4Q_SCALE_LAYOUT_MMA;

@@ -136,7 +136,7 @@ __device__ __forceinline__ void normalize16_neg(const float (&nu)[16], float (&x
 // 16 values -> 16 codes (two 32-bit words, element 2i in the low nibble of
 // byte i); optional dequantized values (e2m1 * s) * S.
 template <bool SR, bool DEQ>
-__device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, const Norm& n, uint64_t seed,
+__device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, const Norm& n, const PhiloxKeys& K,
                                          uint32_t step, uint32_t orient, uint64_t n0, uint32_t& w0, uint32_t& w1,
                                          float (&deq)[16]) {
   float t[16];
@@ -151,13 +151,27 @@ __device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, 
     w1 = e2m1x8_rne(t + 8);
     return;
   }
-  if (SR) {
+  if (SR) {  // the chosen grid values, encoded by the hardware conversion (exact)
+    float g[16];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const uint4 rw = sr_words(seed, step, orient, (n0 >> 2) + (uint64_t)w);
-      byte[2 * w] = e2m1_sr(t[4 * w], rw.x) | (e2m1_sr(t[4 * w + 1], rw.y) << 4);
-      byte[2 * w + 1] = e2m1_sr(t[4 * w + 2], rw.z) | (e2m1_sr(t[4 * w + 3], rw.w) << 4);
+      const uint4 rw = sr_words(K, step, orient, (n0 >> 2) + (uint64_t)w);
+      g[4 * w] = e2m1_sr_value(t[4 * w], rw.x);
+      g[4 * w + 1] = e2m1_sr_value(t[4 * w + 1], rw.y);
+      g[4 * w + 2] = e2m1_sr_value(t[4 * w + 2], rw.z);
+      g[4 * w + 3] = e2m1_sr_value(t[4 * w + 3], rw.w);
     }
+    w0 = e2m1x8_rne(g);
+    w1 = e2m1x8_rne(g + 8);
+    if (DEQ) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float d = ieee_mul(g[i], T.x);
+        if (!n.none) d = ieee_mul(d, n.S);
+        deq[i] = d;
+      }
+    }
+    return;
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) byte[i] = e2m1x2_rne(t[2 * i], t[2 * i + 1]);
@@ -183,7 +197,7 @@ __device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, 
 // fallback.  OUTER: an outer scale applies; NEG: the values arrive negated.
 template <bool SR, bool UE5M3, bool OUTER, bool NEG>
 __device__ __forceinline__ uint32_t block_fast(const float4* tab, const float (&v)[16], float a, float S, float r,
-                                               uint64_t seed, uint32_t step, uint32_t orient, uint64_t n0,
+                                               const PhiloxKeys& K, uint32_t step, uint32_t orient, uint64_t n0,
                                                uint32_t& w0, uint32_t& w1) {
   const uint32_t sc = encode_scale<UE5M3>(div_bmr(a, bitsf(kSixHi), bitsf(kSixLo)));
   const float4 T = tab[sc];
@@ -196,7 +210,7 @@ __device__ __forceinline__ uint32_t block_fast(const float4* tab, const float (&
   float x[16], dq[16];
   if (NEG) normalize16_neg<SR>(v, x, n);
   else normalize16<SR>(v, x, n);
-  encode16<SR, false>(x, T, n, seed, step, orient, n0, w0, w1, dq);
+  encode16<SR, false>(x, T, n, K, step, orient, n0, w0, w1, dq);
   return sc;
 }
 

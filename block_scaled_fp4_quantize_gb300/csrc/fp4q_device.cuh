@@ -140,42 +140,77 @@ __device__ __forceinline__ void e2m1x2_decode(uint32_t byte, float& lo, float& h
 
 // Stochastic rounding of t onto the E2M1 grid with the 32-bit random word w:
 // between neighbours lo < |t| < hi the result is hi iff (w >> 8) < f * 2^24,
-// f = (|t| - lo) / (hi - lo).  Branch-free: the grid spacing is 1/2 on
-// [0, 2), 1 on [2, 4) and 2 on [4, 6), so y = |t| / spacing (exact) has
-// lo / spacing = floor(y) and f = y - floor(y) (exact); floor(y) comes from
-// one add rounded toward -inf onto 1.5 * 2^23, whose low bits then hold it.
-__device__ __forceinline__ uint32_t e2m1_sr(float t, uint32_t w) {
-  const uint32_t sign = (fbits(t) >> 28) & 8u;
-  const float a = bitsf(abs_bits(t));
-  const bool lt2 = a < 2.0f, lt4 = a < 4.0f;
-  const float y = ieee_mul(a, lt2 ? 2.0f : (lt4 ? 1.0f : 0.5f));
-  float tmp;
-  asm("add.rm.f32 %0, %1, 0f4B400000;" : "=f"(tmp) : "f"(y));
-  const float fl = ieee_sub(tmp, 12582912.0f);
-  const float f24 = ieee_mul(ieee_sub(y, fl), 16777216.0f);
-  const uint32_t up = ((float)(w >> 8) < f24) ? 1u : 0u;
-  const uint32_t k = (fbits(tmp) & 3u) + (lt2 ? 0u : (lt4 ? 2u : 4u)) + up;
-  return sign | (a < 6.0f ? k : 7u);
+// f = (|t| - lo) / (hi - lo); the value is returned, sign kept (a grid value,
+// so the hardware E2M1 conversion encodes it exactly).
+// On the bit pattern b of |t| >= 1/2 the grid keeps one mantissa bit above 1
+// and none in [1/2, 1) (its points there are 1/2 and 1), so the d = 22 (or
+// 23) bits below the kept ones hold f * 2^d exactly.  Adding (2^d - 1) - (w >>
+// (32 - d)) to b carries into the kept bits iff (w >> (32 - d)) < f * 2^d,
+// which for integers is the condition above, and clearing the d bits leaves
+// the chosen neighbour (a carry out of the mantissa lands on the next binade's
+// first point).  Above 6 the result saturates at 6.  Below 1/2 the neighbours
+// are 0 and 1/2, f * 2^24 = |t| * 2^25, compared in binary32 (both sides exact).
+__device__ __forceinline__ float e2m1_sr_value(float t, uint32_t w) {
+  const uint32_t b = abs_bits(t);
+  const bool ge1 = b >= 0x3F800000u;
+  const uint32_t mask = ge1 ? 0x3FFFFFu : 0x7FFFFFu;
+  const uint32_t rnd = ge1 ? (w >> 10) : (w >> 9);
+  uint32_t r = (b + (rnd ^ mask)) & ~mask;
+  r = r < 0x40C00000u ? r : 0x40C00000u;
+  float t25, u24;
+  asm("mul.rn.f32 %0, %1, 0f4C000000;" : "=f"(t25) : "f"(bitsf(b)));
+  asm("cvt.rn.f32.u32 %0, %1;" : "=f"(u24) : "r"(w >> 8));
+  uint32_t half;
+  asm("{\n\t.reg .pred p;\n\tsetp.lt.f32 p, %1, %2;\n\tselp.u32 %0, 0x3F000000, 0, p;\n\t}"
+      : "=r"(half) : "f"(u24), "f"(t25));
+  r = b < 0x3F000000u ? half : r;
+  return bitsf(r | (fbits(t) & 0x80000000u));
 }
+
+// The E2M1 code of e2m1_sr_value.
+__device__ __forceinline__ uint32_t e2m1_sr(float t, uint32_t w) { return e2m1x2_rne(e2m1_sr_value(t, w), 0.0f) & 0xFu; }
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+
+// The ten round keys of a 64-bit key: round r uses (k0 + r W0, k1 + r W1),
+// W0 = 0x9E3779B9, W1 = 0xBB67AE85.  The kernels take them precomputed from
+// their parameter block, so the rounds read them as constant operands.
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__host__ __device__ inline PhiloxKeys philox_keys(uint64_t key) {
+  PhiloxKeys K;
+  uint32_t k0 = (uint32_t)key, k1 = (uint32_t)(key >> 32);
+  for (int r = 0; r < 10; ++r) {
+    K.k0[r] = k0;
+    K.k1[r] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return K;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& K) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
     const uint64_t p0 = (uint64_t)0xD2511F53u * c.x, p1 = (uint64_t)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ K.k0[r], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ K.k1[r],
+                   (uint32_t)p0);
   }
   return c;
 }
 
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+  return philox4x32_10(c, philox_keys(((uint64_t)k1 << 32) | k0));
+}
+
 // Random words of elements 4*blk .. 4*blk+3 of an orientation's flat index
-// space: counter (blk lo, blk hi, step, orient), key = seed.
-__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint32_t step, uint32_t orient, uint64_t blk) {
-  return philox4x32_10(make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), step, orient), (uint32_t)seed,
-                       (uint32_t)(seed >> 32));
+// space: counter (blk lo, blk hi, step, orient), key = seed (as round keys).
+__device__ __forceinline__ uint4 sr_words(const PhiloxKeys& K, uint32_t step, uint32_t orient, uint64_t blk) {
+  return philox4x32_10(make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), step, orient), K);
 }
 
 // ---------------------------------------------------------------------------

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "fp4q_device.cuh"
+
 namespace fp4q {
 
 // Where a kernel takes the outer scale S from.
@@ -76,6 +78,7 @@ struct QuantJob {
   float* residual;  // [G, M, K] contiguous, rowwise only
   int mode, ob, outer_2d, inner_2d, ue5m3, sr;
   uint64_t seed;
+  PhiloxKeys srk;   // the round keys of `seed` (stochastic rounding)
   uint32_t step;
   int do_row, do_col;
   int s_src;

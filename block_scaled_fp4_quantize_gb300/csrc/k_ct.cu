@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
         if (staged) stage_block<IN_BF16>(xs, row, b, x);
         if (j.do_row) {
           float deq[16];
-          if (deq_row) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, n0), cw[2 * q], cw[2 * q + 1], deq);
-          else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, n0), cw[2 * q], cw[2 * q + 1], deq);
+          if (deq_row) encode16<SR, true>(x, T, n, j.srk, j.step, 0u, sr_row_n(j, n0), cw[2 * q], cw[2 * q + 1], deq);
+          else encode16<SR, false>(x, T, n, j.srk, j.step, 0u, sr_row_n(j, n0), cw[2 * q], cw[2 * q + 1], deq);
           scw |= sc << (8 * q);
           if (valid) {
             if (j.residual) {
@@ -603,8 +603,8 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
       // SR index of the column block: row g K + k0 + col of x transposed
       const uint64_t n0 = sr_col_n(j, p.g * j.K + p.k0 + col, p.m0 + rbeg + 16 * q);
       float deq[16];
-      if (j.qdq_orient == 2) encode16<SR, true>(x, T, n, j.seed, j.step, 1u, n0, ccw[2 * q], ccw[2 * q + 1], deq);
-      else encode16<SR, false>(x, T, n, j.seed, j.step, 1u, n0, ccw[2 * q], ccw[2 * q + 1], deq);
+      if (j.qdq_orient == 2) encode16<SR, true>(x, T, n, j.srk, j.step, 1u, n0, ccw[2 * q], ccw[2 * q + 1], deq);
+      else encode16<SR, false>(x, T, n, j.srk, j.step, 1u, n0, ccw[2 * q], ccw[2 * q + 1], deq);
       cscw |= sc << (8 * q);
       if (j.qdq_orient == 2 && kvalid && mb < j.M) {
 #pragma unroll

@@ -118,7 +118,7 @@ __device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (
   float x[16], dq[16];
   if (NEG) normalize16_neg<SR>(v, x, n);
   else normalize16<SR>(v, x, n);
-  encode16<SR, false>(x, T, n, j.seed, j.step, orient, n0, w0, w1, dq);
+  encode16<SR, false>(x, T, n, j.srk, j.step, orient, n0, w0, w1, dq);
   return sc;
 }
 
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         for (int b = 0; b < 2; ++b) {
           float u[16];
           row_u(b, u);
-          scw |= block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE>(tab, u, ab[b], S[b], R[b], j.seed, j.step, 0u,
+          scw |= block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE>(tab, u, ab[b], S[b], R[b], j.srk, j.step, 0u,
                                                                       sr_row_n(j, rel + 16 * b), cw[2 * b],
                                                                       cw[2 * b + 1])
                  << (8 * b);
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
         col_u(c, u);
         uint32_t w0, w1;
         const uint32_t sc = block_fast<SR, UE5M3, BO != BO_NONE, BO != BO_NONE && !RHT>(
-            tab, u, ac[c], S[c], R[c], j.seed, j.step, 1u, col_sr(c), w0, w1);
+            tab, u, ac[c], S[c], R[c], j.srk, j.step, 1u, col_sr(c), w0, w1);
         col_stage(c, w0, w1, sc);
       }
     } else {

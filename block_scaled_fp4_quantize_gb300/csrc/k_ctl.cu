@@ -202,7 +202,7 @@ __device__ __forceinline__ void col_codes16(const uint32_t (&w)[16], uint64_t P,
 // 16 values u (as -u when NEG), block maximum am, outer scale S, R = 1 / S.
 template <bool UE5M3, bool NEG>
 __device__ __forceinline__ uint32_t slow_block(const float4* tab, const float (&v)[16], float am, float S, float R,
-                                            bool none, uint32_t& w0, uint32_t& w1) {
+                                               bool none, const PhiloxKeys& K, uint32_t& w0, uint32_t& w1) {
   Norm n;
   n.none = none;
   n.S = S;
@@ -217,7 +217,7 @@ __device__ __forceinline__ uint32_t slow_block(const float4* tab, const float (&
   float x[16], dq[16];
   if (NEG) normalize16_neg<false>(v, x, n);
   else normalize16<false>(v, x, n);
-  encode16<false, false>(x, T, n, 0ull, 0u, 0u, 0ull, w0, w1, dq);
+  encode16<false, false>(x, T, n, K, 0u, 0u, 0ull, w0, w1, dq);
   return sc;
 }
 
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
             u[2 * i] = bf16lo(wd[i]);
             u[2 * i + 1] = bf16hi(wd[i]);
           }
-          const uint32_t s1 = slow_block<UE5M3, false>(tab, u, b ? am1 : am0, S, R, !OUTER, c[2 * b], c[2 * b + 1]);
+          const uint32_t s1 = slow_block<UE5M3, false>(tab, u, b ? am1 : am0, S, R, !OUTER, j.srk, c[2 * b], c[2 * b + 1]);
           sc = b ? (sc | (s1 << 8)) : s1;
         }
       }
@@ -378,14 +378,16 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
     } else {  // 1 x 64: the row's 64 columns are this thread's two blocks and its partner's
       uint32_t g = umax(ram & 0xFFFFu, ram >> 16);
       g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1)) << 16;
-      const float S = div_bmr(bitsf(g), denh, denl);
-      if (rh == 0) j.row_outer[row * (j.K >> 6) + (tk0 >> 6)] = S;
+      const float S = div_bmr(bitsf(g), denh, denl);  // exact for g >= 2^-90
+      float* so = j.row_outer + row * (j.K >> 6) + (tk0 >> 6);
       if (__all_sync(0xFFFFFFFFu, g >= kTiny && fbits(S) < 0x6C800000u)) {
+        if (rh == 0) *so = S;
         float zh, zl;
         zsplit(g, S, ztab, zh, zl);
         row_pass(a, ram, NM_BMR, S, 1.0f, pk2(zh, zh), pk2(zl, zl));
       } else {
         const float S1 = outer_scale<UE5M3>(bitsf(g));
+        if (rh == 0) *so = S1;
         row_pass(a, ram, PM_SLOW, S1, ieee_rcp(S1), 0ull, 0ull);
       }
     }
@@ -466,14 +468,8 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
         const uint32_t g0 = g << 16, g1 = g & 0xFFFF0000u;
         float Sv0, Sv1;
         upk2(bmr2(pk2(bitsf(g0), bitsf(g1)), pk2(denh, denh), pk2(denl, denl)), Sv0, Sv1);
-        S[0] = Sv0;
+        S[0] = Sv0;  // exact for g >= 2^-90
         S[1] = Sv1;
-        if ((warp & 3) == 0) {
-          const int64_t M64 = j.M >> 6;
-          float* d = j.col_outer + ((int64_t)tg * j.K + tk0 + 2 * lane) * M64 + (tm0 >> 6) + (warp >> 2);
-          d[0] = S[0];
-          d[M64] = S[1];
-        }
         if (__all_sync(0xFFFFFFFFu, umin(g0, g1) >= kTiny && umax(fbits(S[0]), fbits(S[1])) < 0x6C800000u)) {
           float zh0, zl0, zh1, zl1;
           zsplit(g0, S[0], ztab, zh0, zl0);
@@ -487,6 +483,12 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
           S[1] = outer_scale<UE5M3>(bitsf(g1));
           R[0] = ieee_rcp(S[0]);
           R[1] = ieee_rcp(S[1]);
+        }
+        if ((warp & 3) == 0) {
+          const int64_t M64 = j.M >> 6;
+          float* d = j.col_outer + ((int64_t)tg * j.K + tk0 + 2 * lane) * M64 + (tm0 >> 6) + (warp >> 2);
+          d[0] = S[0];
+          d[M64] = S[1];
         }
       }
       uint32_t c[4], sc;
@@ -510,7 +512,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
           float u[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) u[i] = k ? bf16hi(wv[i]) : bf16lo(wv[i]);
-          const uint32_t s1 = slow_block<UE5M3, false>(tab, u, k ? am1 : am0, S[k], R[k], !OUTER, c[2 * k], c[2 * k + 1]);
+          const uint32_t s1 = slow_block<UE5M3, false>(tab, u, k ? am1 : am0, S[k], R[k], !OUTER, j.srk, c[2 * k], c[2 * k + 1]);
           sc = k ? (sc | (s1 << 8)) : s1;
         }
       }

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(RT) row_kernel(const QuantJob j) {
       float a = am;
       const bool fast = !SR && !deq && __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
       if (fast) {
-        sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, 0ull, 0u, 0u, 0ull, w0, w1);
+        sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, j.srk, 0u, 0u, 0ull, w0, w1);
       } else {
         n.pos = n.none || positive(n.S);
         n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
@@ -202,8 +202,8 @@ __global__ void __launch_bounds__(RT) row_kernel(const QuantJob j) {
         sc = block_scale<UE5M3>(tv, am, n, T);
         float x[16];
         normalize16<SR>(u, x, n);
-        if (deq) encode16<SR, true>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, 16 * b[q]), w0, w1, dq);
-        else encode16<SR, false>(x, T, n, j.seed, j.step, 0u, sr_row_n(j, 16 * b[q]), w0, w1, dq);
+        if (deq) encode16<SR, true>(x, T, n, j.srk, j.step, 0u, sr_row_n(j, 16 * b[q]), w0, w1, dq);
+        else encode16<SR, false>(x, T, n, j.srk, j.step, 0u, sr_row_n(j, 16 * b[q]), w0, w1, dq);
       }
       if (!valid[q]) continue;
       if (j.row_codes) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
     float a = am;
     const bool fast = __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
     if (fast) {
-      sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, 0ull, 0u, 0u, 0ull, w0, w1);
+      sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, j.srk, 0u, 0u, 0ull, w0, w1);
     } else {
       n.pos = n.none || positive(n.S);
       n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
       sc = block_scale<UE5M3>(tv, am, n, T);
       float x[16], dq[16];
       normalize16<false>(u, x, n);
-      encode16<false, false>(x, T, n, 0ull, 0u, 0u, 0ull, w0, w1, dq);
+      encode16<false, false>(x, T, n, j.srk, 0u, 0u, 0ull, w0, w1, dq);
     }
     if (valid) {
       *reinterpret_cast<uint2*>(j.row_codes + 8 * b) = make_uint2(w0, w1);

@@ -49,7 +49,7 @@ struct SegOut {
 
 template <bool WANT_DEQ>
 __device__ __forceinline__ SegOut quantize_segment(const float (&u)[16], float S, bool no_outer, uint32_t a_bits,
-                                                   const ScaleFmt& f, bool sr, uint64_t seed, uint32_t step,
+                                                   const ScaleFmt& f, bool sr, const PhiloxKeys& K, uint32_t step,
                                                    uint32_t orient, uint64_t n0, float (&deq)[16]) {
   // inner scale from the block amax in normalized space (a_bits, already
   // reduced over a 16x16 block when required)
@@ -69,7 +69,7 @@ __device__ __forceinline__ SegOut quantize_segment(const float (&u)[16], float S
   if (sr) {
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const uint4 r = sr_words(seed, step, orient, (n0 >> 2) + (uint64_t)w);
+      const uint4 r = sr_words(K, step, orient, (n0 >> 2) + (uint64_t)w);
       q[4 * w + 0] = e2m1_sr(t[4 * w + 0], r.x);
       q[4 * w + 1] = e2m1_sr(t[4 * w + 1], r.y);
       q[4 * w + 2] = e2m1_sr(t[4 * w + 2], r.z);
@@ -319,8 +319,8 @@ __global__ void __launch_bounds__(NTHR) quant_tile_kernel(const QuantJob j) {
       float deq[16];
       const uint64_t n0 = (uint64_t)((g * j.M + m) * j.K + kb);
       SegOut o;
-      if (deq_row) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, sr_row_n(j, (int64_t)n0), deq);
-      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 0u, sr_row_n(j, (int64_t)n0), deq);
+      if (deq_row) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.srk, j.step, 0u, sr_row_n(j, (int64_t)n0), deq);
+      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.srk, j.step, 0u, sr_row_n(j, (int64_t)n0), deq);
       if (valid) {
         if (j.row_codes) *reinterpret_cast<uint2*>(j.row_codes + n0 / 2) = make_uint2(o.codes_lo, o.codes_hi);
         if (j.row_scales) j.row_scales[sf_offset(j.rsl, g, m, kb / 16)] = (uint8_t)o.sc;
@@ -378,8 +378,8 @@ __global__ void __launch_bounds__(NTHR) quant_tile_kernel(const QuantJob j) {
       const uint64_t n0 = (uint64_t)((g * j.K + k) * j.M + mb);
       SegOut o;
       const uint64_t nsr = sr_col_n(j, g * j.K + k, mb);
-      if (qdq_col) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, nsr, deq);
-      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.seed, j.step, 1u, nsr, deq);
+      if (qdq_col) o = quantize_segment<true>(u, S, no_outer, a_bits, f, SR, j.srk, j.step, 1u, nsr, deq);
+      else o = quantize_segment<false>(u, S, no_outer, a_bits, f, SR, j.srk, j.step, 1u, nsr, deq);
       if (valid) {
         if (j.col_codes) *reinterpret_cast<uint2*>(j.col_codes + n0 / 2) = make_uint2(o.codes_lo, o.codes_hi);
         if (j.col_scales) j.col_scales[sf_offset(j.csl, g, k, mb / 16)] = (uint8_t)o.sc;

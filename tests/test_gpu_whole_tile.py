@@ -41,6 +41,7 @@ def _special(shape, seed):
     for _ in range(4):                                   # tiny patches (below 2^-90, some subnormal)
         r, c = int(torch.randint(0, M // 16, (1,), generator=g)) * 16, int(torch.randint(0, K // 16, (1,), generator=g)) * 16
         flat[-1, r:r + 16, c:c + 16] = torch.randn(16, 16, generator=g) * 2.0 ** -120
+    flat[0, 64:128, 0:64] = torch.randn(64, 64, generator=g) * 2.0 ** -118   # a whole 64 x 64 block below 2^-90
     flat[0, 5, 7] = float("nan")
     flat[-1, M - 3, K - 9] = float("inf")
     flat[0, M // 2, 3] = -float("inf")
