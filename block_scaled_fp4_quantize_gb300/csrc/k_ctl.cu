@@ -91,44 +91,6 @@ __device__ __forceinline__ bool nonfinite2(uint32_t m) {
   return (m & 0xFFFFu) >= 0x7F80u || (m >> 16) >= 0x7F80u;
 }
 
-// How x' = u / S is formed on the fast path.
-enum NMode : int {
-  NM_NONE = 0,  // no outer scale: x' = u
-  NM_MARK = 1,  // Markstein's correction from RN(1 / S): the pair (S, -1 / S)
-  NM_BMR = 2,   // the known-divisor method: the pair (zh, zl) of S (zsplit below)
-};
-
-// The split reciprocal (zh, zl) = (RD(1 / S), RN(1 / S - zh)) of an outer
-// scale S = RN(A / (scale_max * 6)) whose amax A is a bf16 value (the
-// maximum of bf16 inputs): S's significand is that of RN(m / 21), m = 128 ..
-// 255 A's significand, so the pair for it comes from a 128-entry table and
-// is scaled by S's power of two.  For every such divisor and every bf16
-// dividend, RN(u zh + RN(u zl)) = RN(u / S) (checked with exact rationals
-// for all 128 x 255 significand pairs); the scaled zl stays normal while S
-// < 2^90 (the smallest table zl is above 2^-30), which callers check.
-__device__ __forceinline__ void zsplit(uint32_t Abits, float S, const float2* ztab, float& zh, float& zl) {
-  const float2 z = ztab[(Abits >> 16) & 0x7Fu];
-  const uint32_t adj = 0x3F800000u - (fbits(S) & 0x7F800000u);
-  zh = bitsf(fbits(z.x) + adj);
-  zl = fbits(z.y) ? bitsf(fbits(z.y) + adj) : 0.0f;
-}
-
-// Fill the table of zsplit: entry m for the significand sigma of RN((128 +
-// m) / 21), zh = RD(1 / sigma) and zl = RN(1 / sigma - zh), where
-// 1 / sigma - zh = (1 - zh sigma) / sigma and 1 - zh sigma is exact in one
-// fused multiply-add.
-__device__ __forceinline__ void build_ztab(float2* ztab, int t) {
-  if (t < 128) {
-    const float q = ieee_div((float)(128 + t), 21.0f);   // in [6.09, 12.15]
-    const float sg = ieee_mul(q, q < 8.0f ? 0.25f : 0.125f);  // exact: [1, 2)
-    float zh, e, zl;
-    asm("div.rm.f32 %0, 0f3F800000, %1;" : "=f"(zh) : "f"(sg));
-    asm("{\n\t.reg .f32 n;\n\tneg.f32 n, %1;\n\tfma.rn.f32 %0, n, %2, 0f3F800000;\n\t}" : "=f"(e) : "f"(zh), "f"(sg));
-    zl = ieee_div(e, sg);
-    ztab[t] = make_float2(zh, zl);
-  }
-}
-
 // x' for a pair of values (lo, hi) packed from a bf16x2 word w.
 template <int NM>
 __device__ __forceinline__ uint64_t norm2(uint32_t w, uint64_t P, uint64_t Q) {

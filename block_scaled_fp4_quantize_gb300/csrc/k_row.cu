@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
   __shared__ __align__(128) unsigned char buf[QS][QB * 32];
   __shared__ float4 tab[256];
   __shared__ __align__(8) uint64_t bars[QS];
+  __shared__ float2 ztab[128];
   const int t = threadIdx.x, lane = t & 31;
   const int64_t nblk = j.G * j.M * j.K / 16, nch = (nblk + QB - 1) / QB;
   const unsigned char* xb = static_cast<const unsigned char*>(j.x);
@@ -286,14 +287,17 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
     }
   }
   build_scale_table<UE5M3>(tab, t, RT);
+  if (RO == RO_WARP || RO == RO_UNIFORM) build_ztab(ztab, t);
   const TabView tv{tab};
   const int per = RO == RO_WARP || RO == RO_BUFFER ? j.ob / 16 : 1;
   const bool per_pow2 = (per & (per - 1)) == 0;
   const int lper = 31 - __clz(per);
   float S_u = 1.0f, r_u = 1.0f;
+  uint32_t A_u = 0;  // the tensorwise amax, when it is computed here (bf16 input: a bf16 value)
   if (RO == RO_UNIFORM) {
     if (j.s_src == S_TENSORWISE_WS) {
-      S_u = ieee_div(bitsf(*j.tw_amax), UE5M3 ? 688128.0f : 2688.0f);
+      A_u = *j.tw_amax;
+      S_u = ieee_div(bitsf(A_u), UE5M3 ? 688128.0f : 2688.0f);
       if (blockIdx.x == 0 && t == 0 && j.tile_outer) j.tile_outer[0] = S_u;
     } else {
       S_u = j.tile_outer[0];
@@ -301,6 +305,9 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
     r_u = ieee_rcp(S_u);
   }
   __syncthreads();
+  float zh_u = 0.0f, zl_u = 0.0f;
+  const bool u_z = RO == RO_UNIFORM && j.s_src == S_TENSORWISE_WS && (A_u & 0xFFFFu) == 0u && zsplit_ok(A_u, S_u);
+  if (u_z) zsplit(A_u, S_u, ztab, zh_u, zl_u);
   int slot = 0;
   uint32_t phase = 0;
   for (int64_t c = blockIdx.x; c < nch; c += gridDim.x) {
@@ -333,31 +340,46 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
     n.none = RO == RO_NONE;
     n.S = 1.0f;
     n.r = 1.0f;
+    bool zfast = u_z;  // the table-driven division of fp4q_block.cuh (zsplit)
+    float zh = zh_u, zl = zl_u;
     if (RO == RO_UNIFORM) {
       n.S = S_u;
       n.r = r_u;
     } else if (RO == RO_WARP) {
       uint32_t g = fbits(am);
       for (int o = 1; o < per; o <<= 1) g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
-      outer_sr<UE5M3>(bitsf(g), n.S, n.r);
+      // the outer amax of bf16 inputs is a bf16 value: the table-driven
+      // division when the warp's scales are in its range
+      const float S = div_bmr(bitsf(g), bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
+      zfast = __all_sync(0xFFFFFFFFu, zsplit_ok(g, S));
+      if (zfast) {
+        n.S = S;
+        zsplit(g, S, ztab, zh, zl);
+      } else {
+        outer_sr<UE5M3>(bitsf(g), n.S, n.r);
+      }
       if (j.row_outer && j.do_row && valid && (lane & (per - 1)) == 0) j.row_outer[b >> lper] = n.S;
     } else if (RO == RO_BUFFER) {
       if (valid) n.S = j.row_outer[per_pow2 ? (b >> lper) : b / per];
       n.r = ieee_rcp(n.S);
     }
     uint32_t sc, w0, w1;
-    float a = am;
-    const bool fast = __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
-    if (fast) {
-      sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, j.srk, 0u, 0u, 0ull, w0, w1);
+    if (zfast) {
+      sc = block_zsplit<UE5M3>(tab, u, am, zh, zl, w0, w1);
     } else {
-      n.pos = n.none || positive(n.S);
-      n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
-      float4 T;
-      sc = block_scale<UE5M3>(tv, am, n, T);
-      float x[16], dq[16];
-      normalize16<false>(u, x, n);
-      encode16<false, false>(x, T, n, j.srk, 0u, 0u, 0ull, w0, w1, dq);
+      float a = am;
+      const bool fast = __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
+      if (fast) {
+        sc = block_fast<false, UE5M3, RO != RO_NONE, false>(tab, u, a, n.S, n.r, j.srk, 0u, 0u, 0ull, w0, w1);
+      } else {
+        n.pos = n.none || positive(n.S);
+        n.fast = !n.none && positive_normal(n.S) && positive_normal(n.r);
+        float4 T;
+        sc = block_scale<UE5M3>(tv, am, n, T);
+        float x[16], dq[16];
+        normalize16<false>(u, x, n);
+        encode16<false, false>(x, T, n, j.srk, 0u, 0u, 0ull, w0, w1, dq);
+      }
     }
     if (valid) {
       *reinterpret_cast<uint2*>(j.row_codes + 8 * b) = make_uint2(w0, w1);
