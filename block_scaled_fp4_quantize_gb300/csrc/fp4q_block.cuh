@@ -364,20 +364,23 @@ __device__ __forceinline__ uint32_t block_zsplit(const float4* tab, const float 
   return sc;
 }
 
-// Inner-scale table in shared memory: entry c holds (DEC(c), zh, zl) with
-// zh + zl the split reciprocal of DEC(c) used by div_bmr.
+// Inner-scale table entry of code c: (DEC(c), zh, zl, 0) with zh + zl the
+// split reciprocal of DEC(c) used by div_bmr.
+template <bool UE5M3>
+__device__ __forceinline__ float4 scale_entry(uint32_t c) {
+  const int bias = UE5M3 ? 15 : 7;
+  const uint32_t e = c >> 3, m = c & 7u;
+  const uint32_t M = e ? 8u + m : m;
+  const int ex = e ? (int)e - 3 - bias : -2 - bias;
+  const uint32_t hi = kRcpHi[M], lo = kRcpLo[M];
+  return make_float4(dec_scale(c, scale_fmt(UE5M3 ? 1 : 0)), M ? bitsf((uint32_t)((int)hi - ex * 8388608)) : 0.0f,
+                     lo ? bitsf((uint32_t)((int)lo - ex * 8388608)) : 0.0f, 0.0f);
+}
+
+// Inner-scale table in shared memory (entries of scale_entry).
 template <bool UE5M3>
 __device__ __forceinline__ void build_scale_table(float4* tab, int t, int nthreads) {
-  for (int c = t; c < 256; c += nthreads) {
-    const int bias = UE5M3 ? 15 : 7;
-    const uint32_t e = (uint32_t)c >> 3, m = (uint32_t)c & 7u;
-    const uint32_t M = e ? 8u + m : m;
-    const int ex = e ? (int)e - 3 - bias : -2 - bias;
-    const uint32_t hi = kRcpHi[M], lo = kRcpLo[M];
-    tab[c] = make_float4(dec_scale((uint32_t)c, scale_fmt(UE5M3 ? 1 : 0)),
-                         M ? bitsf((uint32_t)((int)hi - ex * 8388608)) : 0.0f,
-                         lo ? bitsf((uint32_t)((int)lo - ex * 8388608)) : 0.0f, 0.0f);
-  }
+  for (int c = t; c < 256; c += nthreads) tab[c] = scale_entry<UE5M3>((uint32_t)c);
 }
 
 }  // namespace

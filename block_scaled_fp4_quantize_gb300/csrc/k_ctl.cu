@@ -6,9 +6,9 @@
 // training", "Technical design": outer and inner scales), for the calls whose
 // facts let every bound check fold away: M a multiple of 128, K of 64, bf16
 // input, round-to-nearest, both orientations, linear scale layout, and an
-// outer scale that is none, one per tensor, 1 x 64 / 64 x 1 or 64 x 64.
-// Every other call takes the general cast-transpose kernel (k_ctb.cuh), which
-// gives the same bits.
+// outer scale that is none, one per tensor (from the tensorwise amax), 1 x 64
+// / 64 x 1 or 64 x 64.  Every other call takes the general cast-transpose
+// kernel (k_ctb.cuh), which gives the same bits.
 //
 // Per tile, one CTA barrier.  Before it, every thread takes the block maxima
 // it needs from the raw tile (rowwise: its half row, two 1 x 16 blocks;
@@ -22,17 +22,27 @@
 // buffers by tile parity, and the tile after next is copied into the slot
 // whose last reader is past this barrier.
 //
-// The arithmetic is that of fp4q_block.cuh: x' = u / S by Markstein's
-// correction from RN(1 / S), a = RN(amax / S) and v = RN(a / 6) two blocks
-// per instruction (packed binary32 pairs), t = x' / s by the known-divisor
-// method, E2M1 and E4M3 by the hardware conversions.  A warp whose outer
-// scales or block maxima leave the range those sequences cover (maxima
-// below 2^-90, non-finite inputs) takes the general per-block steps with
-// div.rn for its tile.
+// The arithmetic.  The outer amax A of bf16 data is a bf16 value, so S =
+// RN(A / (scale_max * 6)) has one of 128 significands (set by the 7 mantissa
+// bits m of A) and an inner scale s one of 8 (its 3 mantissa bits j).  For
+// every pair (j, m) the table of fp4q_pairtab.cuh holds multipliers c1, c2
+// with which RN(RN(u c1) c2) has the E2M1 code of the two rounded divisions
+// RN(RN(u / S) / s) for every bf16 u (checked by enumeration): two packed
+// multiplies per pair of values.  The inner scale itself, a = RN(am / S) and
+// v = RN(a / 6), comes from the known-divisor method (exact for bf16
+// dividends), its E4M3 code from the hardware conversion.  The table rows are
+// kept in shared memory with the exponent of S folded in less the bits of A,
+// so a block's multipliers are two table loads and two integer adds.  A warp
+// whose outer amax lies outside [2^-90, 2^101) (2^109 for UE5M3 scales),
+// where the scaled entries stay normal, takes the general per-block steps
+// with div.rn.
 #include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
+#include "fp4q_pairtab.cuh"
 #include "fp4q_tma.cuh"
+
+#include <type_traits>
 
 namespace fp4q {
 namespace {
@@ -40,24 +50,124 @@ namespace {
 constexpr int LT = 256;           // threads per CTA
 constexpr int LM = 128, LK = 64;  // tile
 constexpr int LRAW = LM * LK * 2; // bytes of one raw bf16 tile
+static_assert(LT == 256, "one thread per scale code builds the code tables");
 
 // Shared memory (offsets from the 1024-byte aligned base)
 struct LL {
-  __host__ __device__ static constexpr int raw(int s) { return s * LRAW; }             // 2 slots
-  __host__ __device__ static constexpr int ccs(int s) { return 2 * LRAW + s * 4096; }  // col codes, [64][64] swizzled
-  __host__ __device__ static constexpr int sst(int s) { return 2 * LRAW + 2 * 4096 + s * 512; }  // col scales [64][8]
-  static constexpr int tab = 2 * LRAW + 2 * 4096 + 2 * 512;                            // 256 x (s, zh, zl, -)
-  __host__ __device__ static constexpr int red(int s) { return tab + 4096 + s * 1024; }  // [8 warps][32 lanes] u32
-  static constexpr int ztab = tab + 4096 + 2 * 1024;                                   // 128 x (zh, zl)
-  static constexpr int bars = ztab + 1024;                                             // 2 mbarriers
-  static constexpr int total = bars + 16 + 1024;                                       // + alignment slack
+  __host__ __device__ static constexpr int raw(int s) { return s * LRAW; }                       // 2 slots
+  __host__ __device__ static constexpr int ccs(int s) { return 2 * LRAW + s * 4096; }            // col codes, [64][64] swizzled
+  __host__ __device__ static constexpr int sst(int s) { return 2 * LRAW + 8192 + s * 512; }      // col scales [64][8]
+  __host__ __device__ static constexpr int red(int s) { return 2 * LRAW + 9216 + s * 1024; }     // [8 warps][32 lanes] u32
+  static constexpr int pt = 2 * LRAW + 11264;  // 10 rows x 128 x (u32, u32), rows 1024 bytes apart
+                                               // (no outer scale: 256 x (c1, c2) by scale code)
+  static constexpr int ctab = pt + 10240;      // 256 x u32: scale code -> row and exponent of 1 / s
+  static constexpr int bars = ctab + 1024;     // 2 mbarriers
+  static constexpr int total = bars + 16 + 1024;  // + alignment slack
 };
+// rows of the shared table besides the 8 pair rows: s = 0, and the split
+// reciprocal (zh, zl) of S
+constexpr uint32_t PT_ZERO = 8, PT_RCP = 9;
 
 // Outer-scale form of a launch
 enum LO : int { LO_NONE = 0, LO_UNIFORM = 1, LO_1D = 2, LO_2D = 3 };
 
 // Set by a tile wait that ran out; read and cleared by fp4q_device_status.
 __device__ unsigned int g_ctl_timeout = 0;
+
+// bits of the amax A = scale_max * 6 (S = 1): the table position of "no outer scale"
+template <bool UE5M3>
+__device__ __forceinline__ constexpr uint32_t unit_amax() { return UE5M3 ? 0x49280000u : 0x45280000u; }
+
+// The amax bits A (a bf16 value) admit the table path: A in [2^-90, 2^101)
+// (E4M3) or [2^-90, 2^109) (UE5M3), so that 2^-90 < S < 2^90.
+template <bool UE5M3>
+__device__ __forceinline__ bool table_ok(uint32_t A) {
+  return A - kTiny < (UE5M3 ? 0x76000000u : 0x72000000u) - kTiny;
+}
+
+// The scale code's table row and exponent: s = (1 + row / 8) 2^e_s, or row
+// PT_ZERO for s = 0.
+template <bool UE5M3>
+__device__ __forceinline__ uint32_t code_row(uint32_t code, int& es) {
+  const uint32_t ex = code >> 3, m3 = code & 7u;
+  const int bias = UE5M3 ? 15 : 7;
+  if (ex) {
+    es = (int)ex - bias;
+    return m3;
+  }
+  es = 0;
+  if (!m3) return PT_ZERO;
+  const int p = 31 - __clz((int)m3);  // subnormal s = m3 2^(-2 - bias)
+  es = p - 2 - bias;
+  return (m3 << (3 - p)) & 7u;
+}
+
+// Fill the shared tables of the outer-scale forms from kPairTab: entry m of
+// each row with c1 (row PT_RCP: zh and zl) plus the exponent offset of S for
+// an amax of mantissa m, plus m << 16, so that c1 - A is c1 / 2^e_S.  S =
+// RN(A / (21 2^(K - 5))) = sigma_m 2^(e_A - K + c), c = 1 when (128 + m) / 21
+// >= 8, i.e. m >= 40.  ctab[code] = (row << 10) | ((-e_s) << 23).
+template <bool UE5M3>
+__device__ __forceinline__ void build_tables(unsigned char* ptb, uint32_t* ctab, int t) {
+  constexpr uint32_t K = UE5M3 ? 20u : 12u;
+  const uint4* src = reinterpret_cast<const uint4*>(&kPairTab[0][0][0]);
+  uint4* dst = reinterpret_cast<uint4*>(ptb);
+  for (int i = t; i < 10 * 64; i += LT) {  // two entries per 16 bytes
+    const uint32_t row = (uint32_t)i >> 6, m = ((uint32_t)i & 63u) * 2;
+    uint4 e = src[i];
+    const uint32_t o0 = ((127u + K - (m >= 40 ? 1u : 0u)) << 23) + (m << 16);
+    const uint32_t o1 = ((127u + K - (m + 1 >= 40 ? 1u : 0u)) << 23) + ((m + 1) << 16);
+    e.x += o0;
+    e.z += o1;
+    if (row == PT_RCP) {
+      e.y += o0;
+      e.w += o1;
+    }
+    dst[i] = e;
+  }
+  int es;
+  const uint32_t row = code_row<UE5M3>((uint32_t)t, es);
+  ctab[t] = (row << 10) | ((uint32_t)(-es) << 23);
+}
+
+// The table of the form without outer scale (S = 1, sigma = 1: m = 40):
+// ntab[code] = (c1, c2 / 2^e_s), c2 = 0 for s = 0.
+template <bool UE5M3>
+__device__ __forceinline__ void build_unit_table(uint2* ntab, int t) {
+  int es;
+  const uint32_t row = code_row<UE5M3>((uint32_t)t, es);
+  const uint32_t c1 = kPairTab[row][40][0], c2 = kPairTab[row][40][1];
+  ntab[t] = make_uint2(c1, row == PT_ZERO ? 0u : c2 + ((uint32_t)(-es) << 23));
+}
+
+// byte offset of the amax's mantissa in a table row
+__device__ __forceinline__ uint32_t moff_of(uint32_t A) { return (A >> 13) & 0x3F8u; }
+
+// c1 and c2 of a block with scale code sc whose outer amax has bits A
+__device__ __forceinline__ void pair_mults(const unsigned char* ptb, const uint32_t* ctab, uint32_t sc, uint32_t A,
+                                           float& c1, float& c2) {
+  const uint32_t w = ctab[sc];
+  const uint2 e = *reinterpret_cast<const uint2*>(ptb + (w & 0xFFFFu) + moff_of(A));
+  c1 = bitsf(e.x - A);
+  c2 = bitsf(e.y + (w & 0xFF800000u));
+}
+
+// split reciprocal (zh, zl) of S for the amax bits A
+__device__ __forceinline__ void outer_rcp(const unsigned char* ptb, uint32_t A, float& zh, float& zl) {
+  const uint2 e = *reinterpret_cast<const uint2*>(ptb + PT_RCP * 1024u + moff_of(A));
+  zh = bitsf(e.x - A);
+  zl = bitsf(e.y - A);
+}
+
+// Column loads of rows c and c + 8 (shared-memory offset OFF of the slot;
+// ca: the lane's address in slot 0, row 0; the 128-byte swizzle XORs the
+// 16-byte chunk index, address bits 4..6, with the row mod 8).
+template <int OFF, int c>
+__device__ __forceinline__ void lds_col(uint32_t ca, uint32_t (&wv)[16]) {
+  const uint32_t a = ca ^ ((uint32_t)c << 4);
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(wv[c]) : "r"(a), "n"(OFF + c * 128) : "memory");
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(wv[c + 8]) : "r"(a), "n"(OFF + c * 128 + 1024) : "memory");
+}
 
 __device__ __forceinline__ void issue_tile(const CUtensorMap* map, const TilePos& p, unsigned char* raw, uint64_t* bar) {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -86,85 +196,71 @@ __device__ __forceinline__ uint32_t rowmax2(const uint4 (&a)[4]) {
   return bf16x2_amax(__byte_perm(m[0], m[1], 0x5410), __byte_perm(m[0], m[1], 0x7632)) & 0x7FFF7FFFu;
 }
 
-// A packed pair of |max| bf16 halves holds a non-finite value.
-__device__ __forceinline__ bool nonfinite2(uint32_t m) {
-  return (m & 0xFFFFu) >= 0x7F80u || (m >> 16) >= 0x7F80u;
-}
+// A packed pair of |max| bf16 halves (each at most 0x7FFF) holds a
+// non-finite value: a half at or above 0x7F80 carries into its bit 15.
+__device__ __forceinline__ bool nonfinite2(uint32_t m) { return ((m + 0x00800080u) & 0x80008000u) != 0u; }
 
-// x' for a pair of values (lo, hi) packed from a bf16x2 word w.
-template <int NM>
-__device__ __forceinline__ uint64_t norm2(uint32_t w, uint64_t P, uint64_t Q) {
-  if (NM == NM_MARK) return markstein2(pk2(nbf16lo(w), nbf16hi(w)), P, Q);
-  if (NM == NM_BMR) return bmr2(pk2(bf16lo(w), bf16hi(w)), P, Q);
-  return pk2(bf16lo(w), bf16hi(w));
-}
-
-// Inner scales of two blocks at once: a = RN(am / S) (or am), v = RN(a /
-// 6), codes (low byte block 0), and their table entries.  am2: the blocks'
-// maxima as bf16 halves.
-template <bool UE5M3, int NM>
-__device__ __forceinline__ uint32_t scales2(const float4* tab, uint32_t am2, uint64_t P, uint64_t Q, float4& T0,
-                                            float4& T1) {
-  const float m0 = bitsf(am2 << 16), m1 = bitsf(am2 & 0xFFFF0000u);
-  uint64_t a2;
-  if (NM == NM_MARK) a2 = markstein2(pk2(bitsf(fbits(m0) | 0x80000000u), bitsf(fbits(m1) | 0x80000000u)), P, Q);
-  else if (NM == NM_BMR) a2 = bmr2(pk2(m0, m1), P, Q);
-  else a2 = pk2(m0, m1);
-  const uint64_t v2 = bmr2(a2, pk2(bitsf(kSixHi), bitsf(kSixHi)), pk2(bitsf(kSixLo), bitsf(kSixLo)));
+// Inner-scale codes of two blocks (block 0 in the low byte) from their
+// maxima am2 (bf16 halves): a = am, or RN(am / S) from the split reciprocal
+// pairs (ZH, ZL); v = RN(a / 6); the E4M3 / UE5M3 code of v.
+template <bool UE5M3, bool OUTER>
+__device__ __forceinline__ uint32_t codes2(uint32_t am2, uint64_t ZH, uint64_t ZL) {
+  uint64_t a2 = pk2(bitsf(am2 << 16), bitsf(am2 & 0xFFFF0000u));
+  if (OUTER) a2 = bmr2(a2, ZH, ZL);
   float v0, v1;
-  upk2(v2, v0, v1);
+  upk2(bmr2(a2, pk2(bitsf(kSixHi), bitsf(kSixHi)), pk2(bitsf(kSixLo), bitsf(kSixLo))), v0, v1);
+  if (UE5M3) return enc_ue5m3(v0) | (enc_ue5m3(v1) << 8);
   uint32_t sc;
-  if (UE5M3) {
-    sc = enc_ue5m3(v0) | (enc_ue5m3(v1) << 8);
-  } else {
-    asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}" : "=r"(sc) : "f"(v1), "f"(v0));
-  }
-  T0 = tab[sc & 0xFFu];
-  T1 = tab[sc >> 8];
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}" : "=r"(sc) : "f"(v1), "f"(v0));
   return sc;
 }
 
-// Codes of one rowwise block from its 8 words (4 per uint4): x' (NM) and
-// t = x' / s, two values per instruction; element 2i in the low nibble of
-// byte i.
-template <int NM>
-__device__ __forceinline__ void row_codes16(const uint4& p, const uint4& q, uint64_t P, uint64_t Q, const float4& T,
-                                            uint32_t& w0, uint32_t& w1) {
-  const uint64_t ZH2 = pk2(T.y, T.y), ZL2 = pk2(T.z, T.z);
+// t = RN(RN(u c1) c2) for the pair of values of bf16x2 word w
+__device__ __forceinline__ uint64_t t2(uint32_t w, uint64_t C1, uint64_t C2) {
+  return mul2(mul2(pk2(bf16lo(w), bf16hi(w)), C1), C2);
+}
+
+// Codes of one rowwise block from its 8 words (4 per uint4); element 2i in
+// the low nibble of byte i.
+__device__ __forceinline__ void row_codes16(const uint4& p, const uint4& q, uint64_t C1, uint64_t C2, uint32_t& w0,
+                                            uint32_t& w1) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const uint4& v = h ? q : p;
     const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
     float t[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) upk2(bmr2(norm2<NM>(wd[i], P, Q), ZH2, ZL2), t[2 * i], t[2 * i + 1]);
+    for (int i = 0; i < 4; ++i) upk2(t2(wd[i], C1, C2), t[2 * i], t[2 * i + 1]);
     (h ? w1 : w0) = e2m1x8_rne(t);
   }
 }
 
 // Codes of the two column blocks of a lane from its 16 words (word i: row i,
 // column 2 lane in the low half, 2 lane + 1 in the high half): the pairs run
-// across the two columns, each with its own outer and inner scale; c[0],
-// c[1]: column 2 lane, rows 0-7 and 8-15; c[2], c[3]: column 2 lane + 1.
-template <int NM>
-__device__ __forceinline__ void col_codes16(const uint32_t (&w)[16], uint64_t P, uint64_t Q, const float4& T0,
-                                            const float4& T1, uint32_t (&c)[4]) {
-  const uint64_t ZH2 = pk2(T0.y, T1.y), ZL2 = pk2(T0.z, T1.z);
+// across the two columns, each with its own multipliers; c[0], c[1]: column
+// 2 lane, rows 0-7 and 8-15; c[2], c[3]: column 2 lane + 1.
+__device__ __forceinline__ void col_codes16(const uint32_t (&w)[16], uint64_t C1, uint64_t C2, uint32_t (&c)[4]) {
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float t0[8], t1[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) upk2(bmr2(norm2<NM>(w[8 * h + i], P, Q), ZH2, ZL2), t0[i], t1[i]);
+    for (int i = 0; i < 8; ++i) upk2(t2(w[8 * h + i], C1, C2), t0[i], t1[i]);
     c[h] = e2m1x8_rne(t0);
     c[2 + h] = e2m1x8_rne(t1);
   }
 }
 
+// Inner-scale table entries computed on demand (for the general steps).
+template <bool UE5M3>
+struct EntryCalc {
+  __device__ __forceinline__ float4 operator[](uint32_t c) const { return scale_entry<UE5M3>(c); }
+};
+
 // The general per-block steps (div.rn where the FMA sequences do not reach):
-// 16 values u (as -u when NEG), block maximum am, outer scale S, R = 1 / S.
-template <bool UE5M3, bool NEG>
-__device__ __forceinline__ uint32_t slow_block(const float4* tab, const float (&v)[16], float am, float S, float R,
-                                               bool none, const PhiloxKeys& K, uint32_t& w0, uint32_t& w1) {
+// 16 values u, block maximum am, outer scale S, R = 1 / S.
+template <bool UE5M3>
+__device__ __forceinline__ uint32_t slow_block(const float (&v)[16], float am, float S, float R, bool none,
+                                               const PhiloxKeys& K, uint32_t& w0, uint32_t& w1) {
   Norm n;
   n.none = none;
   n.S = S;
@@ -172,20 +268,15 @@ __device__ __forceinline__ uint32_t slow_block(const float4* tab, const float (&
   n.pos = none || positive(S);
   n.fast = !none && positive_normal(S) && positive_normal(R);
   struct {
-    const float4* tab;
-  } tv{tab};
+    EntryCalc<UE5M3> tab;
+  } tv;
   float4 T;
   const uint32_t sc = block_scale<UE5M3>(tv, am, n, T);
   float x[16], dq[16];
-  if (NEG) normalize16_neg<false>(v, x, n);
-  else normalize16<false>(v, x, n);
+  normalize16<false>(v, x, n);
   encode16<false, false>(x, T, n, K, 0u, 0u, 0ull, w0, w1, dq);
   return sc;
 }
-
-// Fast-path mode of a pass, warp-uniform: the general per-block steps, or
-// NM_NONE / NM_MARK / NM_BMR.
-constexpr int PM_SLOW = -1;
 
 template <bool UE5M3, int LOF>
 __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
@@ -195,8 +286,8 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  float4* tab = reinterpret_cast<float4*>(smem + LL::tab);
-  float2* ztab = reinterpret_cast<float2*>(smem + LL::ztab);
+  const unsigned char* ptb = smem + LL::pt;
+  const uint32_t* ctab = reinterpret_cast<const uint32_t*>(smem + LL::ctab);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LL::bars);
 
   TileIter cur;
@@ -212,8 +303,8 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
     if (cur.idx + (int)gridDim.x < cur.ntiles)
       issue_tile(&tmap, cur.pos_of<LM>(cur.idx + (int)gridDim.x), smem + LL::raw(1), &bars[1]);
   }
-  build_scale_table<UE5M3>(tab, t, LT);
-  if (OUTER) build_ztab(ztab, t);
+  if (OUTER) build_tables<UE5M3>(smem + LL::pt, reinterpret_cast<uint32_t*>(smem + LL::ctab), t);
+  else build_unit_table<UE5M3>(reinterpret_cast<uint2*>(smem + LL::pt), t);
   const float denh = bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), denl = bitsf(UE5M3 ? kDenLoU5 : kDenLoE4);
 
   // rowwise: thread t owns row t / 2, columns 32 (t mod 2) .. + 31 (two
@@ -223,95 +314,93 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
 #pragma unroll
   for (int q = 0; q < 4; ++q) roff[q] = (uint32_t)(rr * 128 + (((4 * rh + q) ^ (rr & 7)) << 4));
   // columnwise: warp w owns rows 16 w .. + 15, lane l columns 2 l, 2 l + 1
-  const uint32_t coff = (uint32_t)(warp * 2048 + (lane & 3) * 4);
-  const int cunit = lane >> 2;
+  const uint32_t ca = smem_u32(smem) + (uint32_t)(warp * 2048 + (lane & 3) * 4 + ((lane >> 2) << 4));
   __syncthreads();
 
-  // one scale for the whole tensor: from the amax in the workspace, or given
-  float S_u = 1.0f, R_u = 1.0f, zh_u = 0.0f, zl_u = 0.0f;
-  int um = NM_MARK;  // the uniform scale's fast mode (CTA-uniform)
-  bool u_ok = true;  // S_u and 1 / S_u normal
+  // one scale for the whole tensor, from the tensorwise amax in the
+  // workspace (a bf16 value: the table path when in range)
+  uint32_t A_u = unit_amax<UE5M3>();
+  float S_u = 1.0f, R_u = 1.0f;
+  uint64_t ZH_u = 0ull, ZL_u = 0ull;
+  bool u_fast = true;
   if (LOF == LO_UNIFORM) {
-    uint32_t Ab = 0;
-    if (j.s_src == S_TENSORWISE_WS) {
-      Ab = *j.tw_amax;
-      S_u = ieee_div(bitsf(Ab), UE5M3 ? 688128.0f : 2688.0f);
-      if (blockIdx.x == 0 && t == 0 && j.tile_outer) j.tile_outer[0] = S_u;
-    } else {
-      S_u = j.tile_outer[0];
-    }
+    A_u = *j.tw_amax;
+    S_u = ieee_div(bitsf(A_u), UE5M3 ? 688128.0f : 2688.0f);
+    if (blockIdx.x == 0 && t == 0 && j.tile_outer) j.tile_outer[0] = S_u;
     R_u = ieee_rcp(S_u);
-    u_ok = positive_normal(S_u) && positive_normal(R_u);
-    // an amax that is a bf16 value (every bf16 tensor's is) in range
-    if (j.s_src == S_TENSORWISE_WS && (Ab & 0xFFFFu) == 0u && Ab >= kTiny && fbits(S_u) < 0x6C800000u) {
-      um = NM_BMR;
-      zsplit(Ab, S_u, ztab, zh_u, zl_u);
+    u_fast = (A_u & 0xFFFFu) == 0u && table_ok<UE5M3>(A_u);
+    if (u_fast) {
+      float zh, zl;
+      outer_rcp(ptb, A_u, zh, zl);
+      ZH_u = pk2(zh, zh);
+      ZL_u = pk2(zl, zl);
     }
   }
 
-  int slot = 0;
+  // c1, c2 of a block with scale code sc and outer amax bits A
+  auto mults = [&](uint32_t sc, uint32_t A, float& c1, float& c2) {
+    if (OUTER) {
+      pair_mults(ptb, ctab, sc, A, c1, c2);
+    } else {
+      const uint2 e = reinterpret_cast<const uint2*>(ptb)[sc];
+      c1 = bitsf(e.x);
+      c2 = bitsf(e.y);
+    }
+  };
+
   uint32_t phase = 0;
   int pg = 0, pm0 = 0, pk0 = 0;  // the previous tile
   int prev_par = 0;
   bool have_prev = false;
-  for (int it = 0; cur.valid(); ++it) {
-    const int par = it & 1;
+  // One tile; the walk alternates the two input slots and the two staging
+  // buffers, so the loop runs two tiles per iteration with the parity a
+  // compile-time constant (shared-memory offsets fold into the loads).
+  auto tile = [&](auto PC) {
+    constexpr int par = decltype(PC)::value;  // input slot and staging buffer
     const int tg = cur.g, tm0 = cur.tm * LM, tk0 = cur.tk * LK;  // this tile
     const int after = cur.idx + 2 * (int)gridDim.x;              // the tile that takes this slot next
     cur.next();
-    const unsigned char* raw = smem + LL::raw(slot);
+    const unsigned char* raw = smem + LL::raw(par);
     // a wait that runs out raises the error flag; the walk goes on (every
     // later wait is bounded and every barrier is still reached)
-    if (!mbar_wait(&bars[slot], phase, 1u << 22)) atomicExch(&g_ctl_timeout, 1u);
+    if (!mbar_wait(&bars[par], phase, 1u << 22)) atomicExch(&g_ctl_timeout, 1u);
     uint32_t* red = reinterpret_cast<uint32_t*>(smem + LL::red(par));
     const int64_t row = (int64_t)tg * j.M + tm0 + rr;  // this thread's row of the [G M, K] view
 
-    // rowwise: scales, codes and stores of the thread's two blocks; mode:
-    // the fast form (P, Q its constants), or PM_SLOW
-    auto row_pass = [&](const uint4 (&a)[4], uint32_t ram, int mode, float S, float R, uint64_t P, uint64_t Q) {
-      uint32_t c[4], sc;
-      if (mode == NM_BMR || mode == NM_NONE) {
-        float4 T0, T1;
-        if (LOF == LO_NONE) {
-          sc = scales2<UE5M3, NM_NONE>(tab, ram, P, Q, T0, T1);
-          row_codes16<NM_NONE>(a[0], a[1], P, Q, T0, c[0], c[1]);
-          row_codes16<NM_NONE>(a[2], a[3], P, Q, T1, c[2], c[3]);
-        } else {
-          sc = scales2<UE5M3, NM_BMR>(tab, ram, P, Q, T0, T1);
-          row_codes16<NM_BMR>(a[0], a[1], P, Q, T0, c[0], c[1]);
-          row_codes16<NM_BMR>(a[2], a[3], P, Q, T1, c[2], c[3]);
-        }
-      } else if (OUTER && mode == NM_MARK) {
-        float4 T0, T1;
-        sc = scales2<UE5M3, NM_MARK>(tab, ram, P, Q, T0, T1);
-        row_codes16<NM_MARK>(a[0], a[1], P, Q, T0, c[0], c[1]);
-        row_codes16<NM_MARK>(a[2], a[3], P, Q, T1, c[2], c[3]);
-      } else {
-        const float am0 = bitsf(ram << 16), am1 = bitsf(ram & 0xFFFF0000u);
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const uint32_t wd[8] = {a[2 * b].x, a[2 * b].y, a[2 * b].z, a[2 * b].w,
-                                  a[2 * b + 1].x, a[2 * b + 1].y, a[2 * b + 1].z, a[2 * b + 1].w};
-          float u[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            u[2 * i] = bf16lo(wd[i]);
-            u[2 * i + 1] = bf16hi(wd[i]);
-          }
-          const uint32_t s1 = slow_block<UE5M3, false>(tab, u, b ? am1 : am0, S, R, !OUTER, j.srk, c[2 * b], c[2 * b + 1]);
-          sc = b ? (sc | (s1 << 8)) : s1;
-        }
-      }
+    auto row_store = [&](const uint32_t (&c)[4], uint32_t sc) {
       const int64_t e = row * j.K + tk0 + 32 * rh;  // flat index of the thread's first element
       *reinterpret_cast<uint4*>(j.row_codes + (e >> 1)) = make_uint4(c[0], c[1], c[2], c[3]);
       *reinterpret_cast<uint16_t*>(j.row_scales + (e >> 4)) = (uint16_t)sc;
     };
-    // Markstein's form with a scale not taken from a bf16 amax: every
-    // block maximum must be 0 or at least 2^-90 and a = RN(am / S) < 2^126
-    auto mark_ok = [&](uint32_t am2, float S, float R) {
-      float d0, d1;
-      return __all_sync(0xFFFFFFFFu, u_ok && fast_block(bitsf(am2 << 16), S, R, d0) &&
-                                         fast_block(bitsf(am2 & 0xFFFF0000u), S, R, d1));
+    // rowwise scales, codes and stores of the thread's two blocks, table path
+    // (A: the outer amax bits, ZH / ZL: the split reciprocal of S)
+    auto row_fast = [&](const uint4 (&a)[4], uint32_t ram, uint32_t A, uint64_t ZH, uint64_t ZL) {
+      const uint32_t sc = codes2<UE5M3, OUTER>(ram, ZH, ZL);
+      float c10, c20, c11, c21;
+      mults(sc & 0xFFu, A, c10, c20);
+      mults(sc >> 8, A, c11, c21);
+      uint32_t c[4];
+      row_codes16(a[0], a[1], pk2(c10, c10), pk2(c20, c20), c[0], c[1]);
+      row_codes16(a[2], a[3], pk2(c11, c11), pk2(c21, c21), c[2], c[3]);
+      row_store(c, sc);
+    };
+    // the same by the general per-block steps
+    auto row_slow = [&](const uint4 (&a)[4], uint32_t ram, float S, float R) {
+      uint32_t c[4], sc = 0;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t wd[8] = {a[2 * b].x, a[2 * b].y, a[2 * b].z, a[2 * b].w,
+                                a[2 * b + 1].x, a[2 * b + 1].y, a[2 * b + 1].z, a[2 * b + 1].w};
+        float u[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          u[2 * i] = bf16lo(wd[i]);
+          u[2 * i + 1] = bf16hi(wd[i]);
+        }
+        const float am = bitsf(b ? (ram & 0xFFFF0000u) : (ram << 16));
+        sc |= slow_block<UE5M3>(u, am, S, R, !OUTER, j.srk, c[2 * b], c[2 * b + 1]) << (8 * b);
+      }
+      row_store(c, sc);
     };
 
     // ------------------------------------------ before the barrier: every read of the raw tile
@@ -333,32 +422,37 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
       for (int o = 16; o > 0; o >>= 1) m = umax(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       if (lane == 0) red[warp * 32] = m;
     } else if (LOF == LO_NONE) {  // the rowwise pass needs nothing from other warps: done here
-      row_pass(a, ram, NM_NONE, 1.0f, 1.0f, 0ull, 0ull);
+      row_fast(a, ram, unit_amax<UE5M3>(), 0ull, 0ull);
     } else if (LOF == LO_UNIFORM) {
-      if (um == NM_BMR) row_pass(a, ram, NM_BMR, S_u, R_u, pk2(zh_u, zh_u), pk2(zl_u, zl_u));
-      else row_pass(a, ram, mark_ok(ram, S_u, R_u) ? NM_MARK : PM_SLOW, S_u, R_u, pk2(S_u, S_u), pk2(-R_u, -R_u));
+      if (u_fast) row_fast(a, ram, A_u, ZH_u, ZL_u);
+      else row_slow(a, ram, S_u, R_u);
     } else {  // 1 x 64: the row's 64 columns are this thread's two blocks and its partner's
       uint32_t g = umax(ram & 0xFFFFu, ram >> 16);
       g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1)) << 16;
-      const float S = div_bmr(bitsf(g), denh, denl);  // exact for g >= 2^-90
       float* so = j.row_outer + row * (j.K >> 6) + (tk0 >> 6);
-      if (__all_sync(0xFFFFFFFFu, g >= kTiny && fbits(S) < 0x6C800000u)) {
-        if (rh == 0) *so = S;
+      if (__all_sync(0xFFFFFFFFu, table_ok<UE5M3>(g))) {
+        if (rh == 0) *so = div_bmr(bitsf(g), denh, denl);  // exact for g >= 2^-90
         float zh, zl;
-        zsplit(g, S, ztab, zh, zl);
-        row_pass(a, ram, NM_BMR, S, 1.0f, pk2(zh, zh), pk2(zl, zl));
+        outer_rcp(ptb, g, zh, zl);
+        row_fast(a, ram, g, pk2(zh, zh), pk2(zl, zl));
       } else {
         const float S1 = outer_scale<UE5M3>(bitsf(g));
         if (rh == 0) *so = S1;
-        row_pass(a, ram, PM_SLOW, S1, ieee_rcp(S1), 0ull, 0ull);
+        row_slow(a, ram, S1, ieee_rcp(S1));
       }
     }
-    uint32_t wv[16];  // rows 16 warp .. + 15, columns 2 lane (low halves) and 2 lane + 1 (high)
-    {
-      const unsigned char* rb = raw + coff;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) wv[i] = *reinterpret_cast<const uint32_t*>(rb + i * 128 + ((cunit ^ (i & 7)) << 4));
-    }
+    // rows 16 warp .. + 15, columns 2 lane (low halves) and 2 lane + 1
+    // (high): row i's word sits in 16-byte chunk cunit ^ (i mod 8), which is
+    // the per-lane base address with bits 4..6 XORed by i mod 8
+    uint32_t wv[16];
+    lds_col<LL::raw(par), 0>(ca, wv);
+    lds_col<LL::raw(par), 1>(ca, wv);
+    lds_col<LL::raw(par), 2>(ca, wv);
+    lds_col<LL::raw(par), 3>(ca, wv);
+    lds_col<LL::raw(par), 4>(ca, wv);
+    lds_col<LL::raw(par), 5>(ca, wv);
+    lds_col<LL::raw(par), 6>(ca, wv);
+    lds_col<LL::raw(par), 7>(ca, wv);
     uint32_t cam = colmax16(wv);
     if (nonfinite2(cam)) {
 #pragma unroll
@@ -371,7 +465,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
     __syncthreads();
 
     if (t == 0) {  // refill the slot, store the previous tile's staged column codes
-      if (after < cur.ntiles) issue_tile(&tmap, cur.pos_of<LM>(after), smem + LL::raw(slot), &bars[slot]);
+      if (after < cur.ntiles) issue_tile(&tmap, cur.pos_of<LM>(after), smem + LL::raw(par), &bars[par]);
       if (have_prev) {
         tma_store3(&cmap, smem + LL::ccs(par ^ 1), pm0 >> 1, pk0, pg);
         bulk_commit();
@@ -381,70 +475,64 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
       const uint2 v = *reinterpret_cast<const uint2*>(smem + LL::sst(par ^ 1) + t * 8);
       *reinterpret_cast<uint2*>(j.col_scales + ((int64_t)pg * j.K + pk0 + t) * (j.M >> 4) + (pm0 >> 4)) = v;
     }
-    if (++slot == 2) {
-      slot = 0;
-      phase ^= 1u;
-    }
 
     // ---------------------------------------- after the barrier: registers and staging only
-    float S2f = 1.0f, zh2 = 0.0f, zl2 = 0.0f;  // the 64 x 64 block's scale (2-D): both orientations
+    uint32_t A2 = 0;  // the 64 x 64 block's amax (2-D): both orientations
+    float S2f = 1.0f;
+    uint64_t ZH2 = 0ull, ZL2 = 0ull;
     bool f2 = true;
     if (LOF == LO_2D) {
       const uint32_t* rq = red + (warp >> 2) * 128;
-      const uint32_t A = umax(umax(rq[0], rq[32]), umax(rq[64], rq[96])) << 16;
-      S2f = div_bmr(bitsf(A), denh, denl);
-      f2 = A >= kTiny && fbits(S2f) < 0x6C800000u;  // uniform over the CTA half
-      if (f2) zsplit(A, S2f, ztab, zh2, zl2);
-      else S2f = outer_scale<UE5M3>(bitsf(A));
+      A2 = umax(umax(rq[0], rq[32]), umax(rq[64], rq[96])) << 16;
+      f2 = table_ok<UE5M3>(A2);  // uniform over the CTA half
+      if (f2) {
+        S2f = div_bmr(bitsf(A2), denh, denl);
+        float zh, zl;
+        outer_rcp(ptb, A2, zh, zl);
+        ZH2 = pk2(zh, zh);
+        ZL2 = pk2(zl, zl);
+      } else {
+        S2f = outer_scale<UE5M3>(bitsf(A2));
+      }
       if ((warp & 3) == 0 && lane == 0)
         j.tile_outer[((int64_t)tg * (j.M >> 6) + (tm0 >> 6) + (warp >> 2)) * (j.K >> 6) + (tk0 >> 6)] = S2f;
-      if (f2) row_pass(a, ram, NM_BMR, S2f, 1.0f, pk2(zh2, zh2), pk2(zl2, zl2));
-      else row_pass(a, ram, PM_SLOW, S2f, ieee_rcp(S2f), 0ull, 0ull);
+      if (f2) row_fast(a, ram, A2, ZH2, ZL2);
+      else row_slow(a, ram, S2f, ieee_rcp(S2f));
     }
     // ----------------------------------------------------------- columnwise
     {
-      float S[2] = {1.0f, 1.0f}, R[2] = {1.0f, 1.0f};
-      int mode = NM_NONE;
-      uint64_t P = 0ull, Q = 0ull;
+      uint32_t A0 = unit_amax<UE5M3>(), A1 = A0;  // the two columns' outer amax bits
+      uint64_t ZH = 0ull, ZL = 0ull;
+      float S[2] = {1.0f, 1.0f};
+      bool fast = true;
       if (LOF == LO_UNIFORM) {
+        A0 = A1 = A_u;
+        ZH = ZH_u;
+        ZL = ZL_u;
         S[0] = S[1] = S_u;
-        R[0] = R[1] = R_u;
-        if (um == NM_BMR) {
-          mode = NM_BMR;
-          P = pk2(zh_u, zh_u);
-          Q = pk2(zl_u, zl_u);
-        } else {
-          mode = mark_ok(cam, S_u, R_u) ? NM_MARK : PM_SLOW;
-          P = pk2(S_u, S_u);
-          Q = pk2(-R_u, -R_u);
-        }
+        fast = u_fast;
       } else if (LOF == LO_2D) {
+        A0 = A1 = A2;
+        ZH = ZH2;
+        ZL = ZL2;
         S[0] = S[1] = S2f;
-        if (!f2) R[0] = R[1] = ieee_rcp(S2f);  // the general steps take 1 / S
-        mode = f2 ? NM_BMR : PM_SLOW;
-        P = pk2(zh2, zh2);
-        Q = pk2(zl2, zl2);
+        fast = f2;
       } else if (LOF == LO_1D) {  // the columns' 64-row maxima over the 4 warps of this half
         const uint32_t* rq = red + (warp >> 2) * 128 + lane;
         const uint32_t g = bf16x2_amax(bf16x2_amax(rq[0], rq[32]), bf16x2_amax(rq[64], rq[96])) & 0x7FFF7FFFu;
-        const uint32_t g0 = g << 16, g1 = g & 0xFFFF0000u;
-        float Sv0, Sv1;
-        upk2(bmr2(pk2(bitsf(g0), bitsf(g1)), pk2(denh, denh), pk2(denl, denl)), Sv0, Sv1);
-        S[0] = Sv0;  // exact for g >= 2^-90
-        S[1] = Sv1;
-        if (__all_sync(0xFFFFFFFFu, umin(g0, g1) >= kTiny && umax(fbits(S[0]), fbits(S[1])) < 0x6C800000u)) {
+        A0 = g << 16;
+        A1 = g & 0xFFFF0000u;
+        fast = __all_sync(0xFFFFFFFFu, table_ok<UE5M3>(A0) && table_ok<UE5M3>(A1));
+        if (fast) {
+          upk2(bmr2(pk2(bitsf(A0), bitsf(A1)), pk2(denh, denh), pk2(denl, denl)), S[0], S[1]);  // exact
           float zh0, zl0, zh1, zl1;
-          zsplit(g0, S[0], ztab, zh0, zl0);
-          zsplit(g1, S[1], ztab, zh1, zl1);
-          mode = NM_BMR;
-          P = pk2(zh0, zh1);
-          Q = pk2(zl0, zl1);
+          outer_rcp(ptb, A0, zh0, zl0);
+          outer_rcp(ptb, A1, zh1, zl1);
+          ZH = pk2(zh0, zh1);
+          ZL = pk2(zl0, zl1);
         } else {
-          mode = PM_SLOW;
-          S[0] = outer_scale<UE5M3>(bitsf(g0));
-          S[1] = outer_scale<UE5M3>(bitsf(g1));
-          R[0] = ieee_rcp(S[0]);
-          R[1] = ieee_rcp(S[1]);
+          S[0] = outer_scale<UE5M3>(bitsf(A0));
+          S[1] = outer_scale<UE5M3>(bitsf(A1));
         }
         if ((warp & 3) == 0) {
           const int64_t M64 = j.M >> 6;
@@ -454,28 +542,21 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
         }
       }
       uint32_t c[4], sc;
-      if (mode == NM_BMR || mode == NM_NONE) {
-        float4 T0, T1;
-        if (LOF == LO_NONE) {
-          sc = scales2<UE5M3, NM_NONE>(tab, cam, P, Q, T0, T1);
-          col_codes16<NM_NONE>(wv, P, Q, T0, T1, c);
-        } else {
-          sc = scales2<UE5M3, NM_BMR>(tab, cam, P, Q, T0, T1);
-          col_codes16<NM_BMR>(wv, P, Q, T0, T1, c);
-        }
-      } else if (LOF == LO_UNIFORM && mode == NM_MARK) {
-        float4 T0, T1;
-        sc = scales2<UE5M3, NM_MARK>(tab, cam, P, Q, T0, T1);
-        col_codes16<NM_MARK>(wv, P, Q, T0, T1, c);
+      if (fast) {
+        sc = codes2<UE5M3, OUTER>(cam, ZH, ZL);
+        float c10, c20, c11, c21;
+        mults(sc & 0xFFu, A0, c10, c20);
+        mults(sc >> 8, A1, c11, c21);
+        col_codes16(wv, pk2(c10, c11), pk2(c20, c21), c);
       } else {
-        const float am0 = bitsf(cam << 16), am1 = bitsf(cam & 0xFFFF0000u);
+        sc = 0;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           float u[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) u[i] = k ? bf16hi(wv[i]) : bf16lo(wv[i]);
-          const uint32_t s1 = slow_block<UE5M3, false>(tab, u, k ? am1 : am0, S[k], R[k], !OUTER, j.srk, c[2 * k], c[2 * k + 1]);
-          sc = k ? (sc | (s1 << 8)) : s1;
+          const float am = bitsf(k ? (cam & 0xFFFF0000u) : (cam << 16));
+          sc |= slow_block<UE5M3>(u, am, S[k], ieee_rcp(S[k]), !OUTER, j.srk, c[2 * k], c[2 * k + 1]) << (8 * k);
         }
       }
       // stage: codes of column 2 lane + k, rows 16 warp .. + 15 go to row
@@ -496,6 +577,12 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
     pk0 = tk0;
     prev_par = par;
     have_prev = true;
+  };
+  while (cur.valid()) {
+    tile(std::integral_constant<int, 0>{});
+    if (!cur.valid()) break;
+    tile(std::integral_constant<int, 1>{});
+    phase ^= 1u;
   }
   // the last tile's columnwise codes and scales
   __syncthreads();
@@ -558,7 +645,7 @@ bool launch_ctl(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
     return false;
   int lof;
   if (j.s_src == S_ONE) lof = LO_NONE;
-  else if (j.mode == 1) lof = LO_UNIFORM;  // tensorwise: from the workspace amax or a given scale
+  else if (j.mode == 1 && j.s_src == S_TENSORWISE_WS) lof = LO_UNIFORM;  // tensorwise, from the workspace amax
   else if (j.s_src == S_IN_TILE && j.ob == 64) lof = j.outer_2d ? LO_2D : LO_1D;
   else return false;
   if (getenv_flag("FP4Q_NO_CTL_KERNEL")) return false;
