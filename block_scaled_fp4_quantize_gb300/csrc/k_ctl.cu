@@ -30,9 +30,10 @@
 // RN(RN(u / S) / s) for every bf16 u (checked by enumeration): two packed
 // multiplies per pair of values.  The inner scale itself, a = RN(am / S) and
 // v = RN(a / 6), comes from the known-divisor method (exact for bf16
-// dividends), its E4M3 code from the hardware conversion.  The table rows are
-// kept in shared memory with the exponent of S folded in less the bits of A,
-// so a block's multipliers are two table loads and two integer adds.  A warp
+// dividends), its E4M3 code from the hardware conversion.  The table rows sit
+// in shared memory with the exponent of S folded in (one bulk copy of a
+// precomputed image per CTA), so a block's multipliers are two table loads
+// and two integer adds.  A warp
 // whose outer amax lies outside [2^-90, 2^101) (2^109 for UE5M3 scales),
 // where the scaled entries stay normal, takes the general per-block steps
 // with div.rn.
@@ -61,12 +62,16 @@ struct LL {
   static constexpr int pt = 2 * LRAW + 11264;  // 10 rows x 128 x (u32, u32), rows 1024 bytes apart
                                                // (no outer scale: 256 x (c1, c2) by scale code)
   static constexpr int ctab = pt + 10240;      // 256 x u32: scale code -> row and exponent of 1 / s
-  static constexpr int bars = ctab + 1024;     // 2 mbarriers
-  static constexpr int total = bars + 16 + 1024;  // + alignment slack
+  static constexpr int bars = ctab + 1024;     // 3 mbarriers: two input slots, the tables
+  static constexpr int total = bars + 32 + 1024;  // + alignment slack
 };
 // rows of the shared table besides the 8 pair rows: s = 0, and the split
 // reciprocal (zh, zl) of S
 constexpr uint32_t PT_ZERO = 8, PT_RCP = 9;
+// bytes of the kCtlTab image the two forms copy: the rows and the code table
+// (outer scales), or the table of the form without outer scale
+constexpr uint32_t kImgOuter = (10 * 128 * 2 + 256) * 4, kImgUnit = 256 * 2 * 4;
+static_assert(kImgOuter + kImgUnit == kCtlTabWords * 4, "image layout");
 
 // Outer-scale form of a launch
 enum LO : int { LO_NONE = 0, LO_UNIFORM = 1, LO_1D = 2, LO_2D = 3 };
@@ -83,61 +88,6 @@ __device__ __forceinline__ constexpr uint32_t unit_amax() { return UE5M3 ? 0x492
 template <bool UE5M3>
 __device__ __forceinline__ bool table_ok(uint32_t A) {
   return A - kTiny < (UE5M3 ? 0x76000000u : 0x72000000u) - kTiny;
-}
-
-// The scale code's table row and exponent: s = (1 + row / 8) 2^e_s, or row
-// PT_ZERO for s = 0.
-template <bool UE5M3>
-__device__ __forceinline__ uint32_t code_row(uint32_t code, int& es) {
-  const uint32_t ex = code >> 3, m3 = code & 7u;
-  const int bias = UE5M3 ? 15 : 7;
-  if (ex) {
-    es = (int)ex - bias;
-    return m3;
-  }
-  es = 0;
-  if (!m3) return PT_ZERO;
-  const int p = 31 - __clz((int)m3);  // subnormal s = m3 2^(-2 - bias)
-  es = p - 2 - bias;
-  return (m3 << (3 - p)) & 7u;
-}
-
-// Fill the shared tables of the outer-scale forms from kPairTab: entry m of
-// each row with c1 (row PT_RCP: zh and zl) plus the exponent offset of S for
-// an amax of mantissa m, plus m << 16, so that c1 - A is c1 / 2^e_S.  S =
-// RN(A / (21 2^(K - 5))) = sigma_m 2^(e_A - K + c), c = 1 when (128 + m) / 21
-// >= 8, i.e. m >= 40.  ctab[code] = (row << 10) | ((-e_s) << 23).
-template <bool UE5M3>
-__device__ __forceinline__ void build_tables(unsigned char* ptb, uint32_t* ctab, int t) {
-  constexpr uint32_t K = UE5M3 ? 20u : 12u;
-  const uint4* src = reinterpret_cast<const uint4*>(&kPairTab[0][0][0]);
-  uint4* dst = reinterpret_cast<uint4*>(ptb);
-  for (int i = t; i < 10 * 64; i += LT) {  // two entries per 16 bytes
-    const uint32_t row = (uint32_t)i >> 6, m = ((uint32_t)i & 63u) * 2;
-    uint4 e = src[i];
-    const uint32_t o0 = ((127u + K - (m >= 40 ? 1u : 0u)) << 23) + (m << 16);
-    const uint32_t o1 = ((127u + K - (m + 1 >= 40 ? 1u : 0u)) << 23) + ((m + 1) << 16);
-    e.x += o0;
-    e.z += o1;
-    if (row == PT_RCP) {
-      e.y += o0;
-      e.w += o1;
-    }
-    dst[i] = e;
-  }
-  int es;
-  const uint32_t row = code_row<UE5M3>((uint32_t)t, es);
-  ctab[t] = (row << 10) | ((uint32_t)(-es) << 23);
-}
-
-// The table of the form without outer scale (S = 1, sigma = 1: m = 40):
-// ntab[code] = (c1, c2 / 2^e_s), c2 = 0 for s = 0.
-template <bool UE5M3>
-__device__ __forceinline__ void build_unit_table(uint2* ntab, int t) {
-  int es;
-  const uint32_t row = code_row<UE5M3>((uint32_t)t, es);
-  const uint32_t c1 = kPairTab[row][40][0], c2 = kPairTab[row][40][1];
-  ntab[t] = make_uint2(c1, row == PT_ZERO ? 0u : c2 + ((uint32_t)(-es) << 23));
 }
 
 // byte offset of the amax's mantissa in a table row
@@ -167,6 +117,14 @@ __device__ __forceinline__ void lds_col(uint32_t ca, uint32_t (&wv)[16]) {
   const uint32_t a = ca ^ ((uint32_t)c << 4);
   asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(wv[c]) : "r"(a), "n"(OFF + c * 128) : "memory");
   asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(wv[c + 8]) : "r"(a), "n"(OFF + c * 128 + 1024) : "memory");
+}
+
+// One bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) into shared memory, completion on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void issue_tile(const CUtensorMap* map, const TilePos& p, unsigned char* raw, uint64_t* bar) {
@@ -282,7 +240,6 @@ template <bool UE5M3, int LOF>
 __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                                         const __grid_constant__ CUtensorMap cmap) {
   constexpr bool OUTER = LOF != LO_NONE;
-  pdl_wait_then_release();
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -295,16 +252,21 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
   if (t == 0) {
     mbar_init(&bars[0]);
     mbar_init(&bars[1]);
+    mbar_init(&bars[2]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the tables are constant data: their copy may start before the
+    // previous grid on the stream has finished
+    const uint32_t* img = kCtlTab[UE5M3 ? 1 : 0] + (OUTER ? 0 : kImgOuter / 4);
+    mbar_expect_tx(&bars[2], OUTER ? kImgOuter : kImgUnit);
+    bulk_load(smem + LL::pt, img, OUTER ? kImgOuter : kImgUnit, &bars[2]);
   }
+  pdl_wait_then_release();
   __syncthreads();
   if (t == 0) {  // the first two tiles; later tiles take a slot once its reads are past a barrier
     if (cur.valid()) issue_tile(&tmap, cur.pos<LM>(), smem + LL::raw(0), &bars[0]);
     if (cur.idx + (int)gridDim.x < cur.ntiles)
       issue_tile(&tmap, cur.pos_of<LM>(cur.idx + (int)gridDim.x), smem + LL::raw(1), &bars[1]);
   }
-  if (OUTER) build_tables<UE5M3>(smem + LL::pt, reinterpret_cast<uint32_t*>(smem + LL::ctab), t);
-  else build_unit_table<UE5M3>(reinterpret_cast<uint2*>(smem + LL::pt), t);
   const float denh = bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), denl = bitsf(UE5M3 ? kDenLoU5 : kDenLoE4);
 
   // rowwise: thread t owns row t / 2, columns 32 (t mod 2) .. + 31 (two
@@ -315,7 +277,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
   for (int q = 0; q < 4; ++q) roff[q] = (uint32_t)(rr * 128 + (((4 * rh + q) ^ (rr & 7)) << 4));
   // columnwise: warp w owns rows 16 w .. + 15, lane l columns 2 l, 2 l + 1
   const uint32_t ca = smem_u32(smem) + (uint32_t)(warp * 2048 + (lane & 3) * 4 + ((lane >> 2) << 4));
-  __syncthreads();
+  if (!mbar_wait(&bars[2], 0u, 1u << 22)) atomicExch(&g_ctl_timeout, 1u);
 
   // one scale for the whole tensor, from the tensorwise amax in the
   // workspace (a bf16 value: the table path when in range)

@@ -29,6 +29,15 @@ the known-divisor method RN(u zh + RN(u zl)) gives RN(u / sigma) for bf16 u
 (the block maxima); for sigma = 1 (zl = 0) row 9 holds zl = 2^-37 zh, which
 changes no quotient that is normal (it stays below half an ulp).
 
+The kernels copy a ready-made shared-memory image per scale format (kCtlTab,
+one bulk copy): the ten rows with the exponent of S folded in (entry m of a
+row gets ((127 + K - c) << 23) + (m << 16) added to c1, and to zh and zl:
+S = sigma_m 2^(e_A - K + c) with c = 1 for m >= 40, K = 12 for E4M3 and 20
+for UE5M3 scales; subtracting the bits of a bf16 amax A then gives the
+multiplier for that S), the scale-code table (code -> row << 10 and the
+negated exponent of s << 23), and the table of the form without an outer
+scale (code -> c1, c2 / s of sigma = 1).
+
 The table is a build input, committed beside the sources; run this script
 to regenerate it (`python -m block_scaled_fp4_quantize_gb300.gen_pairtab`).
 tests/test_pairtab.py checks the committed table the same way.
@@ -143,6 +152,42 @@ def table():
     return t
 
 
+def code_row(code, ue5m3):
+    """(row, exponent) of an inner-scale code: s = (1 + row / 8) 2^e, row 8
+    for s = 0."""
+    ex, m3 = code >> 3, code & 7
+    bias = 15 if ue5m3 else 7
+    if ex:
+        return m3, ex - bias
+    if not m3:
+        return 8, 0
+    p = m3.bit_length() - 1  # subnormal s = m3 2^(-2 - bias)
+    return (m3 << (3 - p)) & 7, p - 2 - bias
+
+
+WORDS = 10 * 128 * 2 + 256 + 256 * 2  # per format: pair rows, code table, unit table
+
+
+def ctl_image(t, ue5m3):
+    """Shared-memory image of the whole-tile kernel for one scale format."""
+    K = 20 if ue5m3 else 12
+    w = []
+    for row in range(10):
+        for m in range(128):
+            off = (((127 + K - (1 if m >= 40 else 0)) << 23) + (m << 16)) & 0xFFFFFFFF
+            c1, c2 = int(t[row, m, 0]), int(t[row, m, 1])
+            w += [(c1 + off) & 0xFFFFFFFF, ((c2 + off) & 0xFFFFFFFF) if row == 9 else c2]
+    for code in range(256):
+        row, e = code_row(code, ue5m3)
+        w.append(((row << 10) | ((-e) << 23)) & 0xFFFFFFFF)
+    for code in range(256):
+        row, e = code_row(code, ue5m3)
+        c1, c2 = int(t[row, 40, 0]), int(t[row, 40, 1])
+        w += [c1, 0 if row == 8 else (c2 + ((-e) << 23)) & 0xFFFFFFFF]
+    assert len(w) == WORDS
+    return w
+
+
 HEADER = """// fp4q_pairtab.cuh -- written by gen_pairtab.py; do not edit.
 //
 // kPairTab[j][m] = {c1, c2} (binary32 bits) for inner-scale significand
@@ -151,6 +196,12 @@ HEADER = """// fp4q_pairtab.cuh -- written by gen_pairtab.py; do not edit.
 // that of RN(RN(u / sigma_m) / (1 + j / 8)) (enumerated by the generator and
 // by tests/test_pairtab.py).  Row 8: {1, 0} (a zero inner scale).  Row 9:
 // {zh, zl}, the split reciprocal of sigma_m (zl = 2^-37 zh for sigma = 1).
+//
+// kCtlTab[f] (f = 0: E4M3 scales, 1: UE5M3) is the shared-memory image of the
+// whole-tile kernel: the ten rows with the exponent of S folded in (entry m
+// gets ((127 + K - c) << 23) + (m << 16) added to c1, and to zh and zl; c = 1
+// for m >= 40, K = 12 / 20), then 256 words code -> (row << 10) | ((-e_s) <<
+// 23), then 256 pairs code -> (c1, c2 / s) of sigma = 1.
 #pragma once
 #include <cstdint>
 
@@ -158,6 +209,8 @@ namespace fp4q {
 
 __device__ const uint32_t __align__(16) kPairTab[10][128][2] = {
 """
+
+CTL_WORDS = "constexpr int kCtlTabWords = %d;\n\n" % WORDS
 
 
 def write(path):
@@ -167,6 +220,15 @@ def write(path):
         lines.append("    {  // %s\n" % ("j = %d" % j if j < 8 else ("zero inner scale" if j == 8 else "split reciprocal of sigma")))
         for m0 in range(0, 128, 4):
             lines.append("        " + " ".join("{0x%08Xu, 0x%08Xu}," % (t[j, m, 0], t[j, m, 1]) for m in range(m0, m0 + 4)) + "\n")
+        lines.append("    },\n")
+    lines.append("};\n\n")
+    lines.append(CTL_WORDS)
+    lines.append("__device__ const uint32_t __align__(16) kCtlTab[2][kCtlTabWords] = {\n")
+    for f in range(2):
+        img = ctl_image(t, f == 1)
+        lines.append("    {  // %s scales\n" % ("UE5M3" if f else "E4M3"))
+        for i in range(0, len(img), 8):
+            lines.append("        " + " ".join("0x%08Xu," % v for v in img[i:i + 8]) + "\n")
         lines.append("    },\n")
     lines.append("};\n\n}  // namespace fp4q\n")
     with open(path, "w") as f:

@@ -14,6 +14,7 @@ import re
 from fractions import Fraction
 
 import numpy as np
+import pytest
 import oracle
 
 F32 = np.float32
@@ -21,12 +22,22 @@ HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
                    "fp4q_pairtab.cuh")
 
 
-def load_table():
+def _hex_between(start, end):
     txt = open(HDR).read()
-    body = txt[txt.index("kPairTab"):]
-    vals = [int(v, 16) for v in re.findall(r"0x([0-9A-F]{8})u", body)]
+    body = txt[txt.index(start):txt.index(end) if end else len(txt)]
+    return [int(v, 16) for v in re.findall(r"0x([0-9A-F]{8})u", body)]
+
+
+def load_table():
+    vals = _hex_between("kPairTab[10]", "kCtlTabWords")
     assert len(vals) == 10 * 128 * 2
     return np.array(vals, dtype=np.uint32).reshape(10, 128, 2)
+
+
+def load_images():
+    vals = _hex_between("kCtlTab[2]", None)
+    assert len(vals) == 2 * 3328
+    return np.array(vals, dtype=np.uint32).reshape(2, 3328)
 
 
 def e2m1_mag(t):
@@ -138,3 +149,52 @@ def test_rows_of_zero_scale_and_split_reciprocal():
             for k in range(128, 256):   # the known-divisor method: RN(u / sigma) for bf16 u
                 u = Fraction(k, 128)
                 assert _r24(u * zh + _r24(u * zl)) == _r24(u / s), (m, k)
+
+
+def _f(b):
+    return float(np.array([b & 0xFFFFFFFF], dtype=np.uint32).view(F32)[0])
+
+
+def _b(x):
+    return int(np.array([x], dtype=F32).view(np.uint32)[0])
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
+def test_kernel_image_folds_the_outer_exponent(fmt):
+    # c1 of the image less the bits of a bf16 amax A is c1 / 2^e_S, S = RN(A / (scale_max * 6))
+    f = 1 if fmt == "ue5m3" else 0
+    raw, img = load_table(), load_images()[f]
+    rows = img[:2560].reshape(10, 128, 2)
+    denom = F32(688128 if f else 2688)
+    for m in range(0, 128, 3):
+        for eA in (-80, -7, 0, 11, 40, 90):
+            A = F32((128 + m) / 128.0 * 2.0 ** eA)
+            S = F32(A) / denom
+            eS = int(np.floor(np.log2(np.float64(S))))
+            for row in (0, 3, 6, 7, 8, 9):
+                got = _f(int(rows[row, m, 0]) - _b(A))
+                assert got == _f(int(raw[row, m, 0])) * 2.0 ** -eS, (fmt, m, eA, row)
+            zl = _f(int(rows[9, m, 1]) - _b(A))
+            assert zl == _f(int(raw[9, m, 1])) * 2.0 ** -eS
+            for row in range(9):
+                assert rows[row, m, 1] == raw[row, m, 1]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
+def test_kernel_image_code_tables(fmt):
+    f = 1 if fmt == "ue5m3" else 0
+    raw, img = load_table(), load_images()[f]
+    ctab, ntab = img[2560:2816], img[2816:].reshape(256, 2)
+    for code in range(256):
+        s = oracle.scale_decode(fmt, code)
+        if not np.isfinite(s):
+            continue
+        w = int(ctab[code])
+        row, e = (w & 0xFFFF) >> 10, -((w >> 23) - (512 if w >> 31 else 0))
+        assert w & 0x7F03FF == 0
+        if s == 0:
+            assert row == 8 and ntab[code, 1] == 0
+        else:
+            assert row < 8 and s == (1 + row / 8) * 2.0 ** e, (fmt, code)
+            assert _f(int(ntab[code, 1])) == _f(int(raw[row, 40, 1])) * 2.0 ** -e
+        assert ntab[code, 0] == raw[row, 40, 0]
