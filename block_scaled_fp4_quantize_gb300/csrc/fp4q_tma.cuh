@@ -133,6 +133,12 @@ __device__ __forceinline__ void tma_store3(const CUtensorMap* map, const void* s
                ::"l"(map), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// One 2-D tensor copy of a box from shared memory to global memory.
+__device__ __forceinline__ void tma_store2(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(map), "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Every store group issued by this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

@@ -53,21 +53,35 @@ constexpr int LM = 128, LK = 64;  // tile
 constexpr int LRAW = LM * LK * 2; // bytes of one raw bf16 tile
 static_assert(LT == 256, "one thread per scale code builds the code tables");
 
-// Shared memory (offsets from the 1024-byte aligned base)
-struct LL {
-  __host__ __device__ static constexpr int raw(int s) { return s * LRAW; }                       // 2 slots
-  __host__ __device__ static constexpr int ccs(int s) { return 2 * LRAW + s * 4096; }            // col codes, [64][64] swizzled
-  __host__ __device__ static constexpr int sst(int s) { return 2 * LRAW + 8192 + s * 512; }      // col scales [64][8]
-  __host__ __device__ static constexpr int red(int s) { return 2 * LRAW + 9216 + s * 1024; }     // [8 warps][32 lanes] u32
-  static constexpr int pt = 2 * LRAW + 11264;  // 10 rows x 128 x (u32, u32), rows 1024 bytes apart
-                                               // (no outer scale: 256 x (c1, c2) by scale code)
-  static constexpr int ctab = pt + 10240;      // 256 x u32: scale code -> row and exponent of 1 / s
-  static constexpr int bars = ctab + 1024;     // 3 mbarriers: two input slots, the tables
+// Shared memory (offsets from the 1024-byte aligned base).  Buffers that
+// tensor copies read or write start on 1024-byte boundaries (the copies need
+// 128, the swizzled loads 1024).  RT: the form stages its rowwise codes too.
+template <bool RT>
+struct LLT {
+  __host__ __device__ static constexpr int raw(int s) { return s * LRAW; }                   // 2 input slots
+  __host__ __device__ static constexpr int ccs(int s) { return 2 * LRAW + s * 4096; }        // col codes, [64][64] swizzled
+  __host__ __device__ static constexpr int rcs(int s) { return 2 * LRAW + 8192 + s * 4096; } // row codes [128][32] (RT)
+  static constexpr int rt_bytes = RT ? 8192 : 0;
+  __host__ __device__ static constexpr int sst(int s) { return 2 * LRAW + 8192 + rt_bytes + s * 512; }  // col scales [64][8]
+  __host__ __device__ static constexpr int red(int s) { return sst(2) + s * 1024; }  // [8 warps][32 lanes] u32
+  static constexpr int pt = red(2);      // 10 rows x 128 x (u32, u32), rows 1024 bytes apart
+                                         // (no outer scale: 256 x (c1, c2) by scale code)
+  static constexpr int ctab = pt + 10240;  // 256 x u32: scale code -> row and exponent of 1 / s
+  static constexpr int bars = ctab + 1024;  // 3 mbarriers: two input slots, the tables
   static constexpr int total = bars + 32 + 1024;  // + alignment slack
 };
-// rows of the shared table besides the 8 pair rows: s = 0, and the split
-// reciprocal (zh, zl) of S
-constexpr uint32_t PT_ZERO = 8, PT_RCP = 9;
+static_assert(LLT<true>::rcs(0) % 1024 == 0 && LLT<true>::rcs(1) % 1024 == 0 && LLT<true>::ccs(1) % 1024 == 0,
+              "tensor-copy staging alignment");
+static_assert(LLT<true>::pt % 16 == 0 && LLT<false>::pt % 16 == 0 && LLT<true>::bars % 8 == 0 && LLT<false>::bars % 8 == 0,
+              "bulk-copy and mbarrier alignment");
+// Forms that stage the rowwise codes in shared memory and store them with
+// tensor copies (their row pass runs after the barrier; three CTAs per SM
+// leave the room).
+__host__ __device__ constexpr bool row_tma(int lof) { return lof >= 2; }
+
+// row of the shared table holding the split reciprocal (zh, zl) of S (rows
+// 0-7: the pairs by inner significand; row 8: a zero inner scale)
+constexpr uint32_t PT_RCP = 9;
 // bytes of the kCtlTab image the two forms copy: the rows and the code table
 // (outer scales), or the table of the form without outer scale
 constexpr uint32_t kImgOuter = (10 * 128 * 2 + 256) * 4, kImgUnit = 256 * 2 * 4;
@@ -237,9 +251,12 @@ __device__ __forceinline__ uint32_t slow_block(const float (&v)[16], float am, f
 }
 
 template <bool UE5M3, int LOF>
-__global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
-                                                                        const __grid_constant__ CUtensorMap cmap) {
+__global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
+                                                                       const __grid_constant__ CUtensorMap cmap,
+                                                                       const __grid_constant__ CUtensorMap rmap) {
   constexpr bool OUTER = LOF != LO_NONE;
+  constexpr bool RT = row_tma(LOF);
+  using LL = LLT<RT>;
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -331,7 +348,8 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
 
     auto row_store = [&](const uint32_t (&c)[4], uint32_t sc) {
       const int64_t e = row * j.K + tk0 + 32 * rh;  // flat index of the thread's first element
-      *reinterpret_cast<uint4*>(j.row_codes + (e >> 1)) = make_uint4(c[0], c[1], c[2], c[3]);
+      if (RT) *reinterpret_cast<uint4*>(smem + LL::rcs(par) + rr * 32 + rh * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+      else *reinterpret_cast<uint4*>(j.row_codes + (e >> 1)) = make_uint4(c[0], c[1], c[2], c[3]);
       *reinterpret_cast<uint16_t*>(j.row_scales + (e >> 4)) = (uint16_t)sc;
     };
     // rowwise scales, codes and stores of the thread's two blocks, table path
@@ -388,7 +406,10 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
     } else if (LOF == LO_UNIFORM) {
       if (u_fast) row_fast(a, ram, A_u, ZH_u, ZL_u);
       else row_slow(a, ram, S_u, R_u);
-    } else {  // 1 x 64: the row's 64 columns are this thread's two blocks and its partner's
+    }
+    // 1 x 64 (after the barrier): the row's 64 columns are this thread's two
+    // blocks and its partner's
+    auto row_1d = [&]() {
       uint32_t g = umax(ram & 0xFFFFu, ram >> 16);
       g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1)) << 16;
       float* so = j.row_outer + row * (j.K >> 6) + (tk0 >> 6);
@@ -402,7 +423,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
         if (rh == 0) *so = S1;
         row_slow(a, ram, S1, ieee_rcp(S1));
       }
-    }
+    };
     // rows 16 warp .. + 15, columns 2 lane (low halves) and 2 lane + 1
     // (high): row i's word sits in 16-byte chunk cunit ^ (i mod 8), which is
     // the per-lane base address with bits 4..6 XORed by i mod 8
@@ -430,6 +451,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
       if (after < cur.ntiles) issue_tile(&tmap, cur.pos_of<LM>(after), smem + LL::raw(par), &bars[par]);
       if (have_prev) {
         tma_store3(&cmap, smem + LL::ccs(par ^ 1), pm0 >> 1, pk0, pg);
+        if (RT) tma_store2(&rmap, smem + LL::rcs(par ^ 1), pk0 >> 1, (int)(pg * j.M + pm0));
         bulk_commit();
       }
     }
@@ -439,6 +461,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
     }
 
     // ---------------------------------------- after the barrier: registers and staging only
+    if (LOF == LO_1D) row_1d();
     uint32_t A2 = 0;  // the 64 x 64 block's amax (2-D): both orientations
     float S2f = 1.0f;
     uint64_t ZH2 = 0ull, ZL2 = 0ull;
@@ -551,6 +574,7 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
   if (have_prev) {
     if (t == 0) {
       tma_store3(&cmap, smem + LL::ccs(prev_par), pm0 >> 1, pk0, pg);
+      if (RT) tma_store2(&rmap, smem + LL::rcs(prev_par), pk0 >> 1, (int)(pg * j.M + pm0));
       bulk_commit();
     }
     if (t < 64) {
@@ -562,7 +586,8 @@ __global__ void __launch_bounds__(LT, LOF == LO_2D ? 3 : 4) ctl_kernel(const Qua
 }
 
 template <bool UE5M3, int LOF>
-cudaError_t launch_ctl_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, cudaStream_t st) {
+cudaError_t launch_ctl_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, const CUtensorMap& rmap,
+                         cudaStream_t st) {
   auto kern = ctl_kernel<UE5M3, LOF>;
   static int per_sm_cache[128] = {0};
   int dev = 0;
@@ -570,28 +595,46 @@ cudaError_t launch_ctl_t(const QuantJob& j, const CUtensorMap& map, const CUtens
   if (dev < 0 || dev >= 128) dev = 0;
   int& per_sm = per_sm_cache[dev];
   if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LL::total);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LLT<row_tma(LOF)>::total);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, LT, LL::total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, LT, LLT<row_tma(LOF)>::total);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
   }
   const int64_t tiles = j.G * (j.M / LM) * (j.K / LK);
   const int64_t cap = (int64_t)num_sms() * per_sm;
-  return launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(LT), (size_t)LL::total, st, j, map, cmap);
+  return launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(LT), (size_t)LLT<row_tma(LOF)>::total, st, j, map,
+                    cmap, rmap);
 }
 
 template <bool UE5M3>
-cudaError_t launch_ctl_f(const QuantJob& j, int lof, const CUtensorMap& map, const CUtensorMap& cmap, cudaStream_t st) {
+cudaError_t launch_ctl_f(const QuantJob& j, int lof, const CUtensorMap& map, const CUtensorMap& cmap,
+                         const CUtensorMap& rmap, cudaStream_t st) {
   switch (lof) {
-    case LO_NONE: return launch_ctl_t<UE5M3, LO_NONE>(j, map, cmap, st);
-    case LO_UNIFORM: return launch_ctl_t<UE5M3, LO_UNIFORM>(j, map, cmap, st);
-    case LO_1D: return launch_ctl_t<UE5M3, LO_1D>(j, map, cmap, st);
-    default: return launch_ctl_t<UE5M3, LO_2D>(j, map, cmap, st);
+    case LO_NONE: return launch_ctl_t<UE5M3, LO_NONE>(j, map, cmap, rmap, st);
+    case LO_UNIFORM: return launch_ctl_t<UE5M3, LO_UNIFORM>(j, map, cmap, rmap, st);
+    case LO_1D: return launch_ctl_t<UE5M3, LO_1D>(j, map, cmap, rmap, st);
+    default: return launch_ctl_t<UE5M3, LO_2D>(j, map, cmap, rmap, st);
   }
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0u; }
+
+// Tensor map of the rowwise codes as a [G M][K / 2] byte matrix for the tile
+// store (box: 32 bytes x 128 rows, no swizzle: the staging holds row r at
+// byte 32 r).  Needs rows of a multiple of 16 bytes (K a multiple of 32), a
+// 16-byte aligned base and G M below 2^31 (a 32-bit coordinate).
+bool make_row_map(const QuantJob& j, CUtensorMap* map) {
+  if (j.K % 32 || !aligned_to(j.row_codes, 16) || j.G * j.M >= ((int64_t)1 << 31)) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(j.K / 2), (cuuint64_t)(j.G * j.M)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(j.K / 2)};
+  const cuuint32_t box[2] = {32u, (cuuint32_t)LM};
+  const cuuint32_t es[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, j.row_codes, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -611,9 +654,10 @@ bool launch_ctl(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   else if (j.s_src == S_IN_TILE && j.ob == 64) lof = j.outer_2d ? LO_2D : LO_1D;
   else return false;
   if (getenv_flag("FP4Q_NO_CTL_KERNEL")) return false;
-  CUtensorMap map, cmap;
+  CUtensorMap map, cmap, rmap = {};
   if (!make_bf16_tile_map(j, &map, LM) || !make_col_map(j, &cmap)) return false;
-  *err = j.ue5m3 ? launch_ctl_f<true>(j, lof, map, cmap, st) : launch_ctl_f<false>(j, lof, map, cmap, st);
+  if (row_tma(lof) && !make_row_map(j, &rmap)) return false;
+  *err = j.ue5m3 ? launch_ctl_f<true>(j, lof, map, cmap, rmap, st) : launch_ctl_f<false>(j, lof, map, cmap, rmap, st);
   return true;
 }
 
