@@ -62,6 +62,21 @@ struct TileIter {
   }
 };
 
+// Position in the grouped walk: group e owns the 128-row tiles
+// tprefix[e] .. tprefix[e + 1] - 1 of the walk; a cursor only moves forward
+// (a CTA's tile indices grow), so finding the group of a tile is amortized.
+struct GroupCursor {
+  int64_t e = -1;
+  uint32_t lo = 0, hi = 0;
+  __device__ __forceinline__ void seek(const uint32_t* tp, uint32_t q) {
+    while (hi <= q) {
+      ++e;
+      lo = hi;
+      hi = tp[e + 1];
+    }
+  }
+};
+
 // ---- programmatic dependent launch ----
 // A kernel launched with programmatic stream serialization may start while
 // the previous grid on the stream is still finishing: it waits for that

@@ -36,9 +36,9 @@ bool ctb_supports(const QuantJob& j) {
 
 // false: the tensor map could not be built (the caller takes another kernel)
 bool launch_ctb(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
+  if (launch_ctl(j, st, err)) return true;  // the whole-tile form (k_ctl.cu)
   if (j.ngroups > 0) return launch_ctb_grouped(j, st, err);
   if (j.col_rht) return launch_ctb_rht(j, st, err);
-  if (launch_ctl(j, st, err)) return true;  // the whole-tile form (k_ctl.cu)
   return launch_ctb_all<false, false>(j, st, err);
 }
 

@@ -122,21 +122,6 @@ __device__ __forceinline__ uint32_t quant_block(const float4* tab, const float (
   return sc;
 }
 
-// Position in the grouped walk: group e owns the 128-row tiles
-// tprefix[e] .. tprefix[e + 1] - 1 of the walk; a cursor only moves forward
-// (a CTA's tile indices grow), so finding the group of a tile is amortized.
-struct GroupCursor {
-  int64_t e = -1;
-  uint32_t lo = 0, hi = 0;
-  __device__ __forceinline__ void seek(const uint32_t* tp, uint32_t q) {
-    while (hi <= q) {
-      ++e;
-      lo = hi;
-      hi = tp[e + 1];
-    }
-  }
-};
-
 // FT, bit 0: every tile is whole along K (K a multiple of 64), so the
 // column edge checks fold away.  Bit 1: whole along M too (M a multiple of
 // 128, no groups), both orientations are written, the columnwise codes

@@ -250,11 +250,18 @@ __device__ __forceinline__ uint32_t slow_block(const float (&v)[16], float am, f
   return sc;
 }
 
-template <bool UE5M3, int LOF>
+// GR: ragged groups (rows [goff[e], goff[e + 1]) form group e, quantized as a
+// matrix of its own, every group a whole number of 64-row outer blocks): the
+// walk covers each group's 128-row tiles, the last one of a group possibly a
+// half tile of 64 rows; the columnwise outputs go to the group's own
+// transpose by vector stores (its row length differs from group to group).
+template <bool UE5M3, int LOF, bool GR>
 __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                                        const __grid_constant__ CUtensorMap cmap,
-                                                                       const __grid_constant__ CUtensorMap rmap) {
+                                                                       const __grid_constant__ CUtensorMap rmap,
+                                                                       const __grid_constant__ CUtensorMap rmap64) {
   constexpr bool OUTER = LOF != LO_NONE;
+  static_assert(!GR || row_tma(LOF), "groups: outer-block forms only");
   constexpr bool RT = row_tma(LOF);
   using LL = LLT<RT>;
   extern __shared__ __align__(16) unsigned char smem_dyn[];
@@ -264,8 +271,6 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
   const uint32_t* ctab = reinterpret_cast<const uint32_t*>(smem + LL::ctab);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LL::bars);
 
-  TileIter cur;
-  cur.init<LM>(j);
   if (t == 0) {
     mbar_init(&bars[0]);
     mbar_init(&bars[1]);
@@ -279,10 +284,24 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
   }
   pdl_wait_then_release();
   __syncthreads();
+  const uint32_t* gtp = GR ? group_tprefix(j.gws) : nullptr;
+  if (GR && j.gws->bad) {  // invalid offsets: write nothing (once the table copy has landed)
+    if (!mbar_wait(&bars[2], 0u, 1u << 22)) atomicExch(&g_ctl_timeout, 1u);
+    return;
+  }
+  TileIter cur;
+  if (GR) cur.init_n((int)(j.K / LK), (int)j.gws->mtiles, 1);
+  else cur.init<LM>(j);
+  GroupCursor gc, pc;  // the group of the processed tile (all threads), of the prefetched one (thread 0)
+  auto tile_at = [&](int i) -> TilePos {
+    if (!GR) return cur.pos_of<LM>(i);
+    const uint32_t q = (uint32_t)(i / cur.tiles_k);
+    pc.seek(gtp, q);
+    return TilePos{0, j.goff[pc.e] + LM * (int64_t)(q - pc.lo), (int64_t)(i - (int)q * cur.tiles_k) * LK};
+  };
   if (t == 0) {  // the first two tiles; later tiles take a slot once its reads are past a barrier
-    if (cur.valid()) issue_tile(&tmap, cur.pos<LM>(), smem + LL::raw(0), &bars[0]);
-    if (cur.idx + (int)gridDim.x < cur.ntiles)
-      issue_tile(&tmap, cur.pos_of<LM>(cur.idx + (int)gridDim.x), smem + LL::raw(1), &bars[1]);
+    if (cur.valid()) issue_tile(&tmap, tile_at(cur.idx), smem + LL::raw(0), &bars[0]);
+    if (cur.idx + (int)gridDim.x < cur.ntiles) issue_tile(&tmap, tile_at(cur.idx + (int)gridDim.x), smem + LL::raw(1), &bars[1]);
   }
   const float denh = bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), denl = bitsf(UE5M3 ? kDenLoU5 : kDenLoE4);
 
@@ -329,15 +348,65 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
 
   uint32_t phase = 0;
   int pg = 0, pm0 = 0, pk0 = 0;  // the previous tile
+  int64_t pgb = 0, pgm = 0, pmr = 0;  // its matrix (a group, or matrix pg): first row, rows; its row in it
+  bool phalf = false;            // it was a half tile
   int prev_par = 0;
   bool have_prev = false;
+  // The previous tile's staged outputs (parity pp): the tensor stores (t ==
+  // 0, one bulk group), and the vector stores of the grouped columnwise
+  // codes and of the column scales (8 bytes per column: 64 x 1 block rows
+  // of the tile; 4 for a half tile).
+  auto store_prev = [&](int pp) {
+    if (t == 0) {
+      if (!GR) tma_store3(&cmap, smem + LL::ccs(pp), pm0 >> 1, pk0, pg);
+      if (RT) tma_store2(phalf ? &rmap64 : &rmap, smem + LL::rcs(pp), pk0 >> 1, (int)(pg * j.M + pm0));
+      bulk_commit();
+    }
+    const int64_t cb = j.K * pgb + pmr;  // columnwise index of (k, first row): cb + k pgm (the matrix's transpose)
+    if (GR) {  // 16-byte chunk q of column c: bytes 16 q .. of its 64 (32 for a half tile)
+      const int c = t >> 2, q = t & 3;
+      if (!phalf || q < 2) {
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + LL::ccs(pp) + c * 64 + ((q ^ ((c >> 1) & 3)) << 4));
+        *reinterpret_cast<uint4*>(j.col_codes + ((cb + (pk0 + c) * pgm) >> 1) + q * 16) = v;
+      }
+    }
+    if (t < 64) {
+      const uint2 v = *reinterpret_cast<const uint2*>(smem + LL::sst(pp) + t * 8);
+      uint8_t* d = j.col_scales + ((cb + (pk0 + t) * pgm) >> 4);
+      if (!GR) {
+        *reinterpret_cast<uint2*>(d) = v;
+      } else {  // 4-byte aligned only (a group's rows / 16 is a multiple of 4)
+        reinterpret_cast<uint32_t*>(d)[0] = v.x;
+        if (!phalf) reinterpret_cast<uint32_t*>(d)[1] = v.y;
+      }
+    }
+  };
   // One tile; the walk alternates the two input slots and the two staging
   // buffers, so the loop runs two tiles per iteration with the parity a
   // compile-time constant (shared-memory offsets fold into the loads).
   auto tile = [&](auto PC) {
     constexpr int par = decltype(PC)::value;  // input slot and staging buffer
-    const int tg = cur.g, tm0 = cur.tm * LM, tk0 = cur.tk * LK;  // this tile
-    const int after = cur.idx + 2 * (int)gridDim.x;              // the tile that takes this slot next
+    const int tk0 = cur.tk * LK;
+    int tg, tm0;        // this tile: matrix, first row (of the matrix; of the [M, K] view with groups)
+    int64_t gb, gm, mr; // its matrix: first row of the [G M] view, rows; the tile's first row in it
+    bool half = false;  // the tile's last 64 rows belong to the next group
+    if (GR) {
+      gc.seek(gtp, (uint32_t)cur.tm);
+      gb = j.goff[gc.e];
+      gm = j.goff[gc.e + 1] - gb;
+      tg = 0;
+      mr = LM * (int64_t)((uint32_t)cur.tm - gc.lo);
+      tm0 = (int)(gb + mr);
+      half = gm - mr == 64;
+    } else {
+      tg = cur.g;
+      tm0 = cur.tm * LM;
+      gb = (int64_t)tg * j.M;
+      gm = j.M;
+      mr = tm0;
+    }
+    const bool rvalid = !half || rr < 64;  // this thread's row belongs to the tile's matrix
+    const int after = cur.idx + 2 * (int)gridDim.x;  // the tile that takes this slot next
     cur.next();
     const unsigned char* raw = smem + LL::raw(par);
     // a wait that runs out raises the error flag; the walk goes on (every
@@ -350,7 +419,7 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
       const int64_t e = row * j.K + tk0 + 32 * rh;  // flat index of the thread's first element
       if (RT) *reinterpret_cast<uint4*>(smem + LL::rcs(par) + rr * 32 + rh * 16) = make_uint4(c[0], c[1], c[2], c[3]);
       else *reinterpret_cast<uint4*>(j.row_codes + (e >> 1)) = make_uint4(c[0], c[1], c[2], c[3]);
-      *reinterpret_cast<uint16_t*>(j.row_scales + (e >> 4)) = (uint16_t)sc;
+      if (rvalid) *reinterpret_cast<uint16_t*>(j.row_scales + (e >> 4)) = (uint16_t)sc;
     };
     // rowwise scales, codes and stores of the thread's two blocks, table path
     // (A: the outer amax bits, ZH / ZL: the split reciprocal of S)
@@ -414,13 +483,13 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
       g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, 1)) << 16;
       float* so = j.row_outer + row * (j.K >> 6) + (tk0 >> 6);
       if (__all_sync(0xFFFFFFFFu, table_ok<UE5M3>(g))) {
-        if (rh == 0) *so = div_bmr(bitsf(g), denh, denl);  // exact for g >= 2^-90
+        if (rh == 0 && rvalid) *so = div_bmr(bitsf(g), denh, denl);  // exact for g >= 2^-90
         float zh, zl;
         outer_rcp(ptb, g, zh, zl);
         row_fast(a, ram, g, pk2(zh, zh), pk2(zl, zl));
       } else {
         const float S1 = outer_scale<UE5M3>(bitsf(g));
-        if (rh == 0) *so = S1;
+        if (rh == 0 && rvalid) *so = S1;
         row_slow(a, ram, S1, ieee_rcp(S1));
       }
     };
@@ -447,18 +516,9 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
     if (t == 0) bulk_wait_read_0();
     __syncthreads();
 
-    if (t == 0) {  // refill the slot, store the previous tile's staged column codes
-      if (after < cur.ntiles) issue_tile(&tmap, cur.pos_of<LM>(after), smem + LL::raw(par), &bars[par]);
-      if (have_prev) {
-        tma_store3(&cmap, smem + LL::ccs(par ^ 1), pm0 >> 1, pk0, pg);
-        if (RT) tma_store2(&rmap, smem + LL::rcs(par ^ 1), pk0 >> 1, (int)(pg * j.M + pm0));
-        bulk_commit();
-      }
-    }
-    if (have_prev && t < 64) {  // the previous tile's column scales: 8 bytes per column
-      const uint2 v = *reinterpret_cast<const uint2*>(smem + LL::sst(par ^ 1) + t * 8);
-      *reinterpret_cast<uint2*>(j.col_scales + ((int64_t)pg * j.K + pk0 + t) * (j.M >> 4) + (pm0 >> 4)) = v;
-    }
+    // refill the slot, store the previous tile's staged outputs
+    if (t == 0 && after < cur.ntiles) issue_tile(&tmap, tile_at(after), smem + LL::raw(par), &bars[par]);
+    if (have_prev) store_prev(par ^ 1);
 
     // ---------------------------------------- after the barrier: registers and staging only
     if (LOF == LO_1D) row_1d();
@@ -479,7 +539,7 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
       } else {
         S2f = outer_scale<UE5M3>(bitsf(A2));
       }
-      if ((warp & 3) == 0 && lane == 0)
+      if ((warp & 3) == 0 && lane == 0 && (!half || warp < 4))
         j.tile_outer[((int64_t)tg * (j.M >> 6) + (tm0 >> 6) + (warp >> 2)) * (j.K >> 6) + (tk0 >> 6)] = S2f;
       if (f2) row_fast(a, ram, A2, ZH2, ZL2);
       else row_slow(a, ram, S2f, ieee_rcp(S2f));
@@ -519,9 +579,9 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
           S[0] = outer_scale<UE5M3>(bitsf(A0));
           S[1] = outer_scale<UE5M3>(bitsf(A1));
         }
-        if ((warp & 3) == 0) {
-          const int64_t M64 = j.M >> 6;
-          float* d = j.col_outer + ((int64_t)tg * j.K + tk0 + 2 * lane) * M64 + (tm0 >> 6) + (warp >> 2);
+        if ((warp & 3) == 0 && (!half || warp < 4)) {  // the matrix's [K, rows / 64] outer scales
+          const int64_t M64 = gm >> 6;
+          float* d = j.col_outer + ((j.K * gb + mr) >> 6) + (tk0 + 2 * lane) * M64 + (warp >> 2);
           d[0] = S[0];
           d[M64] = S[1];
         }
@@ -560,6 +620,10 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
     pg = tg;
     pm0 = tm0;
     pk0 = tk0;
+    pgb = gb;
+    pgm = gm;
+    pmr = mr;
+    phalf = half;
     prev_par = par;
     have_prev = true;
   };
@@ -569,68 +633,65 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
     tile(std::integral_constant<int, 1>{});
     phase ^= 1u;
   }
-  // the last tile's columnwise codes and scales
+  // the last tile's staged outputs
   __syncthreads();
-  if (have_prev) {
-    if (t == 0) {
-      tma_store3(&cmap, smem + LL::ccs(prev_par), pm0 >> 1, pk0, pg);
-      if (RT) tma_store2(&rmap, smem + LL::rcs(prev_par), pk0 >> 1, (int)(pg * j.M + pm0));
-      bulk_commit();
-    }
-    if (t < 64) {
-      const uint2 v = *reinterpret_cast<const uint2*>(smem + LL::sst(prev_par) + t * 8);
-      *reinterpret_cast<uint2*>(j.col_scales + ((int64_t)pg * j.K + pk0 + t) * (j.M >> 4) + (pm0 >> 4)) = v;
-    }
-  }
+  if (have_prev) store_prev(prev_par);
   if (t == 0) bulk_wait_all();
 }
 
-template <bool UE5M3, int LOF>
+template <bool UE5M3, int LOF, bool GR>
 cudaError_t launch_ctl_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, const CUtensorMap& rmap,
-                         cudaStream_t st) {
-  auto kern = ctl_kernel<UE5M3, LOF>;
+                         const CUtensorMap& rmap64, cudaStream_t st) {
+  auto kern = ctl_kernel<UE5M3, LOF, GR>;
+  constexpr int smem = LLT<row_tma(LOF)>::total;
   static int per_sm_cache[128] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 128) dev = 0;
   int& per_sm = per_sm_cache[dev];
   if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LLT<row_tma(LOF)>::total);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, LT, LLT<row_tma(LOF)>::total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, LT, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
   }
-  const int64_t tiles = j.G * (j.M / LM) * (j.K / LK);
+  // grouped: the tile count lives on the device; at most ceil(M / 128) +
+  // groups 128-row tiles per 64-column strip
+  const int64_t tiles = GR ? (j.M / LM + j.ngroups) * (j.K / LK) : j.G * (j.M / LM) * (j.K / LK);
   const int64_t cap = (int64_t)num_sms() * per_sm;
-  return launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(LT), (size_t)LLT<row_tma(LOF)>::total, st, j, map,
-                    cmap, rmap);
+  return launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(LT), (size_t)smem, st, j, map, cmap, rmap,
+                    rmap64);
 }
 
 template <bool UE5M3>
 cudaError_t launch_ctl_f(const QuantJob& j, int lof, const CUtensorMap& map, const CUtensorMap& cmap,
-                         const CUtensorMap& rmap, cudaStream_t st) {
+                         const CUtensorMap& rmap, const CUtensorMap& rmap64, cudaStream_t st) {
+  if (j.ngroups > 0) {
+    return lof == LO_1D ? launch_ctl_t<UE5M3, LO_1D, true>(j, map, cmap, rmap, rmap64, st)
+                        : launch_ctl_t<UE5M3, LO_2D, true>(j, map, cmap, rmap, rmap64, st);
+  }
   switch (lof) {
-    case LO_NONE: return launch_ctl_t<UE5M3, LO_NONE>(j, map, cmap, rmap, st);
-    case LO_UNIFORM: return launch_ctl_t<UE5M3, LO_UNIFORM>(j, map, cmap, rmap, st);
-    case LO_1D: return launch_ctl_t<UE5M3, LO_1D>(j, map, cmap, rmap, st);
-    default: return launch_ctl_t<UE5M3, LO_2D>(j, map, cmap, rmap, st);
+    case LO_NONE: return launch_ctl_t<UE5M3, LO_NONE, false>(j, map, cmap, rmap, rmap64, st);
+    case LO_UNIFORM: return launch_ctl_t<UE5M3, LO_UNIFORM, false>(j, map, cmap, rmap, rmap64, st);
+    case LO_1D: return launch_ctl_t<UE5M3, LO_1D, false>(j, map, cmap, rmap, rmap64, st);
+    default: return launch_ctl_t<UE5M3, LO_2D, false>(j, map, cmap, rmap, rmap64, st);
   }
 }
 
 bool aligned_to(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0u; }
 
 // Tensor map of the rowwise codes as a [G M][K / 2] byte matrix for the tile
-// store (box: 32 bytes x 128 rows, no swizzle: the staging holds row r at
+// store (box: 32 bytes x box_m rows, no swizzle: the staging holds row r at
 // byte 32 r).  Needs rows of a multiple of 16 bytes (K a multiple of 32), a
 // 16-byte aligned base and G M below 2^31 (a 32-bit coordinate).
-bool make_row_map(const QuantJob& j, CUtensorMap* map) {
+bool make_row_map(const QuantJob& j, CUtensorMap* map, int box_m) {
   if (j.K % 32 || !aligned_to(j.row_codes, 16) || j.G * j.M >= ((int64_t)1 << 31)) return false;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)(j.K / 2), (cuuint64_t)(j.G * j.M)};
   const cuuint64_t strides[1] = {(cuuint64_t)(j.K / 2)};
-  const cuuint32_t box[2] = {32u, (cuuint32_t)LM};
+  const cuuint32_t box[2] = {32u, (cuuint32_t)box_m};
   const cuuint32_t es[2] = {1u, 1u};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, j.row_codes, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -640,24 +701,29 @@ bool make_row_map(const QuantJob& j, CUtensorMap* map) {
 
 // The whole-tile form, when the call's facts allow it (false: the caller
 // takes the general cast-transpose kernel).  FP4Q_NO_CTL_KERNEL=1 turns it
-// off (the parity tests run every kernel that can take a case).
+// off (the parity tests run every kernel that can take a case).  Ragged
+// groups take it with 1-D or 2-D outer blocks of 64 (every group then a
+// multiple of 64 rows).
 bool launch_ctl(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
-  if (!j.in_bf16 || !j.do_row || !j.do_col || j.sr || j.inner_2d || j.residual || j.qdq_orient || j.ngroups ||
-      j.col_rht || j.rsl.mma || j.csl.mma || j.M % LM || j.K % LK)
+  const bool gr = j.ngroups > 0;
+  if (!j.in_bf16 || !j.do_row || !j.do_col || j.sr || j.inner_2d || j.residual || j.qdq_orient || j.col_rht ||
+      j.rsl.mma || j.csl.mma || j.K % LK || (gr ? (j.G != 1 || j.M % 64) : j.M % LM))
     return false;
   if (!aligned_to(j.x, 16) || (j.ld * 2) % 16 || !aligned_to(j.row_codes, 16) || !aligned_to(j.row_scales, 2) ||
-      !aligned_to(j.col_codes, 16) || !aligned_to(j.col_scales, 8))
+      !aligned_to(j.col_codes, 16) || !aligned_to(j.col_scales, gr ? 4 : 8))
     return false;
   int lof;
   if (j.s_src == S_ONE) lof = LO_NONE;
   else if (j.mode == 1 && j.s_src == S_TENSORWISE_WS) lof = LO_UNIFORM;  // tensorwise, from the workspace amax
   else if (j.s_src == S_IN_TILE && j.ob == 64) lof = j.outer_2d ? LO_2D : LO_1D;
   else return false;
+  if (gr && !row_tma(lof)) return false;
   if (getenv_flag("FP4Q_NO_CTL_KERNEL")) return false;
-  CUtensorMap map, cmap, rmap = {};
-  if (!make_bf16_tile_map(j, &map, LM) || !make_col_map(j, &cmap)) return false;
-  if (row_tma(lof) && !make_row_map(j, &rmap)) return false;
-  *err = j.ue5m3 ? launch_ctl_f<true>(j, lof, map, cmap, rmap, st) : launch_ctl_f<false>(j, lof, map, cmap, rmap, st);
+  CUtensorMap map, cmap = {}, rmap = {}, rmap64 = {};
+  if (!make_bf16_tile_map(j, &map, LM) || (!gr && !make_col_map(j, &cmap))) return false;
+  if (row_tma(lof) && (!make_row_map(j, &rmap, LM) || (gr && !make_row_map(j, &rmap64, 64)))) return false;
+  *err = j.ue5m3 ? launch_ctl_f<true>(j, lof, map, cmap, rmap, rmap64, st)
+                 : launch_ctl_f<false>(j, lof, map, cmap, rmap, rmap64, st);
   return true;
 }
 

@@ -32,9 +32,22 @@ CASES = [dict(mode="none"), dict(mode="tensorwise"), dict(mode="outer_block", ou
          dict(mode="outer_block", outer_block_size=64, outer_2d=True), dict(mode="none", stochastic=True, seed=9)]
 
 
+@pytest.fixture(params=["whole", "general"])
+def kernel(request, monkeypatch):
+    """Ragged groups with 64-row outer blocks and both orientations take the
+    whole-tile kernel (half tiles at group tails); "general" forces the
+    general cast-transpose kernel for the same calls."""
+    monkeypatch.delenv("FP4Q_NO_CTL_KERNEL", raising=False)
+    if request.param == "general":
+        monkeypatch.setenv("FP4Q_NO_CTL_KERNEL", "1")
+    return request.param
+
+
 @pytest.mark.parametrize("case", CASES, ids=["none", "tensorwise", "ob64", "ob16-ue5m3", "ob64-2d", "sr"])
 @pytest.mark.parametrize("mask", [(True, False), (False, True), (True, True)], ids=["row", "col", "both"])
-def test_grouped_matches_per_group_oracle(orc, case, mask):
+def test_grouped_matches_per_group_oracle(orc, case, mask, kernel):
+    if kernel == "general" and not (mask == (True, True) and case.get("outer_block_size") == 64):
+        pytest.skip("the same kernel runs either way")
     align = 64 if case.get("outer_block_size", 0) == 64 else 16
     sizes = [0, 3 * align, 128, align, 5 * align + 128, 0, 2 * align]
     K = 320
@@ -89,6 +102,21 @@ def test_grouped_invalid_offsets_write_nothing():
     q2 = fq.quantize_grouped(x, off2, rowwise=True)
     torch.cuda.synchronize()
     assert int(q2.group_error.item()) != 0
+
+
+@pytest.mark.parametrize("outer_2d", [False, True], ids=["1d", "2d"])
+def test_grouped_invalid_offsets_write_nothing_whole_tile(outer_2d):
+    x = W.lognormal((256, 128), 73).cuda()
+    off = torch.tensor([0, 64, 160, 256], dtype=torch.int64, device="cuda")  # 96 rows: not a multiple of 64
+    kw = dict(mode="outer_block", outer_block_size=64, outer_2d=outer_2d, rowwise=True, columnwise=True)
+    q = fq.quantize_grouped(x, off, **kw)
+    for t in (q.col_codes, q.row_codes, q.col_scales, q.row_scales):
+        t.fill_(0x5A)
+    q = fq.quantize_grouped(x, off, out=q, **kw)
+    torch.cuda.synchronize()
+    assert int(q.group_error.item()) != 0
+    for t in (q.col_codes, q.row_codes, q.col_scales, q.row_scales):
+        assert bool((t == 0x5A).all())
 
 
 def test_grouped_single_group_equals_plain_quantize():
