@@ -384,23 +384,23 @@ def _extra_workloads():
     return {
         "small_nvfp4_quantize": (small_nvfp4_quantize, 200, 10),
         "activations_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64),
-                                                 2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1), 50, 5),
-        "activations_tensorwise": (activations_tensorwise, 50, 5),
-        "activations_none": (_activations(dict(mode="none"), 2 * codes + 2 * (M * K // 16), 1), 50, 5),
+                                                 2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1), 200, 5),
+        "activations_tensorwise": (activations_tensorwise, 200, 5),
+        "activations_none": (_activations(dict(mode="none"), 2 * codes + 2 * (M * K // 16), 1), 200, 5),
         "activations_hadamard_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64,
                                                                col_hadamard=True, hadamard_signs=0xA5C3),
                                                           2 * codes + 2 * (M * K // 16) + 2 * (M * K // 64) * 4, 1),
-                                             50, 5),
+                                             200, 5),
         "activations_rowwise_outer_block": (_activations(dict(mode="outer_block", outer_block_size=64),
                                                          codes + M * K // 16 + (M * K // 64) * 4, 1,
-                                                         columnwise=False), 50, 5),
+                                                         columnwise=False), 200, 5),
         "activations_rowwise_sr": (_activations(dict(mode="none", stochastic=True), codes + M * K // 16, 1,
-                                                columnwise=False), 50, 5),
-        "dequantize_activations": (dequantize_activations, 50, 5),
-        "moe_experts_e4m3": (_moe("e4m3"), 20, 3),
-        "moe_experts_ue5m3": (_moe("ue5m3"), 20, 3),
-        "moe_grouped_tokens": (moe_grouped_tokens, 30, 3),
-        "mxfp4_project_mxfp8": (mxfp4_project_mxfp8, 50, 5),
+                                                columnwise=False), 200, 5),
+        "dequantize_activations": (dequantize_activations, 200, 5),
+        "moe_experts_e4m3": (_moe("e4m3"), 40, 3),
+        "moe_experts_ue5m3": (_moe("ue5m3"), 40, 3),
+        "moe_grouped_tokens": (moe_grouped_tokens, 80, 3),
+        "mxfp4_project_mxfp8": (mxfp4_project_mxfp8, 200, 5),
         "sr_ef_weight_qdq": (sr_ef_weight_qdq, 20, 3),
     }
 

@@ -529,7 +529,8 @@ int fp4q_abi_version(void) { return FP4Q_ABI_VERSION; }
 int fp4q_device_status(int clear, void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP4Q_ERR_CUDA;
   cudaError_t (*const readers[])(uint32_t*, bool) = {ctb_timeout_flag, ctb_grouped_timeout_flag, ctb_rht_timeout_flag,
-                                                      ctl_timeout_flag, row_timeout_flag, ct_timeout_flag};
+                                                      ctl_timeout_flag, row_timeout_flag, ct_timeout_flag,
+                                                      mxfp8_timeout_flag};
   uint32_t any = 0;
   for (auto rd : readers) {
     uint32_t v = 0;

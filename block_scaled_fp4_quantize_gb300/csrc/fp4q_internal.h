@@ -168,6 +168,7 @@ cudaError_t ctb_grouped_timeout_flag(uint32_t* v, bool clear);
 cudaError_t ctb_rht_timeout_flag(uint32_t* v, bool clear);
 cudaError_t row_timeout_flag(uint32_t* v, bool clear);
 cudaError_t ct_timeout_flag(uint32_t* v, bool clear);
+cudaError_t mxfp8_timeout_flag(uint32_t* v, bool clear);
 cudaError_t ctl_timeout_flag(uint32_t* v, bool clear);
 cudaError_t set_ctb_timeout_flag();
 

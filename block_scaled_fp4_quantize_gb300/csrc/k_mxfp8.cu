@@ -261,6 +261,117 @@ __global__ void __launch_bounds__(XT, 4) mxfp8_kernel(const QuantJob j, int64_t 
   col_work(j, ys, g, m0, k0, t);
 }
 
+// ---- persistent form for bf16 input: 128 x 64 tiles copied by the tensor
+// memory accelerator into two slots (128-byte swizzle), a CTA walking the
+// tiles grid-stride, so the next tile is in flight while this one is
+// processed.  Per tile: the rowwise pass reads its 1 x 32 block from the
+// slot and stages the projection; a barrier frees the slot (refilled with
+// the tile after next) and publishes the staging; the columnwise pass; a
+// second barrier frees the staging.
+constexpr int XLRAW = XM * XK * 2;
+struct XL {
+  __host__ __device__ static constexpr int raw(int s) { return s * XLRAW; }  // 2 slots
+  static constexpr int ys = 2 * XLRAW;                                      // projected tile, bf16
+  static constexpr int bars = ys + XM * YS;                                 // 2 mbarriers
+  static constexpr int total = bars + 16 + 1024;                            // + alignment slack
+};
+
+// Set by a tile wait that ran out; read and cleared by fp4q_device_status.
+__device__ unsigned int g_mx8_timeout = 0;
+
+__device__ __forceinline__ void mx8_issue(const CUtensorMap* map, const TilePos& p, unsigned char* raw, uint64_t* bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_tx(bar, (uint32_t)XLRAW);
+  tma_load3(raw, map, (int)p.k0, (int)p.m0, (int)p.g, bar);
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(XT, 4) mxfp8_tma_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
+  pdl_wait_then_release();
+  extern __shared__ __align__(16) unsigned char smem_dyn[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  const int t = threadIdx.x;
+  unsigned char* ys = smem + XL::ys;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + XL::bars);
+  TileIter cur;
+  cur.init<XM>(j);
+  if (t == 0) {
+    mbar_init(&bars[0]);
+    mbar_init(&bars[1]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (t == 0) {  // the first two tiles; later tiles take a slot once its reads are past a barrier
+    if (cur.valid()) mx8_issue(&tmap, cur.pos<XM>(), smem + XL::raw(0), &bars[0]);
+    if (cur.idx + (int)gridDim.x < cur.ntiles)
+      mx8_issue(&tmap, cur.pos_of<XM>(cur.idx + (int)gridDim.x), smem + XL::raw(1), &bars[1]);
+  }
+  // rowwise: thread t owns row t / 2, columns 32 (t mod 2) .. + 31 (one
+  // 1 x 32 block); its four 16-byte chunks sit at these swizzled offsets
+  const int rr = t >> 1, rh = t & 1;
+  uint32_t roff[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) roff[q] = (uint32_t)(rr * 128 + (((4 * rh + q) ^ (rr & 7)) << 4));
+  int slot = 0;
+  uint32_t phase = 0;
+  while (cur.valid()) {
+    const int64_t g = cur.g, m0 = (int64_t)cur.tm * XM, k0 = (int64_t)cur.tk * XK;
+    const int after = cur.idx + 2 * (int)gridDim.x;  // the tile that takes this slot next
+    cur.next();
+    // a wait that runs out raises the error flag; the walk goes on (every
+    // later wait is bounded and every barrier is still reached)
+    if (!mbar_wait(&bars[slot], phase, 1u << 22)) atomicExch(&g_mx8_timeout, 1u);
+    const unsigned char* raw = smem + XL::raw(slot);
+    const int64_t m = m0 + rr, k = k0 + 32 * rh;
+    if (m < j.M && k < j.K) {  // rows and columns past the edge arrive as zeros and are not used
+      float v[32];
+      uint32_t mx = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + roff[q]);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * q + 2 * i] = bf16lo(ww[i]);
+          v[8 * q + 2 * i + 1] = bf16hi(ww[i]);
+          mx = q == 0 && i == 0 ? ww[i] : bf16x2_amax(mx, ww[i]);
+        }
+      }
+      mx &= 0x7FFF7FFFu;
+      const uint32_t hi = mx >> 16, lo = mx & 0xFFFFu;
+      row_work<OUT_BF16>(j, v, (hi > lo ? hi : lo) << 16, g, m, k, rr, rh, ys);
+    }
+    __syncthreads();  // the staging is complete, the slot's reads are done
+    if (t == 0 && after < cur.ntiles) mx8_issue(&tmap, cur.pos_of<XM>(after), smem + XL::raw(slot), &bars[slot]);
+    if (j.col_codes) col_work(j, ys, g, m0, k0, t);
+    __syncthreads();  // the staging is free for the next tile
+    if (++slot == 2) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+template <bool OUT_BF16>
+cudaError_t launch_tma_t(const QuantJob& j, const CUtensorMap& map, cudaStream_t st) {
+  auto kern = mxfp8_tma_kernel<OUT_BF16>;
+  static int per_sm_cache[128] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 128) dev = 0;
+  int& per_sm = per_sm_cache[dev];
+  if (per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, XL::total);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, XT, XL::total);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+  }
+  const int64_t tiles = j.G * ((j.M + XM - 1) / XM) * ((j.K + XK - 1) / XK);
+  const int64_t cap = (int64_t)num_sms() * per_sm;
+  return launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(XT), (size_t)XL::total, st, j, map);
+}
+
 template <bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_t(const QuantJob& j, cudaStream_t st) {
   const int64_t tiles_m = (j.M + XM - 1) / XM, tiles_k = (j.K + XK - 1) / XK;
@@ -270,9 +381,26 @@ cudaError_t launch_t(const QuantJob& j, cudaStream_t st) {
 
 }  // namespace
 
+// bf16 input whose rows the tensor copies can address (16-byte aligned base
+// and row stride, tile counts in 32 bits) takes the persistent form;
+// FP4Q_NO_MX8_TMA=1 turns it off (the tests run both forms).
 cudaError_t launch_mxfp8(const QuantJob& j, cudaStream_t st) {
+  if (j.in_bf16 && (reinterpret_cast<uintptr_t>(j.x) & 15u) == 0 && (j.ld * 2) % 16 == 0 &&
+      j.G * ((j.M + XM - 1) / XM) * ((j.K + XK - 1) / XK) < ((int64_t)1 << 31) && !getenv_flag("FP4Q_NO_MX8_TMA")) {
+    CUtensorMap map;
+    if (make_bf16_tile_map(j, &map, XM)) return j.out_bf16 ? launch_tma_t<true>(j, map, st) : launch_tma_t<false>(j, map, st);
+  }
   if (j.in_bf16) return j.out_bf16 ? launch_t<true, true>(j, st) : launch_t<true, false>(j, st);
   return j.out_bf16 ? launch_t<false, true>(j, st) : launch_t<false, false>(j, st);
+}
+
+cudaError_t mxfp8_timeout_flag(uint32_t* v, bool clear) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_mx8_timeout, sizeof(uint32_t));
+  if (e == cudaSuccess && clear) {
+    const uint32_t z = 0;
+    e = cudaMemcpyToSymbol(g_mx8_timeout, &z, sizeof z);
+  }
+  return e;
 }
 
 }  // namespace fp4q

@@ -20,6 +20,16 @@ def _cuda():
     fq.build()
 
 
+@pytest.fixture(params=["tma", "plain"], autouse=True)
+def form(request, monkeypatch):
+    """bf16 input takes the persistent TMA-fed kernel; "plain" forces the
+    one-tile-per-CTA kernel (fp32 input always takes it)."""
+    monkeypatch.delenv("FP4Q_NO_MX8_TMA", raising=False)
+    if request.param == "plain":
+        monkeypatch.setenv("FP4Q_NO_MX8_TMA", "1")
+    return request.param
+
+
 def _check(orc, x, rowwise=True, columnwise=True, out_dtype=None):
     out_dtype = out_dtype or x.dtype
     q = fq.mxfp4_project_mxfp8(x.cuda(), rowwise=rowwise, columnwise=columnwise, with_y=True, out_dtype=out_dtype)
