@@ -98,8 +98,9 @@ __device__ __forceinline__ void amax_unit(const uint4 w, const float* res, uint3
 }
 
 // Tensorwise amax of a contiguous tensor (leading dimension K, 16-byte
-// aligned x and residual): four 16-byte loads in flight per thread per
-// iteration, a scalar tail, one atomicMax per CTA.
+// aligned x and residual): each warp streams 2 KB contiguous chunks (four
+// 512-byte loads in flight), a scalar tail, one atomicMax per CTA.  (Four
+// strided streams per thread, or more loads in flight, read slower.)
 template <bool IN_BF16, bool RES>
 __global__ void __launch_bounds__(256) tensor_amax_flat_kernel(const QuantJob j, uint32_t* amax) {
   pdl_wait_then_release();
@@ -109,16 +110,18 @@ __global__ void __launch_bounds__(256) tensor_amax_flat_kernel(const QuantJob j,
   const int64_t nv = n / EPV;
   const uint4* xv = static_cast<const uint4*>(j.x);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // each warp reads 2 KB contiguous per iteration (four 512-byte loads)
+  const int64_t wstride = stride * 4;
+  int64_t i = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 128 + (threadIdx.x & 31);
   uint32_t acc = 0;
-  for (; i + 3 * stride < nv; i += 4 * stride) {
+  for (; i + 96 < nv; i += wstride) {
     uint4 w[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = __ldcs(xv + i + q * stride);
+    for (int q = 0; q < 4; ++q) w[q] = __ldcs(xv + i + q * 32);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) amax_unit<IN_BF16, RES>(w[q], RES ? j.residual + (i + q * stride) * EPV : nullptr, acc);
+    for (int q = 0; q < 4; ++q) amax_unit<IN_BF16, RES>(w[q], RES ? j.residual + (i + q * 32) * EPV : nullptr, acc);
   }
-  for (; i < nv; i += stride) amax_unit<IN_BF16, RES>(__ldcs(xv + i), RES ? j.residual + i * EPV : nullptr, acc);
+  for (; i < nv; i += 32) amax_unit<IN_BF16, RES>(__ldcs(xv + i), RES ? j.residual + i * EPV : nullptr, acc);
   uint32_t v;
   if (RES) {
     v = acc;
