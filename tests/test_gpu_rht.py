@@ -51,9 +51,13 @@ def test_rht_matches_oracle(orc, case, signs):
                                   dict(mode="outer_block", outer_block_size=64, scale_format="ue5m3")],
                          ids=["none", "ob64", "ob64-ue5m3"])
 def test_rht_whole_tiles(orc, case):
-    """M a multiple of 128 and K of 64: the kernel's whole-tile form."""
+    """M a multiple of 128 and K of 64: the kernel's whole-tile form, with a
+    block whose butterfly sums overflow, a zero 64-row column group and a
+    block of tiny values (the general per-block steps)."""
     x = W.lognormal((2, 256, 192), 93, sigma=2.5)
     x[1, 128:144, 70] = 3.3895314e38
+    x[0, 0:64, 5] = 0.0
+    x[0, 128:144, 9] *= 1e-30
     for mask in ((False, True), (True, True)):
         kw = dict(case, rowwise=mask[0], columnwise=mask[1], col_hadamard=True, hadamard_signs=0x5A0F)
         _, g = gpu_quantize(x, **kw)
