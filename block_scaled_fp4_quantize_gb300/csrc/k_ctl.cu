@@ -4,23 +4,24 @@
 // cast-transpose; section 6: a 2-D outer scale computed once and shared by
 // both orientations; "NVFP4 / AMD-FP4 outer-block (two-level) scaling for FP4
 // training", "Technical design": outer and inner scales), for the calls whose
-// facts let every bound check fold away: M a multiple of 128, K of 64, bf16
-// input, round-to-nearest, both orientations, linear scale layout, and an
-// outer scale that is none, one per tensor (from the tensorwise amax), 1 x 64
-// / 64 x 1 or 64 x 64.  Every other call takes the general cast-transpose
-// kernel (k_ctb.cuh), which gives the same bits.
+// facts let every bound check fold away: M a multiple of 128 (64 for ragged
+// groups), K of 64, bf16 input, round-to-nearest, both orientations, linear
+// scale layout, and an outer scale that is none, one per tensor (from the
+// tensorwise amax), 1 x 64 / 64 x 1 or 64 x 64.  Every other call takes the
+// general cast-transpose kernel (k_ctb.cuh), which gives the same bits.
 //
-// Per tile, one CTA barrier.  Before it, every thread takes the block maxima
-// it needs from the raw tile (rowwise: its half row, two 1 x 16 blocks;
-// columnwise: its two 16 x 1 column blocks) and publishes what other warps
-// need (the columns' 64-row maxima for 64 x 1 outer blocks, the warp's
-// maximum for 64 x 64 blocks).  After it, the columnwise pass (its 16 words
-// still in registers) and the rowwise pass (four 16-byte reloads) compute
-// scales and codes.  The barrier also orders the previous tile's staged
-// columnwise codes and scales before their stores (tensor store of the
-// codes, 8-byte stores of the scales), so staging alternates between two
-// buffers by tile parity, and the tile after next is copied into the slot
-// whose last reader is past this barrier.
+// Per tile, one CTA barrier.  Before it, every thread reads what it needs
+// from the raw tile (rowwise: its half row, two 1 x 16 blocks; columnwise:
+// its two 16 x 1 column blocks, kept in registers) and publishes what other
+// warps need (the columns' 64-row maxima for 64 x 1 outer blocks, the warp's
+// maximum for 64 x 64 blocks); the forms without outer blocks finish their
+// rowwise pass there.  After it, the columnwise pass and (outer-block forms)
+// the rowwise pass compute scales and codes.  The barrier also orders the
+// previous tile's staged codes and scales before their stores (tensor stores
+// of the columnwise codes and, for the outer-block forms, of the rowwise
+// codes; 8-byte stores of the column scales), so staging alternates between
+// two buffers by tile parity, and the tile after next is copied into the
+// slot whose last reader is past this barrier.
 //
 // The arithmetic.  The outer amax A of bf16 data is a bf16 value, so S =
 // RN(A / (scale_max * 6)) has one of 128 significands (set by the 7 mantissa
@@ -33,10 +34,9 @@
 // dividends), its E4M3 code from the hardware conversion.  The table rows sit
 // in shared memory with the exponent of S folded in (one bulk copy of a
 // precomputed image per CTA), so a block's multipliers are two table loads
-// and two integer adds.  A warp
-// whose outer amax lies outside [2^-90, 2^101) (2^109 for UE5M3 scales),
-// where the scaled entries stay normal, takes the general per-block steps
-// with div.rn.
+// and two integer adds.  A warp whose outer amax lies outside [2^-90, 2^101)
+// (2^109 for UE5M3 scales), where the scaled entries stay normal, takes the
+// general per-block steps with div.rn.
 #include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
