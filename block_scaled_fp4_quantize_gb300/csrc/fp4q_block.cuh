@@ -195,8 +195,8 @@ __device__ __forceinline__ void encode16(const float (&x)[16], const float4& T, 
 // Per-block steps for a block the FMA division sequences cover
 // (fast_block below): `a` = RN(am / S) is already known and no step needs a
 // fallback.  OUTER: an outer scale applies; NEG: the values arrive negated.
-template <bool SR, bool UE5M3, bool OUTER, bool NEG>
-__device__ __forceinline__ uint32_t block_fast(const float4* tab, const float (&v)[16], float a, float S, float r,
+template <bool SR, bool UE5M3, bool OUTER, bool NEG, class TabT>
+__device__ __forceinline__ uint32_t block_fast(const TabT& tab, const float (&v)[16], float a, float S, float r,
                                                const PhiloxKeys& K, uint32_t step, uint32_t orient, uint64_t n0,
                                                uint32_t& w0, uint32_t& w1) {
   const uint32_t sc = encode_scale<UE5M3>(div_bmr(a, bitsf(kSixHi), bitsf(kSixLo)));

@@ -40,7 +40,7 @@
 #include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
-#include "fp4q_pairtab.cuh"
+#include "fp4q_pair.cuh"
 #include "fp4q_tma.cuh"
 
 #include <type_traits>
@@ -79,49 +79,11 @@ static_assert(LLT<true>::pt % 16 == 0 && LLT<false>::pt % 16 == 0 && LLT<true>::
 // leave the room).
 __host__ __device__ constexpr bool row_tma(int lof) { return lof >= 2; }
 
-// row of the shared table holding the split reciprocal (zh, zl) of S (rows
-// 0-7: the pairs by inner significand; row 8: a zero inner scale)
-constexpr uint32_t PT_RCP = 9;
-// bytes of the kCtlTab image the two forms copy: the rows and the code table
-// (outer scales), or the table of the form without outer scale
-constexpr uint32_t kImgOuter = (10 * 128 * 2 + 256) * 4, kImgUnit = 256 * 2 * 4;
-static_assert(kImgOuter + kImgUnit == kCtlTabWords * 4, "image layout");
-
 // Outer-scale form of a launch
 enum LO : int { LO_NONE = 0, LO_UNIFORM = 1, LO_1D = 2, LO_2D = 3 };
 
 // Set by a tile wait that ran out; read and cleared by fp4q_device_status.
 __device__ unsigned int g_ctl_timeout = 0;
-
-// bits of the amax A = scale_max * 6 (S = 1): the table position of "no outer scale"
-template <bool UE5M3>
-__device__ __forceinline__ constexpr uint32_t unit_amax() { return UE5M3 ? 0x49280000u : 0x45280000u; }
-
-// The amax bits A (a bf16 value) admit the table path: A in [2^-90, 2^101)
-// (E4M3) or [2^-90, 2^109) (UE5M3), so that 2^-90 < S < 2^90.
-template <bool UE5M3>
-__device__ __forceinline__ bool table_ok(uint32_t A) {
-  return A - kTiny < (UE5M3 ? 0x76000000u : 0x72000000u) - kTiny;
-}
-
-// byte offset of the amax's mantissa in a table row
-__device__ __forceinline__ uint32_t moff_of(uint32_t A) { return (A >> 13) & 0x3F8u; }
-
-// c1 and c2 of a block with scale code sc whose outer amax has bits A
-__device__ __forceinline__ void pair_mults(const unsigned char* ptb, const uint32_t* ctab, uint32_t sc, uint32_t A,
-                                           float& c1, float& c2) {
-  const uint32_t w = ctab[sc];
-  const uint2 e = *reinterpret_cast<const uint2*>(ptb + (w & 0xFFFFu) + moff_of(A));
-  c1 = bitsf(e.x - A);
-  c2 = bitsf(e.y + (w & 0xFF800000u));
-}
-
-// split reciprocal (zh, zl) of S for the amax bits A
-__device__ __forceinline__ void outer_rcp(const unsigned char* ptb, uint32_t A, float& zh, float& zl) {
-  const uint2 e = *reinterpret_cast<const uint2*>(ptb + PT_RCP * 1024u + moff_of(A));
-  zh = bitsf(e.x - A);
-  zl = bitsf(e.y - A);
-}
 
 // Column loads of rows c and c + 8 (shared-memory offset OFF of the slot;
 // ca: the lane's address in slot 0, row 0; the 128-byte swizzle XORs the
@@ -222,11 +184,6 @@ __device__ __forceinline__ void col_codes16(const uint32_t (&w)[16], uint64_t C1
   }
 }
 
-// Inner-scale table entries computed on demand (for the general steps).
-template <bool UE5M3>
-struct EntryCalc {
-  __device__ __forceinline__ float4 operator[](uint32_t c) const { return scale_entry<UE5M3>(c); }
-};
 
 // The general per-block steps (div.rn where the FMA sequences do not reach):
 // 16 values u, block maximum am, outer scale S, R = 1 / S.

@@ -18,6 +18,7 @@
 #include "fp4q_block.cuh"
 #include "fp4q_device.cuh"
 #include "fp4q_internal.h"
+#include "fp4q_pair.cuh"
 #include "fp4q_tma.cuh"
 
 namespace fp4q {
@@ -257,13 +258,18 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// With 1 x ob outer blocks or one tensorwise scale (PAIR) the kernel takes
+// the pair-table path of fp4q_pair.cuh when the outer amax (a bf16 value) is
+// in its range: the table image arrives by one more bulk copy, and per value
+// pair the codes cost two packed multiplies; the general per-block steps
+// then take their inner-scale entries computed on demand.
 template <bool UE5M3, int RO>
 __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
-  pdl_wait_then_release();
+  constexpr bool PAIR = RO == RO_WARP || RO == RO_UNIFORM;
   __shared__ __align__(128) unsigned char buf[QS][QB * 32];
-  __shared__ float4 tab[256];
-  __shared__ __align__(8) uint64_t bars[QS];
-  __shared__ float2 ztab[128];
+  __shared__ __align__(16) unsigned char img[PAIR ? kImgOuter : 16];  // the pair-table image
+  __shared__ float4 tab_s[PAIR ? 1 : 256];                            // inner-scale table (other forms)
+  __shared__ __align__(8) uint64_t bars[QS + 1];
   const int t = threadIdx.x, lane = t & 31;
   const int64_t nblk = j.G * j.M * j.K / 16, nch = (nblk + QB - 1) / QB;
   const unsigned char* xb = static_cast<const unsigned char*>(j.x);
@@ -275,9 +281,14 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
   };
   if (t == 0) {
 #pragma unroll
-    for (int s = 0; s < QS; ++s) mbar_init(&bars[s]);
+    for (int s = 0; s <= QS; ++s) mbar_init(&bars[s]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (PAIR) {  // constant data: the copy may start before the previous grid has finished
+      mbar_expect_tx(&bars[QS], kImgOuter);
+      bulk_load(img, kCtlTab[UE5M3 ? 1 : 0], kImgOuter, &bars[QS]);
+    }
   }
+  pdl_wait_then_release();
   __syncthreads();
   if (t == 0) {
 #pragma unroll
@@ -286,9 +297,18 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
       if (c < nch) issue(c, s);
     }
   }
-  build_scale_table<UE5M3>(tab, t, RT);
-  if (RO == RO_WARP || RO == RO_UNIFORM) build_ztab(ztab, t);
-  const TabView tv{tab};
+  if (!PAIR) build_scale_table<UE5M3>(tab_s, t, RT);
+  // the inner-scale entries: the shared table, or computed on demand
+  auto entries = [&]() {
+    if constexpr (PAIR) return EntryCalc<UE5M3>{};
+    else return static_cast<const float4*>(tab_s);
+  };
+  const auto tab = entries();
+  struct {
+    decltype(entries()) tab;
+  } tv{tab};
+  const unsigned char* ptb = img;
+  const uint32_t* ctab = reinterpret_cast<const uint32_t*>(PAIR ? img + 10240 : img);
   const int per = RO == RO_WARP || RO == RO_BUFFER ? j.ob / 16 : 1;
   const bool per_pow2 = (per & (per - 1)) == 0;
   const int lper = 31 - __clz(per);
@@ -305,9 +325,10 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
     r_u = ieee_rcp(S_u);
   }
   __syncthreads();
+  if (PAIR && !mbar_wait(&bars[QS], 0u, 1u << 22)) atomicExch(&g_row_timeout, 1u);
   float zh_u = 0.0f, zl_u = 0.0f;
-  const bool u_z = RO == RO_UNIFORM && j.s_src == S_TENSORWISE_WS && (A_u & 0xFFFFu) == 0u && zsplit_ok(A_u, S_u);
-  if (u_z) zsplit(A_u, S_u, ztab, zh_u, zl_u);
+  const bool u_z = RO == RO_UNIFORM && j.s_src == S_TENSORWISE_WS && (A_u & 0xFFFFu) == 0u && table_ok<UE5M3>(A_u);
+  if (u_z) outer_rcp(ptb, A_u, zh_u, zl_u);
   int slot = 0;
   uint32_t phase = 0;
   for (int64_t c = blockIdx.x; c < nch; c += gridDim.x) {
@@ -340,21 +361,22 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
     n.none = RO == RO_NONE;
     n.S = 1.0f;
     n.r = 1.0f;
-    bool zfast = u_z;  // the table-driven division of fp4q_block.cuh (zsplit)
+    bool zfast = u_z;  // the pair-table path
     float zh = zh_u, zl = zl_u;
+    uint32_t A = A_u;  // the outer amax bits (pair path)
     if (RO == RO_UNIFORM) {
       n.S = S_u;
       n.r = r_u;
     } else if (RO == RO_WARP) {
       uint32_t g = fbits(am);
       for (int o = 1; o < per; o <<= 1) g = umax(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
-      // the outer amax of bf16 inputs is a bf16 value: the table-driven
-      // division when the warp's scales are in its range
-      const float S = div_bmr(bitsf(g), bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));
-      zfast = __all_sync(0xFFFFFFFFu, zsplit_ok(g, S));
+      // the outer amax of bf16 inputs is a bf16 value: the pair table when
+      // the warp's scales are in its range
+      zfast = __all_sync(0xFFFFFFFFu, table_ok<UE5M3>(g));
       if (zfast) {
-        n.S = S;
-        zsplit(g, S, ztab, zh, zl);
+        n.S = div_bmr(bitsf(g), bitsf(UE5M3 ? kDenHiU5 : kDenHiE4), bitsf(UE5M3 ? kDenLoU5 : kDenLoE4));  // exact
+        outer_rcp(ptb, g, zh, zl);
+        A = g;
       } else {
         outer_sr<UE5M3>(bitsf(g), n.S, n.r);
       }
@@ -364,8 +386,18 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
       n.r = ieee_rcp(n.S);
     }
     uint32_t sc, w0, w1;
-    if (zfast) {
-      sc = block_zsplit<UE5M3>(tab, u, am, zh, zl, w0, w1);
+    if (PAIR && zfast) {
+      // a = RN(am / S), v = RN(a / 6) by the known-divisor method; the codes
+      // by the pair's multipliers, two values per instruction
+      sc = encode_scale<UE5M3>(div_bmr(div_bmr(am, zh, zl), bitsf(kSixHi), bitsf(kSixLo)));
+      float c1, c2;
+      pair_mults(ptb, ctab, sc, A, c1, c2);
+      const uint64_t C1 = pk2(c1, c1), C2 = pk2(c2, c2);
+      float tq[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) upk2(mul2(mul2(pk2(u[i], u[i + 1]), C1), C2), tq[i], tq[i + 1]);
+      w0 = e2m1x8_rne(tq);
+      w1 = e2m1x8_rne(tq + 8);
     } else {
       float a = am;
       const bool fast = __all_sync(0xFFFFFFFFu, RO == RO_NONE || fast_block(am, n.S, n.r, a));
