@@ -301,69 +301,6 @@ __device__ __forceinline__ float bf16x2_hmax(uint32_t m) {
   return bitsf((hi > lo ? hi : lo) << 16);
 }
 
-// How x' = u / S is formed on the fast path.
-enum NMode : int {
-  NM_NONE = 0,  // no outer scale: x' = u
-  NM_MARK = 1,  // Markstein's correction from RN(1 / S): the pair (S, -1 / S)
-  NM_BMR = 2,   // the known-divisor method: the pair (zh, zl) of S (zsplit below)
-};
-
-// The split reciprocal (zh, zl) = (RD(1 / S), RN(1 / S - zh)) of an outer
-// scale S = RN(A / (scale_max * 6)) whose amax A is a bf16 value (the
-// maximum of bf16 inputs): S's significand is that of RN(m / 21), m = 128 ..
-// 255 A's significand, so the pair for it comes from a 128-entry table and
-// is scaled by S's power of two.  For every such divisor and every bf16
-// dividend, RN(u zh + RN(u zl)) = RN(u / S) (checked with exact rationals
-// for all 128 x 255 significand pairs); the scaled zl stays normal while S
-// < 2^90 (the smallest table zl is above 2^-30), which callers check with
-// zsplit_ok.
-__device__ __forceinline__ void zsplit(uint32_t Abits, float S, const float2* ztab, float& zh, float& zl) {
-  const float2 z = ztab[(Abits >> 16) & 0x7Fu];
-  const uint32_t adj = 0x3F800000u - (fbits(S) & 0x7F800000u);
-  zh = bitsf(fbits(z.x) + adj);
-  zl = fbits(z.y) ? bitsf(fbits(z.y) + adj) : 0.0f;
-}
-
-// Fill the table of zsplit: entry m for the significand sigma of RN((128 +
-// m) / 21), zh = RD(1 / sigma) and zl = RN(1 / sigma - zh), where
-// 1 / sigma - zh = (1 - zh sigma) / sigma and 1 - zh sigma is exact in one
-// fused multiply-add.
-__device__ __forceinline__ void build_ztab(float2* ztab, int t) {
-  if (t < 128) {
-    const float q = ieee_div((float)(128 + t), 21.0f);   // in [6.09, 12.15]
-    const float sg = ieee_mul(q, q < 8.0f ? 0.25f : 0.125f);  // exact: [1, 2)
-    float zh, e, zl;
-    asm("div.rm.f32 %0, 0f3F800000, %1;" : "=f"(zh) : "f"(sg));
-    asm("{\n\t.reg .f32 n;\n\tneg.f32 n, %1;\n\tfma.rn.f32 %0, n, %2, 0f3F800000;\n\t}" : "=f"(e) : "f"(zh), "f"(sg));
-    zl = ieee_div(e, sg);
-    ztab[t] = make_float2(zh, zl);
-  }
-}
-
-// The amax A (bits) and its scale S admit zsplit: A at least 2^-90 (S
-// normal) and S below 2^90.
-__device__ __forceinline__ bool zsplit_ok(uint32_t Abits, float S) { return Abits >= kTiny && fbits(S) < 0x6C800000u; }
-
-// One 1 x 16 block of bf16-exact values u with an outer scale S given by its
-// split reciprocal (zh, zl) (zsplit): a = RN(am / S) and x' = RN(u / S) by the
-// known-divisor method (exact for bf16 dividends, no range check needed:
-// a value whose quotient is small enough to lose bits cannot move a code),
-// then the inner scale and the codes.
-template <bool UE5M3>
-__device__ __forceinline__ uint32_t block_zsplit(const float4* tab, const float (&u)[16], float am, float zh, float zl,
-                                                 uint32_t& w0, uint32_t& w1) {
-  const float a = div_bmr(am, zh, zl);
-  const uint32_t sc = encode_scale<UE5M3>(div_bmr(a, bitsf(kSixHi), bitsf(kSixLo)));
-  const float4 T = tab[sc];
-  const uint64_t ZS = pk2(zh, zh), LS = pk2(zl, zl), ZH2 = pk2(T.y, T.y), ZL2 = pk2(T.z, T.z);
-  float t[16];
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) upk2(bmr2(bmr2(pk2(u[i], u[i + 1]), ZS, LS), ZH2, ZL2), t[i], t[i + 1]);
-  w0 = e2m1x8_rne(t);
-  w1 = e2m1x8_rne(t + 8);
-  return sc;
-}
-
 // Inner-scale table entry of code c: (DEC(c), zh, zl, 0) with zh + zl the
 // split reciprocal of DEC(c) used by div_bmr.
 template <bool UE5M3>
