@@ -100,3 +100,58 @@ def test_whole_tile_reused_outputs_and_back_to_back_calls():
             r = refs[2]
             for k in ("row_codes", "row_scales", "row_outer", "col_codes", "col_scales", "col_outer"):
                 assert torch.equal(getattr(q, k), getattr(r, k)), k
+
+
+# outer amax values at the edges of the pair-table range (bf16 values):
+# 2^-90 and just above (the smallest S), the largest in range with sigma = 1
+# (m = 40: the folded zl of S = 2^89 is exactly 2^-126) and with m = 127,
+# and the first ones outside (the general steps)
+_EDGES = {"e4m3": [2.0 ** -90, 1.0078125 * 2.0 ** -90, 1.3125 * 2.0 ** 100, 1.9921875 * 2.0 ** 100, 2.0 ** 101,
+                   1.5 * 2.0 ** -91],
+          "ue5m3": [2.0 ** -90, 1.3125 * 2.0 ** 108, 1.9921875 * 2.0 ** 108, 2.0 ** 109, 1.5 * 2.0 ** -91]}
+
+
+def _edge_blocks(amaxes, seed):
+    """[1, 128, 64 * n]: one 128 x 64 tile per amax, every 64 x 64 block and
+    every 1 x 64 / 64 x 1 group of it holding that amax, the other values
+    spread over 2^-30 of it up to it."""
+    g = torch.Generator().manual_seed(seed)
+    tiles = []
+    for A in amaxes:
+        t = torch.rand(128, 64, generator=g, dtype=torch.float64) * 2.0 - 1.0
+        t = t * torch.pow(2.0, -30.0 * torch.rand(128, 64, generator=g, dtype=torch.float64))
+        t = t * A
+        idx = torch.arange(128)
+        t[idx, (idx * 7) % 64] = A * torch.where(idx % 2 == 0, 1.0, -1.0).double()   # each row's max
+        t[(torch.arange(64) * 5) % 128, torch.arange(64)] = A                          # each column's max
+        tiles.append(t)
+    return torch.cat(tiles, dim=1)[None].to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
+@pytest.mark.parametrize("mode,cols", [("ob64", True), ("ob64-2d", True), ("ob64", False)],
+                         ids=["ob64", "ob64-2d", "ob64-rowwise"])
+def test_whole_tile_scale_range_edges(orc, fmt, mode, cols, monkeypatch):
+    """The whole-tile kernel (rowwise + columnwise) and the bulk rowwise
+    kernel (rowwise only) on outer amax values at the pair table's range
+    edges, against the oracle and against the general kernels."""
+    x = _edge_blocks(_EDGES[fmt], 95)
+    assert (x.float().abs().amax(dim=1)[0].view(-1, 64).amax(dim=1).double() ==
+            torch.tensor(_EDGES[fmt], dtype=torch.float64)).all()
+    kw = dict(MODES[mode], scale_format=fmt, rowwise=True, columnwise=cols)
+    _, g = gpu_quantize(x, **kw)
+    assert_same(g, oracle_quantize(orc, x, **kw))
+    monkeypatch.setenv("FP4Q_NO_CTL_KERNEL", "1")
+    monkeypatch.setenv("FP4Q_GENERAL_KERNEL", "1")
+    _, g2 = gpu_quantize(x, **kw)
+    assert_same(g2, {k: v for k, v in g.items() if v is not None})
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "ue5m3"])
+@pytest.mark.parametrize("cols", [True, False], ids=["both", "rowwise"])
+def test_whole_tile_tensorwise_range_edges(orc, fmt, cols):
+    for A in _EDGES[fmt]:
+        x = _edge_blocks([A], 96)
+        kw = dict(MODES["tensorwise"], scale_format=fmt, rowwise=True, columnwise=cols)
+        _, g = gpu_quantize(x, **kw)
+        assert_same(g, oracle_quantize(orc, x, **kw))
