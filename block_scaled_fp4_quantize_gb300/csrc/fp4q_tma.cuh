@@ -106,6 +106,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // ---- tensor-memory-access (TMA) tile loads, completion on an mbarrier ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+// The dynamic shared-memory base rounded up to a 1024-byte boundary.  The
+// result is an offset from `base`, not an integer cast back to a pointer, so
+// the compiler still knows it points to shared memory: accesses through it
+// compile to 32-bit shared loads and stores rather than 64-bit generic ones.
+__device__ __forceinline__ unsigned char* smem_align1024(unsigned char* base) {
+  return base + ((0u - smem_u32(base)) & 1023u);
+}
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar) {
   asm volatile("mbarrier.init.shared.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(NT, COL ? 2 : 3) cp_kernel(const QuantJob j, c
   using L = Layout<IN_BF16, NS>;
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   // the 128-byte swizzle of the tensor copies needs 1024-byte aligned tiles
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  unsigned char* smem = smem_align1024(smem_dyn);
   const int t = threadIdx.x;
   const bool none = j.s_src == S_ONE;
   const bool shared_S = none || j.mode == 1 || j.outer_2d;

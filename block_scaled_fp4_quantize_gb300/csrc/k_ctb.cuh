@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(BT, (RHT || SR) ? 3 : 4) ctb_kernel(const Quan
   const int col_tma = FTM ? 1 : col_tma_;
   pdl_wait_then_release();
   extern __shared__ __align__(16) unsigned char smem_dyn[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  unsigned char* smem = smem_align1024(smem_dyn);
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   float4* tab = reinterpret_cast<float4*>(smem + BL::tab);
   uint32_t* red2d = reinterpret_cast<uint32_t*>(smem + BL::red2d);

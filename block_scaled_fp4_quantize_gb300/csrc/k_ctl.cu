@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
   constexpr bool RT = row_tma(LOF);
   using LL = LLT<RT>;
   extern __shared__ __align__(16) unsigned char smem_dyn[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  unsigned char* smem = smem_align1024(smem_dyn);
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const unsigned char* ptb = smem + LL::pt;
   const uint32_t* ctab = reinterpret_cast<const uint32_t*>(smem + LL::ctab);

@@ -289,7 +289,7 @@ template <bool OUT_BF16>
 __global__ void __launch_bounds__(XT, 4) mxfp8_tma_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap) {
   pdl_wait_then_release();
   extern __shared__ __align__(16) unsigned char smem_dyn[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  unsigned char* smem = smem_align1024(smem_dyn);
   const int t = threadIdx.x;
   unsigned char* ys = smem + XL::ys;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + XL::bars);
