@@ -14,14 +14,15 @@
 // from the raw tile (rowwise: its half row, two 1 x 16 blocks; columnwise:
 // its two 16 x 1 column blocks, kept in registers) and publishes what other
 // warps need (the columns' 64-row maxima for 64 x 1 outer blocks, the warp's
-// maximum for 64 x 64 blocks); the forms without outer blocks finish their
-// rowwise pass there.  After it, the columnwise pass and (outer-block forms)
-// the rowwise pass compute scales and codes.  The barrier also orders the
-// previous tile's staged codes and scales before their stores (tensor stores
-// of the columnwise codes and, for the outer-block forms, of the rowwise
-// codes; 8-byte stores of the column scales), so staging alternates between
-// two buffers by tile parity, and the tile after next is copied into the
-// slot whose last reader is past this barrier.
+// maximum for 64 x 64 blocks).  After it, the rowwise and columnwise passes
+// compute scales and codes and stage the codes in shared memory.  The barrier
+// also orders the previous tile's staged codes and scales before their
+// stores (tensor stores of the rowwise and columnwise codes, 8-byte stores of
+// the column scales), so staging alternates between two buffers by tile
+// parity, and the tile after next is copied into the slot whose last reader
+// is past this barrier.  Staging the rowwise codes for tensor stores costs
+// the shared memory of a fourth CTA per SM and still measured faster than
+// 16-byte stores from registers at four CTAs.
 //
 // The arithmetic.  The outer amax A of bf16 data is a bf16 value, so S =
 // RN(A / (scale_max * 6)) has one of 128 significands (set by the 7 mantissa
@@ -55,29 +56,25 @@ static_assert(LT == 256, "one thread per scale code builds the code tables");
 
 // Shared memory (offsets from the 1024-byte aligned base).  Buffers that
 // tensor copies read or write start on 1024-byte boundaries (the copies need
-// 128, the swizzled loads 1024).  RT: the form stages its rowwise codes too.
-template <bool RT>
-struct LLT {
+// 128, the swizzled loads 1024).
+struct LL {
   __host__ __device__ static constexpr int raw(int s) { return s * LRAW; }                   // 2 input slots
   __host__ __device__ static constexpr int ccs(int s) { return 2 * LRAW + s * 4096; }        // col codes, [64][64] swizzled
-  __host__ __device__ static constexpr int rcs(int s) { return 2 * LRAW + 8192 + s * 4096; } // row codes [128][32] (RT)
-  static constexpr int rt_bytes = RT ? 8192 : 0;
-  __host__ __device__ static constexpr int sst(int s) { return 2 * LRAW + 8192 + rt_bytes + s * 512; }  // col scales [64][8]
-  __host__ __device__ static constexpr int red(int s) { return sst(2) + s * 1024; }  // [8 warps][32 lanes] u32
-  static constexpr int pt = red(2);      // 10 rows x 128 x (u32, u32), rows 1024 bytes apart
-                                         // (no outer scale: 256 x (c1, c2) by scale code)
-  static constexpr int ctab = pt + 10240;  // 256 x u32: scale code -> row and exponent of 1 / s
-  static constexpr int bars = ctab + 1024;  // 3 mbarriers: two input slots, the tables
+  __host__ __device__ static constexpr int rcs(int s) { return 2 * LRAW + 8192 + s * 4096; } // row codes [128][32]
+  __host__ __device__ static constexpr int sst(int s) { return 2 * LRAW + 16384 + s * 512; }  // col scales [64][8]
+  __host__ __device__ static constexpr int red(int s) { return 2 * LRAW + 17408 + s * 1024; }  // [8 warps][32 lanes] u32
+  static constexpr int pt = 2 * LRAW + 19456;  // 10 rows x 128 x (u32, u32), rows 1024 bytes apart
+                                               // (no outer scale: 256 x (c1, c2) by scale code)
+  static constexpr int ctab = pt + 10240;      // 256 x u32: scale code -> row and exponent of 1 / s
+  static constexpr int bars = ctab + 1024;     // 3 mbarriers: two input slots, the tables
   static constexpr int total = bars + 32 + 1024;  // + alignment slack
 };
-static_assert(LLT<true>::rcs(0) % 1024 == 0 && LLT<true>::rcs(1) % 1024 == 0 && LLT<true>::ccs(1) % 1024 == 0,
+static_assert(LL::rcs(0) % 1024 == 0 && LL::rcs(1) % 1024 == 0 && LL::ccs(1) % 1024 == 0,
               "tensor-copy staging alignment");
-static_assert(LLT<true>::pt % 16 == 0 && LLT<false>::pt % 16 == 0 && LLT<true>::bars % 8 == 0 && LLT<false>::bars % 8 == 0,
-              "bulk-copy and mbarrier alignment");
-// Forms that stage the rowwise codes in shared memory and store them with
-// tensor copies (their row pass runs after the barrier; three CTAs per SM
-// leave the room).
-__host__ __device__ constexpr bool row_tma(int lof) { return lof >= 2; }
+static_assert(LL::pt % 16 == 0 && LL::bars % 8 == 0, "bulk-copy and mbarrier alignment");
+static_assert(LL::sst(0) == LL::rcs(2) && LL::red(0) == LL::sst(2) && LL::pt == LL::red(2), "regions back to back");
+// resident CTAs per SM (shared memory: 3 x LL::total fit)
+constexpr int kCtlPerSm = 3;
 
 // Outer-scale form of a launch
 enum LO : int { LO_NONE = 0, LO_UNIFORM = 1, LO_1D = 2, LO_2D = 3 };
@@ -213,14 +210,12 @@ __device__ __forceinline__ uint32_t slow_block(const float (&v)[16], float am, f
 // half tile of 64 rows; the columnwise outputs go to the group's own
 // transpose by vector stores (its row length differs from group to group).
 template <bool UE5M3, int LOF, bool GR>
-__global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(LT, kCtlPerSm) ctl_kernel(const QuantJob j, const __grid_constant__ CUtensorMap tmap,
                                                                        const __grid_constant__ CUtensorMap cmap,
                                                                        const __grid_constant__ CUtensorMap rmap,
                                                                        const __grid_constant__ CUtensorMap rmap64) {
   constexpr bool OUTER = LOF != LO_NONE;
-  static_assert(!GR || row_tma(LOF), "groups: outer-block forms only");
-  constexpr bool RT = row_tma(LOF);
-  using LL = LLT<RT>;
+  static_assert(!GR || LOF == LO_1D || LOF == LO_2D, "groups: outer-block forms only");
   extern __shared__ __align__(16) unsigned char smem_dyn[];
   unsigned char* smem = smem_align1024(smem_dyn);
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -316,7 +311,7 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
   auto store_prev = [&](int pp) {
     if (t == 0) {
       if (!GR) tma_store3(&cmap, smem + LL::ccs(pp), pm0 >> 1, pk0, pg);
-      if (RT) tma_store2(phalf ? &rmap64 : &rmap, smem + LL::rcs(pp), pk0 >> 1, (int)(pg * j.M + pm0));
+      tma_store2(phalf ? &rmap64 : &rmap, smem + LL::rcs(pp), pk0 >> 1, (int)(pg * j.M + pm0));
       bulk_commit();
     }
     const int64_t cb = j.K * pgb + pmr;  // columnwise index of (k, first row): cb + k pgm (the matrix's transpose)
@@ -374,8 +369,7 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
 
     auto row_store = [&](const uint32_t (&c)[4], uint32_t sc) {
       const int64_t e = row * j.K + tk0 + 32 * rh;  // flat index of the thread's first element
-      if (RT) *reinterpret_cast<uint4*>(smem + LL::rcs(par) + rr * 32 + rh * 16) = make_uint4(c[0], c[1], c[2], c[3]);
-      else *reinterpret_cast<uint4*>(j.row_codes + (e >> 1)) = make_uint4(c[0], c[1], c[2], c[3]);
+      *reinterpret_cast<uint4*>(smem + LL::rcs(par) + rr * 32 + rh * 16) = make_uint4(c[0], c[1], c[2], c[3]);
       if (rvalid) *reinterpret_cast<uint16_t*>(j.row_scales + (e >> 4)) = (uint16_t)sc;
     };
     // rowwise scales, codes and stores of the thread's two blocks, table path
@@ -427,11 +421,6 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = umax(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       if (lane == 0) red[warp * 32] = m;
-    } else if (LOF == LO_NONE) {  // the rowwise pass needs nothing from other warps: done here
-      row_fast(a, ram, unit_amax<UE5M3>(), 0ull, 0ull);
-    } else if (LOF == LO_UNIFORM) {
-      if (u_fast) row_fast(a, ram, A_u, ZH_u, ZL_u);
-      else row_slow(a, ram, S_u, R_u);
     }
     // 1 x 64 (after the barrier): the row's 64 columns are this thread's two
     // blocks and its partner's
@@ -478,7 +467,14 @@ __global__ void __launch_bounds__(LT, row_tma(LOF) ? 3 : 4) ctl_kernel(const Qua
     if (have_prev) store_prev(par ^ 1);
 
     // ---------------------------------------- after the barrier: registers and staging only
-    if (LOF == LO_1D) row_1d();
+    if (LOF == LO_1D) {
+      row_1d();
+    } else if (LOF == LO_NONE) {
+      row_fast(a, ram, unit_amax<UE5M3>(), 0ull, 0ull);
+    } else if (LOF == LO_UNIFORM) {
+      if (u_fast) row_fast(a, ram, A_u, ZH_u, ZL_u);
+      else row_slow(a, ram, S_u, R_u);
+    }
     uint32_t A2 = 0;  // the 64 x 64 block's amax (2-D): both orientations
     float S2f = 1.0f;
     uint64_t ZH2 = 0ull, ZL2 = 0ull;
@@ -600,7 +596,7 @@ template <bool UE5M3, int LOF, bool GR>
 cudaError_t launch_ctl_t(const QuantJob& j, const CUtensorMap& map, const CUtensorMap& cmap, const CUtensorMap& rmap,
                          const CUtensorMap& rmap64, cudaStream_t st) {
   auto kern = ctl_kernel<UE5M3, LOF, GR>;
-  constexpr int smem = LLT<row_tma(LOF)>::total;
+  constexpr int smem = LL::total;
   static int per_sm_cache[128] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -674,11 +670,11 @@ bool launch_ctl(const QuantJob& j, cudaStream_t st, cudaError_t* err) {
   else if (j.mode == 1 && j.s_src == S_TENSORWISE_WS) lof = LO_UNIFORM;  // tensorwise, from the workspace amax
   else if (j.s_src == S_IN_TILE && j.ob == 64) lof = j.outer_2d ? LO_2D : LO_1D;
   else return false;
-  if (gr && !row_tma(lof)) return false;
+  if (gr && lof != LO_1D && lof != LO_2D) return false;
   if (getenv_flag("FP4Q_NO_CTL_KERNEL")) return false;
   CUtensorMap map, cmap = {}, rmap = {}, rmap64 = {};
   if (!make_bf16_tile_map(j, &map, LM) || (!gr && !make_col_map(j, &cmap))) return false;
-  if (row_tma(lof) && (!make_row_map(j, &rmap, LM) || (gr && !make_row_map(j, &rmap64, 64)))) return false;
+  if (!make_row_map(j, &rmap, LM) || (gr && !make_row_map(j, &rmap64, 64))) return false;
   *err = j.ue5m3 ? launch_ctl_f<true>(j, lof, map, cmap, rmap, rmap64, st)
                  : launch_ctl_f<false>(j, lof, map, cmap, rmap, rmap64, st);
   return true;
