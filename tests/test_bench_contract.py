@@ -34,3 +34,26 @@ def test_reference_arm_prints_one_line_with_the_contract_keys():
 def test_reference_arm_other_ranks_exit_quietly():
     out = _run({"RANK": "1", "WORLD_SIZE": "2"})
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_oracle_pool_matches_one_process():
+    """The all-cores CPU baseline runs the oracle unchanged on row slices:
+    the slices' outputs add up to the output of one call on every row."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from block_scaled_fp4_quantize_gb300 import workloads as W
+
+    x = W.lognormal((96, 256), 61, sigma=3.0).view(__import__("torch").int16).numpy().view(np.uint16)
+    pool = bench.OraclePool(x, cores=3)
+    try:
+        pool.run(96)
+        got = pool.checksum
+        pool.run(50)  # a leading part, uneven slices
+        part = pool.checksum
+    finally:
+        pool.close()
+    assert got == int(oracle.mxfp4_fake_quantize(x).view("u2").sum(dtype="u8"))
+    assert part == int(oracle.mxfp4_fake_quantize(x[:50]).view("u2").sum(dtype="u8"))
