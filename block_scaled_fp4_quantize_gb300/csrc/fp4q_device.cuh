@@ -295,6 +295,13 @@ __device__ __forceinline__ uint32_t enc_e4m3_hw(float v) {
   return r & 0xFFu;
 }
 
+// One 256-bit store (p 32-byte aligned): a lane fills a whole 32-byte sector.
+__device__ __forceinline__ void st256(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Packed binary32 pairs (f32x2, one 64-bit register): two lanes of the same
 // IEEE operation per instruction, round to nearest even, subnormals kept.

@@ -251,7 +251,11 @@ __global__ void __launch_bounds__(256) outer_2d_kernel(const QuantJob j) {
 // function of the flat block index b (codes at 8 b, scale at b, a 1 x ob
 // outer scale at 16 b / ob), so there is no division.  One thread per
 // microblock, two in flight per thread; OUTER: 0 none, 1 one scale, 2 1-D.
-template <bool OUT_BF16, int OUTER>
+// W32: y is 32-byte aligned and each microblock's output leaves in 256-bit
+// stores, so a warp's store instruction fills whole 32-byte sectors (two
+// 16-byte stores a lane 32 bytes apart each fill half of every sector, and
+// the sectors went to L2 twice).
+template <bool OUT_BF16, int OUTER, bool W32>
 __global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
   pdl_wait_then_release();
   const ScaleFmt f = scale_fmt(j.ue5m3);
@@ -291,10 +295,21 @@ __global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
         v[2 * i + 1] = d1;
         w[i] = pack_bf16x2(d0, d1);
       }
-      if (OUT_BF16) {
+      if (OUT_BF16 && W32) {
+        st256(static_cast<uint16_t*>(j.y) + b * 16, w);
+      } else if (OUT_BF16) {
         uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + b * 16);
         __stcs(p, make_uint4(w[0], w[1], w[2], w[3]));
         __stcs(p + 1, make_uint4(w[4], w[5], w[6], w[7]));
+      } else if (W32) {
+        float* p = static_cast<float*>(j.y) + b * 16;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t u[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) u[i] = fbits(v[8 * h + i]);
+          st256(p + 8 * h, u);
+        }
       } else {
         float4* p = reinterpret_cast<float4*>(static_cast<float*>(j.y) + b * 16);
 #pragma unroll
@@ -427,11 +442,20 @@ cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st) {
   const int vec = vec_aligned(j.y, 16);
   if (vec && !j.sl.mma && !(j.mode == 2 && j.outer_2d) && (reinterpret_cast<uintptr_t>(j.codes) & 7u) == 0) {
     const int grid = grid_for((nmb + 1) / 2, 256, 8);
+    const bool w32 = (reinterpret_cast<uintptr_t>(j.y) & 31u) == 0;
     void (*kern)(const DequantJob) =
-        j.out_bf16 ? (j.mode == 0 ? dequant_flat_kernel<true, 0> : j.mode == 1 ? dequant_flat_kernel<true, 1>
-                                                                                 : dequant_flat_kernel<true, 2>)
-                   : (j.mode == 0 ? dequant_flat_kernel<false, 0> : j.mode == 1 ? dequant_flat_kernel<false, 1>
-                                                                                  : dequant_flat_kernel<false, 2>);
+        w32 ? (j.out_bf16 ? (j.mode == 0   ? dequant_flat_kernel<true, 0, true>
+                             : j.mode == 1 ? dequant_flat_kernel<true, 1, true>
+                                           : dequant_flat_kernel<true, 2, true>)
+                          : (j.mode == 0   ? dequant_flat_kernel<false, 0, true>
+                             : j.mode == 1 ? dequant_flat_kernel<false, 1, true>
+                                           : dequant_flat_kernel<false, 2, true>))
+            : (j.out_bf16 ? (j.mode == 0   ? dequant_flat_kernel<true, 0, false>
+                             : j.mode == 1 ? dequant_flat_kernel<true, 1, false>
+                                           : dequant_flat_kernel<true, 2, false>)
+                          : (j.mode == 0   ? dequant_flat_kernel<false, 0, false>
+                             : j.mode == 1 ? dequant_flat_kernel<false, 1, false>
+                                           : dequant_flat_kernel<false, 2, false>));
     return launch_pdl(kern, dim3((unsigned)grid), dim3(256), 0, st, j);
   }
   const int grid = grid_for(nmb, 256, 8);

@@ -39,11 +39,6 @@ __device__ __forceinline__ U32B ld256_stream(const void* p) {
                : "l"(p));
   return r;
 }
-__device__ __forceinline__ void st256(void* p, const uint32_t (&w)[8]) {
-  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
 
 template <typename TI>
 struct InTraits;

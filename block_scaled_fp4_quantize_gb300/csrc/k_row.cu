@@ -46,11 +46,6 @@ __device__ __forceinline__ void ld256_rw(const void* p, uint32_t (&a)[8]) {
                : "l"(p)
                : "memory");
 }
-__device__ __forceinline__ void st256(void* p, const uint32_t (&a)[8]) {
-  asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]),
-               "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
-               : "memory");
-}
 
 template <bool IN_BF16>
 struct Raw {

@@ -176,6 +176,29 @@ def test_dequantize_ragged_counts(orc, kw, shape, out_dtype):
                          mode=okw["mode"], ob=okw["ob"], outer_2d=False, fmt=okw["fmt"])
     assert_same({"y": host_np(y)}, {"y": ref})
 
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("offset_bytes", [16, 32], ids=["16B", "32B"])
+def test_dequantize_into_offset_output(orc, out_dtype, offset_bytes):
+    """An output 16 bytes past a 32-byte boundary takes the 16-byte stores,
+    one 32 bytes past it the 256-bit stores; both give the oracle's bits."""
+    G, M, K = 1, 96, 256
+    kw = dict(mode="outer_block", outer_block_size=64)
+    x = W.lognormal((G, M, K), 27, sigma=2.5)
+    q, g = gpu_quantize(x, rowwise=True, columnwise=False, **kw)
+    es = 2 if out_dtype == torch.bfloat16 else 4
+    buf = torch.full((G * M * K + 64,), float("nan"), dtype=out_dtype, device="cuda")
+    off = offset_bytes // es
+    y = buf[off:off + G * M * K].view(G, M, K)
+    assert y.data_ptr() % 32 == (offset_bytes % 32)
+    fq.dequantize(q, orient="row", out_dtype=out_dtype, out=y)
+    okw = oracle_kw(kw)
+    ref = orc.dequantize(g["row_codes"], g["row_scales"], g, G=G, M=M, K=K, orient=ROW,
+                         out_dtype="bf16" if out_dtype == torch.bfloat16 else "fp32",
+                         mode=okw["mode"], ob=okw["ob"], outer_2d=False, fmt=okw["fmt"])
+    assert_same({"y": host_np(y)}, {"y": ref})
+    assert torch.isnan(buf[:off].float()).all() and torch.isnan(buf[off + G * M * K:].float()).all()
+
+
 def test_precomputed_outer_scale_round_trip(orc):
     x = W.activations(M=128, K=256, n_cols=2, n_rows=1)
     for kw in (dict(mode="outer_block", outer_block_size=64, outer_2d=True),
