@@ -131,22 +131,37 @@ __device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32]
   // projected values y = e2m1(q) 2^E (exact), recomputed from the codes
   // for each output so that no 32-value array stays live
   const int64_t n = (g * M + m) * K + k;  // element index of the block in the [G, M, K] outputs
+  // a lane's 64 bytes of projection and 32 of rowwise codes leave in 256-bit
+  // stores (whole 32-byte sectors) when both outputs are 32-byte aligned
+  const bool w32 = ((reinterpret_cast<uintptr_t>(j.y) | reinterpret_cast<uintptr_t>(j.row_codes)) & 31u) == 0;
   if (j.y || j.col_codes) {
     const uint64_t SC2 = pk2(sc, sc);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w[4];
+    for (int qq = 0; qq < 2; ++qq) {
+      uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float g0, g1;
-        e2m1x2_decode(qb[4 * q + i], g0, g1);
-        upk2(mul2(pk2(g0, g1), SC2), g0, g1);
-        w[i] = poison ? 0x7FC07FC0u : pack_bf16x2(g0, g1);
+      for (int h = 0; h < 2; ++h) {
+        const int q = 2 * qq + h;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float g0, g1;
+          e2m1x2_decode(qb[4 * q + i], g0, g1);
+          upk2(mul2(pk2(g0, g1), SC2), g0, g1);
+          w[4 * h + i] = poison ? 0x7FC07FC0u : pack_bf16x2(g0, g1);
+        }
+        if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
+          *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ ys_swz(rr)) << 4)) =
+              make_uint4(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
       }
-      if (j.col_codes)  // staged as bf16 (exact; NaN for a poisoned block)
-        *reinterpret_cast<uint4*>(ys + rr * YS + (((4 * rh + q) ^ ys_swz(rr)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      if (j.y && OUT_BF16) reinterpret_cast<uint4*>(static_cast<uint16_t*>(j.y) + n)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      if (j.y && OUT_BF16) {
+        uint16_t* d = static_cast<uint16_t*>(j.y) + n + 16 * qq;
+        if (w32) {
+          st256(d, w);
+        } else {
+          reinterpret_cast<uint4*>(d)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(d)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
     }
     if (j.y && !OUT_BF16) {
       float4* d = reinterpret_cast<float4*>(static_cast<float*>(j.y) + n);
@@ -176,9 +191,13 @@ __device__ __forceinline__ void row_work(const QuantJob& j, const float (&v)[32]
               (e4m3x2_f16x2_scaled(e2m1x2_f16x2(qb[2 * i + 1]), P2) << 16);
       if (poison) cw[i] = 0x7F7F7F7Fu;
     }
-    uint4* d = reinterpret_cast<uint4*>(j.row_codes + n);
-    d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    if (w32) {
+      st256(j.row_codes + n, cw);
+    } else {
+      uint4* d = reinterpret_cast<uint4*>(j.row_codes + n);
+      d[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      d[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    }
     j.row_scales[n / 32] = poison ? (uint8_t)0xFF : (uint8_t)(X + 127);
   }
 }

@@ -75,3 +75,22 @@ def test_more_tiles_than_resident_ctas(orc):
     # CTAs, with a half-filled last tile column
     x = W.lognormal((2, 2048, 2080), 83, sigma=4.0)
     _check(orc, x)
+
+
+def test_outputs_16_bytes_past_a_32_byte_boundary(orc):
+    """Projection and rowwise codes 16 bytes past a 32-byte boundary take the
+    16-byte stores (32-byte aligned ones the 256-bit stores); same bits."""
+    G, M, K = 1, 96, 256
+    x = W.lognormal((G, M, K), 84, sigma=4.0)
+    n = G * M * K
+    ybuf = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+    cbuf = torch.empty(n + 32, dtype=torch.uint8, device="cuda")
+    out = fq.MXFP8Pair()
+    out.y = ybuf[8:8 + n].view(G, M, K)
+    out.row_codes = cbuf[16:16 + n].view(G, M, K)
+    out.row_scales = torch.empty(G, M, K // 32, dtype=torch.uint8, device="cuda")
+    assert out.y.data_ptr() % 32 == 16 and out.row_codes.data_ptr() % 32 == 16
+    q = fq.mxfp4_project_mxfp8(x.cuda(), columnwise=False, with_y=True, out=out)
+    ref = orc.mxfp4_project_mxfp8(host_np(x), out_dtype="bf16", out_mask=1)
+    assert_same({k: host_np(getattr(q, k)) for k in ("y", "row_codes", "row_scales")},
+                {k: ref[k] for k in ("y", "row_codes", "row_scales")})
