@@ -192,19 +192,28 @@ def _warm(fn, warmup, min_seconds=0.5):
 
 
 class StepGraph:
-    """`fn(i)` for i = 0 .. n-1 captured as CUDA graphs: one graph of up to
-    `chunk` consecutive calls replayed as often as needed, plus one graph
-    for the remainder, so that exactly n calls run.  The replays enqueue the
-    same kernels the eager calls do, without the Python launch path between
-    them (host-side hiccups then cannot leave the GPU idle inside the timed
-    region).  `ok` is False when capture failed (run eagerly then)."""
+    """`fn(i)` for i = 0 .. n-1 captured as CUDA graphs (a head graph of up to
+    `chunk` calls, a body graph of `chunk` calls replayed as often as needed,
+    a tail graph of the rest), so that exactly n calls run.  The replays
+    enqueue the same kernels the eager calls do, without the Python launch
+    path between them (host-side hiccups then cannot leave the GPU idle
+    inside the timed region).  The two timing events are nodes of the head
+    and tail graphs (external events): the region they bound is the n
+    calls' execution on the GPU, not the host's submission of the first
+    graph to an idle GPU.  Where the events cannot be captured they are
+    recorded around the replays (`inside` False); where nothing can be
+    captured the calls run eagerly (`ok` False)."""
 
     def __init__(self, fn, n, chunk=100):
         import torch
 
-        self.fn, self.n, self.ok = fn, n, False
+        self.fn, self.n, self.ok, self.inside = fn, n, False, False
         self.chunk = max(1, min(n, chunk))
-        self.reps, rem = divmod(n, self.chunk)
+        # head: calls 0 .. h-1; body: `nb` replays of `chunk` calls; tail: the rest (>= 1 when n > chunk)
+        self.h = self.chunk
+        rest = n - self.h
+        self.nb = (rest - 1) // self.chunk if rest > 0 else 0
+        self.t = rest - self.nb * self.chunk
         try:
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())
@@ -213,31 +222,63 @@ class StepGraph:
                     fn(i)
             torch.cuda.current_stream().wait_stream(s)
             torch.cuda.synchronize()
-            self.g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(self.g):
-                for i in range(self.chunk):
-                    fn(i)
-            self.r = None
-            if rem:
-                self.r = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(self.r):
-                    for i in range(rem):
-                        fn(self.reps * self.chunk + i)
+            try:
+                self.e0 = torch.cuda.Event(enable_timing=True, external=True)
+                self.e1 = torch.cuda.Event(enable_timing=True, external=True)
+                self._capture(True)
+                self.inside = True
+            except Exception:  # noqa: BLE001 -- no event nodes in graphs here: events around the replays
+                torch.cuda.synchronize()
+                self.e0, self.e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                self._capture(False)
             torch.cuda.synchronize()
             self.ok = True
         except Exception as e:  # noqa: BLE001 -- any capture failure falls back to eager calls
             self.error = repr(e)[:200]
             torch.cuda.synchronize()
+            self.e0, self.e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def _capture(self, events):
+        import torch
+
+        def graph(first, count, head, tail):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                if head and events:
+                    self.e0.record()
+                for i in range(count):
+                    self.fn(first + i)
+                if tail and events:
+                    self.e1.record()
+            return g
+
+        self.gh = graph(0, self.h, True, self.t == 0)
+        self.gb = graph(self.h, self.chunk, False, False) if self.nb else None
+        self.gt = graph(self.h + self.nb * self.chunk, self.t, False, True) if self.t else None
 
     def run(self):
         if not self.ok:
             for i in range(self.n):
                 self.fn(i)
             return
-        for _ in range(self.reps):
-            self.g.replay()
-        if self.r is not None:
-            self.r.replay()
+        self.gh.replay()
+        for _ in range(self.nb):
+            self.gb.replay()
+        if self.gt is not None:
+            self.gt.replay()
+
+    def timed(self):
+        """Run the n calls as the timed region; ms of the region (call after
+        a device synchronize)."""
+        import torch
+
+        if not (self.ok and self.inside):
+            self.e0.record()
+        self.run()
+        if not (self.ok and self.inside):
+            self.e1.record()
+        torch.cuda.synchronize()
+        return self.e0.elapsed_time(self.e1)
 
 
 def _events_time(fn, iters, warmup, graph=True):
@@ -247,13 +288,16 @@ def _events_time(fn, iters, warmup, graph=True):
     import torch
 
     sg = StepGraph(fn, iters) if graph else None
-    run = sg.run if sg is not None and sg.ok else (lambda: [fn(i) for i in range(iters)])
-    _warm(lambda i: run() if sg is not None and sg.ok else fn(i), warmup if sg is None or not sg.ok else 1,
-          min_seconds=0.3)
+    if sg is not None and sg.ok:
+        _warm(lambda i: sg.run(), 1, min_seconds=0.3)
+        torch.cuda.synchronize()
+        return sg.timed() / iters
+    _warm(fn, warmup, min_seconds=0.3)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    run()
+    for i in range(iters):
+        fn(i)
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / iters
@@ -452,14 +496,10 @@ def run_ours(args, dist):
     _warm(step, args.warmup, min_seconds=0.5)
     dist.barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    sg.run()
-    ev1.record()
-    torch.cuda.synchronize()
+    ms_region = sg.timed()  # synchronizes the device at its end
     dist.barrier()
     t1 = time.time()
-    ms_total = dist.max(ev0.elapsed_time(ev1))
+    ms_total = dist.max(ms_region)
     clocks = sampler.stop(t0, t1) if sampler else None
     ms_step = ms_total / args.steps
     value = MXFP4_BYTES * dist.world / (ms_step * 1e-3) / 1e9
@@ -506,8 +546,9 @@ def run_ours(args, dist):
         "config": {"workload": "mxfp4_weight: MXFP4 fake-quantize bf16[8192,8192] ~N(0,0.02), 0.1% edge blocks, "
                                "bf16 out", "shape": [8192, 8192], "bytes_per_step": MXFP4_BYTES,
                    "l2": "2 rotating input/output sets (537 MB > L2)", "parallelism": "replicas" if dist.world > 1 else "none",
-                   "timing": "CUDA events around K steps run as CUDA graph replays" if sg.ok else
-                             "CUDA events around K eager steps",
+                   "timing": ("CUDA events as the first and last nodes of the K steps' CUDA graphs" if sg.ok and sg.inside
+                              else "CUDA events around K steps run as CUDA graph replays" if sg.ok
+                              else "CUDA events around K eager steps"),
                    "warmup_policy": "at least W steps and 0.5 s of steps, no idle gap before the timed region"},
         "roofline": {"bound": "hbm", "achieved": round(kernel_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(kernel_gbs / peak, 4), "peak_source": peak_src,
