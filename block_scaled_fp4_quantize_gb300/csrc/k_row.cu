@@ -258,7 +258,8 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // in its range: the table image arrives by one more bulk copy, and per value
 // pair the codes cost two packed multiplies; the general per-block steps
 // then take their inner-scale entries computed on demand.
-template <bool UE5M3, int RO>
+// OB64: the outer block is 1 x 64 (four lanes), a compile-time constant.
+template <bool UE5M3, int RO, bool OB64 = false>
 __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
   constexpr bool PAIR = RO == RO_WARP || RO == RO_UNIFORM;
   __shared__ __align__(128) unsigned char buf[QS][QB * 32];
@@ -304,9 +305,9 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
   } tv{tab};
   const unsigned char* ptb = img;
   const uint32_t* ctab = reinterpret_cast<const uint32_t*>(PAIR ? img + 10240 : img);
-  const int per = RO == RO_WARP || RO == RO_BUFFER ? j.ob / 16 : 1;
+  const int per = OB64 ? 4 : RO == RO_WARP || RO == RO_BUFFER ? j.ob / 16 : 1;
   const bool per_pow2 = (per & (per - 1)) == 0;
-  const int lper = 31 - __clz(per);
+  const int lper = OB64 ? 2 : 31 - __clz(per);
   float S_u = 1.0f, r_u = 1.0f;
   uint32_t A_u = 0;  // the tensorwise amax, when it is computed here (bf16 input: a bf16 value)
   if (RO == RO_UNIFORM) {
@@ -420,9 +421,9 @@ __global__ void __launch_bounds__(RT) row_bulk_kernel(const QuantJob j) {
   }
 }
 
-template <bool UE5M3, int RO>
+template <bool UE5M3, int RO, bool OB64 = false>
 cudaError_t launch_row_bulk_t(const QuantJob& j, cudaStream_t st) {
-  auto kern = row_bulk_kernel<UE5M3, RO>;
+  auto kern = row_bulk_kernel<UE5M3, RO, OB64>;
   static int per_sm_cache[128] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -442,7 +443,8 @@ template <bool UE5M3>
 cudaError_t launch_row_bulk_o(const QuantJob& j, cudaStream_t st) {
   if (j.s_src == S_ONE) return launch_row_bulk_t<UE5M3, RO_NONE>(j, st);
   if (j.s_src == S_TENSORWISE_WS || j.mode == 1) return launch_row_bulk_t<UE5M3, RO_UNIFORM>(j, st);
-  if (j.s_src == S_IN_TILE) return launch_row_bulk_t<UE5M3, RO_WARP>(j, st);
+  if (j.s_src == S_IN_TILE)
+    return j.ob == 64 ? launch_row_bulk_t<UE5M3, RO_WARP, true>(j, st) : launch_row_bulk_t<UE5M3, RO_WARP>(j, st);
   return launch_row_bulk_t<UE5M3, RO_BUFFER>(j, st);
 }
 
