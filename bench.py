@@ -191,6 +191,16 @@ def _warm(fn, warmup, min_seconds=0.5):
     return i
 
 
+def graph_split(n, chunk=100):
+    """(head, body replays, body size, tail) of n calls: head = min(n,
+    chunk) calls, then `body replays` x `body size` calls, then a tail of
+    1 .. chunk calls (0 when n <= chunk); the parts add up to n."""
+    ch = max(1, min(n, chunk))
+    rest = n - ch
+    nb = (rest - 1) // ch if rest > 0 else 0
+    return ch, nb, ch, rest - nb * ch
+
+
 class StepGraph:
     """`fn(i)` for i = 0 .. n-1 captured as CUDA graphs (a head graph of up to
     `chunk` calls, a body graph of `chunk` calls replayed as often as needed,
@@ -208,12 +218,8 @@ class StepGraph:
         import torch
 
         self.fn, self.n, self.ok, self.inside = fn, n, False, False
-        self.chunk = max(1, min(n, chunk))
         # head: calls 0 .. h-1; body: `nb` replays of `chunk` calls; tail: the rest (>= 1 when n > chunk)
-        self.h = self.chunk
-        rest = n - self.h
-        self.nb = (rest - 1) // self.chunk if rest > 0 else 0
-        self.t = rest - self.nb * self.chunk
+        self.h, self.nb, self.chunk, self.t = graph_split(n, chunk)
         try:
             s = torch.cuda.Stream()
             s.wait_stream(torch.cuda.current_stream())

@@ -57,3 +57,20 @@ def test_oracle_pool_matches_one_process():
         pool.close()
     assert got == int(oracle.mxfp4_fake_quantize(x).view("u2").sum(dtype="u8"))
     assert part == int(oracle.mxfp4_fake_quantize(x[:50]).view("u2").sum(dtype="u8"))
+
+
+def test_graph_split_covers_every_call_once():
+    """The timed calls are split into a head graph (holding the start event),
+    replays of a body graph and a tail graph (holding the end event): the
+    parts add up to n, the tail is 1 .. chunk calls when n > chunk, and a
+    single graph holds both events otherwise."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for n in list(range(1, 420)) + [25000]:
+        for chunk in (1, 7, 100):
+            h, nb, ch, t = bench.graph_split(n, chunk)
+            assert h + nb * ch + t == n
+            assert h == min(n, chunk) and ch == min(n, chunk)
+            assert (t == 0) == (n <= chunk)
+            assert t == 0 or 1 <= t <= chunk
