@@ -250,11 +250,12 @@ __global__ void __launch_bounds__(256) outer_2d_kernel(const QuantJob j) {
 // Dequantize, linear scales without 2-D outer blocks: every index is a
 // function of the flat block index b (codes at 8 b, scale at b, a 1 x ob
 // outer scale at 16 b / ob), so there is no division.  One thread per
-// microblock, two in flight per thread; OUTER: 0 none, 1 one scale, 2 1-D.
+// microblock, DQ_IN_FLIGHT in flight per thread; OUTER: 0 none, 1 one scale, 2 1-D.
 // W32: y is 32-byte aligned and each microblock's output leaves in 256-bit
 // stores, so a warp's store instruction fills whole 32-byte sectors (two
 // 16-byte stores a lane 32 bytes apart each fill half of every sector, and
 // the sectors went to L2 twice).
+constexpr int DQ_IN_FLIGHT = 4;  // microblocks per thread in flight (8 measured slower)
 template <bool OUT_BF16, int OUTER, bool W32>
 __global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
   pdl_wait_then_release();
@@ -264,12 +265,14 @@ __global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
   const bool pow2 = j.ob > 0 && (j.ob & (j.ob - 1)) == 0;
   const float S1 = OUTER == 1 ? j.outer[0] : 1.0f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b0 < nmb; b0 += 2 * stride) {
-    uint2 cw[2];
-    uint32_t sb[2];
-    float S[2] = {S1, S1};
+  for (int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b0 < nmb; b0 += DQ_IN_FLIGHT * stride) {
+    uint2 cw[DQ_IN_FLIGHT];
+    uint32_t sb[DQ_IN_FLIGHT];
+    float S[DQ_IN_FLIGHT];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < DQ_IN_FLIGHT; ++q) S[q] = S1;
+#pragma unroll
+    for (int q = 0; q < DQ_IN_FLIGHT; ++q) {
       const int64_t b = b0 + q * stride;
       if (b < nmb) {
         cw[q] = __ldcs(reinterpret_cast<const uint2*>(j.codes) + b);
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(256) dequant_flat_kernel(const DequantJob j) {
       }
     }
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < DQ_IN_FLIGHT; ++q) {
       const int64_t b = b0 + q * stride;
       if (b >= nmb) continue;
       const float s = dec_scale(sb[q], f);
@@ -441,7 +444,7 @@ cudaError_t launch_dequant(const DequantJob& j, cudaStream_t st) {
   const int64_t nmb = j.G * j.R * (j.C / 16);
   const int vec = vec_aligned(j.y, 16);
   if (vec && !j.sl.mma && !(j.mode == 2 && j.outer_2d) && (reinterpret_cast<uintptr_t>(j.codes) & 7u) == 0) {
-    const int grid = grid_for((nmb + 1) / 2, 256, 8);
+    const int grid = grid_for((nmb + DQ_IN_FLIGHT - 1) / DQ_IN_FLIGHT, 256, 8);
     const bool w32 = (reinterpret_cast<uintptr_t>(j.y) & 31u) == 0;
     void (*kern)(const DequantJob) =
         w32 ? (j.out_bf16 ? (j.mode == 0   ? dequant_flat_kernel<true, 0, true>
